@@ -1,0 +1,172 @@
+"""fp64 CPU oracle for Kimi Delta Attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+import this package.  The CUDA library never links or calls it, and it shares
+no code with it.
+
+The arithmetic lives in ``kda_oracle.c`` (plain C, fp64, token by token); this
+module compiles it with gcc on first use and marshals numpy arrays through
+ctypes.  See the C file's header for what is computed and which page passage
+each part follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "libkda_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ERRORS = {0: "ok", -1: "invalid argument", -2: "state index out of range",
+          -3: "checkpoint capacity too small", -4: "out of memory"}
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/libkda_oracle.so``."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            lib.kda_oracle_prefill.restype = ctypes.c_int
+            lib.kda_oracle_prefill.argtypes = [
+                P, P, P, P, P, P, ctypes.c_int, P, P, ctypes.c_int64, P, P, ctypes.c_int,
+                ctypes.c_int64, P, P, P, ctypes.c_double, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_double, ctypes.c_int]
+            lib.kda_oracle_decode.restype = ctypes.c_int
+            lib.kda_oracle_decode.argtypes = [
+                P, P, P, P, P, P, ctypes.c_int, P, ctypes.c_int64, P, P, P, ctypes.c_double,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int]
+            lib.kda_oracle_norm_gate.restype = ctypes.c_int
+            lib.kda_oracle_norm_gate.argtypes = [P, P, P, ctypes.c_double, P, ctypes.c_int64,
+                                                 ctypes.c_int]
+            lib.kda_oracle_checkpoint_offsets.restype = ctypes.c_int64
+            lib.kda_oracle_checkpoint_offsets.argtypes = [P, ctypes.c_int, ctypes.c_int, P]
+            lib.kda_oracle_max_threads.restype = ctypes.c_int
+            lib.kda_oracle_max_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _f64(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # a torch tensor: widen exactly on the CPU
+        a = a.detach().cpu().double().numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _i32(a):
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc):
+    if rc != 0:
+        raise OracleError(ERRORS.get(rc, f"error {rc}"))
+
+
+def max_threads() -> int:
+    return _load().kda_oracle_max_threads()
+
+
+def checkpoint_offsets(cu_seqlens, every: int) -> np.ndarray:
+    """Exclusive prefix sum of floor(len_i / every) over the sequences ([N+1])."""
+    cu = _i32(cu_seqlens)
+    n = cu.shape[0] - 1
+    offs = np.zeros(n + 1, np.int32)
+    total = _load().kda_oracle_checkpoint_offsets(_ptr(cu), n, int(every), _ptr(offs))
+    if total < 0:
+        raise OracleError("malformed cu_seqlens")
+    return offs
+
+
+def prefill(q, k, v, g, beta, cu_seqlens, state_indices, pool, *, checkpoint_every=0,
+            gate=None, norm_w=None, eps=1e-6, scale=None, nthreads=0):
+    """Token-by-token KDA prefill in fp64.
+
+    Shapes: q,k,g [T,H,dk]; v [T,H,dv]; beta [T,H]; cu_seqlens [N+1];
+    state_indices [N]; pool [num_slots,H,dk,dv].  Returns
+    ``(out [T,H,dv], pool_after [num_slots,H,dk,dv], checkpoints [n,H,dk,dv],
+    ckpt_offsets [N+1])``.  The input pool is not modified.
+    """
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    cu, idx = _i32(cu_seqlens), _i32(state_indices)
+    pool = _f64(pool).copy()
+    gate, norm_w = _f64(gate), _f64(norm_w)
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = idx.shape[0]
+    if scale is None or scale <= 0:
+        scale = 1.0 / np.sqrt(dk)
+    offs = checkpoint_offsets(cu, checkpoint_every) if N > 0 else np.zeros(1, np.int32)
+    n_ck = int(offs[-1])
+    ck = np.zeros((max(n_ck, 1), H, dk, dv), np.float64)
+    out = np.zeros((T, H, dv), np.float64)
+    offs_out = np.zeros(N + 1, np.int32)
+    rc = _load().kda_oracle_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu), N, _ptr(idx), _ptr(pool),
+        pool.shape[0], _ptr(out), _ptr(ck), int(checkpoint_every), ck.shape[0], _ptr(offs_out),
+        _ptr(gate), _ptr(norm_w), float(eps), H, dk, dv, float(scale), int(nthreads))
+    _check(rc)
+    return out, pool, ck[:n_ck], offs_out
+
+
+def decode(q, k, v, g, beta, state_indices, pool, *, gate=None, norm_w=None, eps=1e-6,
+           scale=None, nthreads=0):
+    """One recurrent decode step in fp64.  q,k,g [N,H,dk]; v [N,H,dv]; beta [N,H].
+
+    Returns ``(out [N,H,dv], pool_after)``; the input pool is not modified.
+    """
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    idx = _i32(state_indices)
+    pool = _f64(pool).copy()
+    gate, norm_w = _f64(gate), _f64(norm_w)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if scale is None or scale <= 0:
+        scale = 1.0 / np.sqrt(dk)
+    out = np.zeros((N, H, dv), np.float64)
+    rc = _load().kda_oracle_decode(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(idx), N, _ptr(pool), pool.shape[0],
+        _ptr(out), _ptr(gate), _ptr(norm_w), float(eps), H, dk, dv, float(scale), int(nthreads))
+    _check(rc)
+    return out, pool
+
+
+def norm_gate(o, gate, w, eps=1e-6):
+    """y = o / sqrt(mean(o^2)+eps) * w * sigmoid(gate) over the last dimension."""
+    o, gate, w = _f64(o), _f64(gate), _f64(w)
+    dv = o.shape[-1]
+    rows = o.size // dv
+    y = np.zeros_like(o)
+    _check(_load().kda_oracle_norm_gate(_ptr(o), _ptr(gate), _ptr(w), float(eps), _ptr(y),
+                                        rows, dv))
+    return y

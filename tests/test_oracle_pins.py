@@ -1,0 +1,359 @@
+"""Pins for the fp64 oracle: each test checks it against something other than
+itself -- a hand-worked example, a closed form, an invariant, brute force on
+tiny inputs, or the independent chunk-form evaluation.  CPU only."""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from chunk_mirror import chunk_prefill
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *nums = line.split()
+            vals[key] = np.array([float(x) for x in nums])
+    return vals
+
+
+def _rand_inputs(rng, T, H, dk, dv, *, unit=True):
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    if unit:
+        q /= np.linalg.norm(q, axis=-1, keepdims=True)
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, dv))
+    g = -np.log1p(np.exp(rng.standard_normal((T, H, dk))))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((T, H))))
+    return q, k, v, g, beta
+
+
+def _one_seq(T):
+    return np.array([0, T], np.int32), np.array([0], np.int32)
+
+
+# ---------------------------------------------------------------- worked example
+def test_hand_worked_example_d2():
+    gd = _read_golden("worked_example_d2.txt")
+    q = np.stack([gd["q1"], gd["q2"]])[:, None, :]
+    k = np.stack([gd["k1"], gd["k2"]])[:, None, :]
+    v = np.stack([gd["v1"], gd["v2"]])[:, None, :]
+    g = np.stack([gd["g1"], gd["g2"]])[:, None, :]
+    beta = np.array([gd["b1"][0], gd["b2"][0]])[:, None]
+    pool = gd["s0"].reshape(1, 1, 2, 2)
+    cu, idx = _one_seq(2)
+    out, pool_after, ck, offs = oracle.prefill(q, k, v, g, beta, cu, idx, pool,
+                                               checkpoint_every=1, scale=1.0)
+    np.testing.assert_allclose(out[0, 0], gd["o1"], atol=1e-12)
+    np.testing.assert_allclose(out[1, 0], gd["o2"], atol=1e-12)
+    np.testing.assert_allclose(ck[0, 0].ravel(), gd["s1"], atol=1e-12)
+    np.testing.assert_allclose(ck[1, 0].ravel(), gd["s2"], atol=1e-12)
+    np.testing.assert_allclose(pool_after[0, 0].ravel(), gd["s2"], atol=1e-12)
+    assert offs.tolist() == [0, 2]
+
+
+def test_hand_worked_norm_gate():
+    gd = _read_golden("norm_gate_example.txt")
+    y = oracle.norm_gate(gd["o"][None], gd["gate"][None], gd["w"], eps=gd["eps"][0])
+    np.testing.assert_allclose(y[0], gd["y"], atol=1e-12)
+
+
+# ---------------------------------------------------------------- brute force
+def _brute_force(q, k, v, g, beta, S0, scale):
+    """Materialise each transition M_t = (I - b k k^T) Diag(exp g) as a dense
+    matrix and multiply: S_t = M_t S_{t-1} + b k v^T, o_t = scale S_t^T q_t."""
+    T, dk = q.shape
+    S = S0.copy()
+    outs, states = [], []
+    for t in range(T):
+        M = (np.eye(dk) - beta[t] * np.outer(k[t], k[t])) @ np.diag(np.exp(g[t]))
+        S = M @ S + beta[t] * np.outer(k[t], v[t])
+        outs.append(scale * S.T @ q[t])
+        states.append(S.copy())
+    return np.array(outs), states
+
+
+@pytest.mark.parametrize("dk,dv,T", [(1, 1, 5), (2, 3, 6), (4, 4, 8), (3, 2, 7)])
+def test_brute_force_tiny(dk, dv, T):
+    rng = np.random.default_rng(100 + dk * 10 + dv)
+    H = 2
+    q, k, v, g, beta = _rand_inputs(rng, T, H, dk, dv, unit=False)
+    pool = rng.standard_normal((3, H, dk, dv))
+    cu, idx = np.array([0, T], np.int32), np.array([2], np.int32)
+    out, pool_after, ck, _ = oracle.prefill(q, k, v, g, beta, cu, idx, pool, checkpoint_every=2,
+                                            scale=0.7)
+    for h in range(H):
+        o_bf, states = _brute_force(q[:, h], k[:, h], v[:, h], g[:, h], beta[:, h], pool[2, h], 0.7)
+        np.testing.assert_allclose(out[:, h], o_bf, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(pool_after[2, h], states[-1], rtol=1e-12, atol=1e-12)
+        for m in range(T // 2):
+            np.testing.assert_allclose(ck[m, h], states[2 * m + 1], rtol=1e-12, atol=1e-12)
+    # untouched slots stay bit-identical
+    assert np.array_equal(pool_after[:2], pool[:2])
+
+
+# ---------------------------------------------------------------- closed forms
+def test_single_token_from_zero_state():
+    rng = np.random.default_rng(1)
+    dk, dv, H = 8, 5, 3
+    q, k, v, g, beta = _rand_inputs(rng, 1, H, dk, dv)
+    pool = np.zeros((1, H, dk, dv))
+    cu, idx = _one_seq(1)
+    out, pool_after, _, _ = oracle.prefill(q, k, v, g, beta, cu, idx, pool, scale=0.3)
+    for h in range(H):
+        S = beta[0, h] * np.outer(k[0, h], v[0, h])
+        np.testing.assert_allclose(pool_after[0, h], S, atol=1e-14)
+        np.testing.assert_allclose(out[0, h], 0.3 * beta[0, h] * (q[0, h] @ k[0, h]) * v[0, h],
+                                   atol=1e-14)
+
+
+def test_beta0_g0_leaves_state_unchanged():
+    rng = np.random.default_rng(2)
+    T, H, dk, dv = 9, 2, 6, 4
+    q, k, v, _, _ = _rand_inputs(rng, T, H, dk, dv)
+    g = np.zeros((T, H, dk))
+    beta = np.zeros((T, H))
+    pool = rng.standard_normal((2, H, dk, dv))
+    cu, idx = np.array([0, T], np.int32), np.array([1], np.int32)
+    out, pool_after, _, _ = oracle.prefill(q, k, v, g, beta, cu, idx, pool, scale=0.5)
+    assert np.array_equal(pool_after, pool)
+    for h in range(H):
+        np.testing.assert_allclose(out[:, h], 0.5 * q[:, h] @ pool[1, h], atol=1e-14)
+
+
+def test_infinite_decay_erases_history():
+    rng = np.random.default_rng(3)
+    T, H, dk, dv = 6, 2, 4, 4
+    q, k, v, _, beta = _rand_inputs(rng, T, H, dk, dv)
+    g = np.full((T, H, dk), -1e30)  # exp(-1e30) == 0 exactly in fp64
+    pool = rng.standard_normal((1, H, dk, dv))
+    cu, idx = _one_seq(T)
+    out, pool_after, _, _ = oracle.prefill(q, k, v, g, beta, cu, idx, pool, scale=1.0)
+    for h in range(H):
+        for t in range(T):
+            np.testing.assert_allclose(out[t, h], beta[t, h] * (q[t, h] @ k[t, h]) * v[t, h],
+                                       atol=1e-14)
+        np.testing.assert_allclose(pool_after[0, h], beta[-1, h] * np.outer(k[-1, h], v[-1, h]),
+                                   atol=1e-14)
+
+
+def test_delta_rule_retrieval_beta1_g0():
+    """beta = 1, no decay, unit k: after writing (k_t, v_t) the state maps k_t
+    to v_t exactly, so reading with q = k returns v."""
+    rng = np.random.default_rng(4)
+    T, H, dk, dv = 10, 2, 6, 3
+    _, k, v, _, _ = _rand_inputs(rng, T, H, dk, dv)
+    g = np.zeros((T, H, dk))
+    beta = np.ones((T, H))
+    pool = rng.standard_normal((1, H, dk, dv))
+    cu, idx = _one_seq(T)
+    out, _, _, _ = oracle.prefill(k, k, v, g, beta, cu, idx, pool, scale=1.0)
+    np.testing.assert_allclose(out, v, atol=1e-12)
+
+
+def test_scalar_geometric_closed_form():
+    """dk = dv = 1, k = 1, v = 1, beta = 1/2, alpha = 1/2, s0 = 0:
+    s_t = (1/4) s_{t-1} + 1/2, whose closed form is s_t = (2/3)(1 - 4^-t)."""
+    T = 12
+    q = np.ones((T, 1, 1))
+    k = np.ones((T, 1, 1))
+    v = np.ones((T, 1, 1))
+    g = np.full((T, 1, 1), math.log(0.5))
+    beta = np.full((T, 1), 0.5)
+    pool = np.zeros((1, 1, 1, 1))
+    cu, idx = _one_seq(T)
+    out, _, _, _ = oracle.prefill(q, k, v, g, beta, cu, idx, pool, scale=1.0)
+    t = np.arange(1, T + 1)
+    np.testing.assert_allclose(out[:, 0, 0], (2 / 3) * (1 - 4.0 ** (-t)), rtol=1e-14)
+
+
+# ---------------------------------------------------------------- invariants
+def test_split_invariance_and_checkpoint_placement():
+    rng = np.random.default_rng(5)
+    T, H, dk, dv, I = 96, 2, 8, 6, 16
+    q, k, v, g, beta = _rand_inputs(rng, T, H, dk, dv)
+    pool = rng.standard_normal((4, H, dk, dv))
+    idx = np.array([3], np.int32)
+    out1, pool1, ck1, _ = oracle.prefill(q, k, v, g, beta, [0, T], idx, pool, checkpoint_every=I)
+    a = 48
+    outa, poola, cka, _ = oracle.prefill(q[:a], k[:a], v[:a], g[:a], beta[:a], [0, a], idx, pool,
+                                         checkpoint_every=I)
+    outb, poolb, ckb, _ = oracle.prefill(q[a:], k[a:], v[a:], g[a:], beta[a:], [0, T - a], idx,
+                                         poola, checkpoint_every=I)
+    np.testing.assert_allclose(np.concatenate([outa, outb]), out1, atol=1e-12)
+    np.testing.assert_allclose(poolb, pool1, atol=1e-12)
+    assert ck1.shape[0] == T // I and cka.shape[0] + ckb.shape[0] == T // I
+    np.testing.assert_allclose(np.concatenate([cka, ckb]), ck1, atol=1e-12)
+    # checkpoint m equals the final state of a prefill over the first (m+1)*I tokens
+    for m in range(T // I):
+        n = (m + 1) * I
+        _, pm, _, _ = oracle.prefill(q[:n], k[:n], v[:n], g[:n], beta[:n], [0, n], idx, pool)
+        np.testing.assert_allclose(ck1[m], pm[3], atol=1e-12)
+
+
+def test_packing_equals_separate_calls_and_offsets():
+    rng = np.random.default_rng(6)
+    lens = [37, 0, 64, 5, 130]
+    T, H, dk, dv, I = sum(lens), 2, 4, 4, 32
+    q, k, v, g, beta = _rand_inputs(rng, T, H, dk, dv)
+    pool = rng.standard_normal((8, H, dk, dv))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    idx = np.array([5, 1, 7, -1, 2], np.int32)
+    out, pool_after, ck, offs = oracle.prefill(q, k, v, g, beta, cu, idx, pool, checkpoint_every=I)
+    assert offs.tolist() == [0, 1, 1, 3, 3, 7]
+    assert ck.shape[0] == 7
+    for i, L in enumerate(lens):
+        t0 = cu[i]
+        sl = slice(t0, t0 + L)
+        if idx[i] < 0:
+            assert np.all(out[sl] == 0)  # padding rows are zeroed
+            continue
+        o_i, p_i, ck_i, _ = oracle.prefill(q[sl], k[sl], v[sl], g[sl], beta[sl], [0, L],
+                                           [idx[i]], pool, checkpoint_every=I)
+        np.testing.assert_allclose(out[sl], o_i, atol=1e-13)
+        np.testing.assert_allclose(pool_after[idx[i]], p_i[idx[i]], atol=1e-13)
+        np.testing.assert_allclose(ck[offs[i]:offs[i + 1]], ck_i, atol=1e-13)
+    # slot 1 belongs to a zero-length segment: untouched; slots 0,3,4,6 untouched
+    for s in (0, 1, 3, 4, 6):
+        assert np.array_equal(pool_after[s], pool[s])
+
+
+def test_linearity_in_state_and_values():
+    rng = np.random.default_rng(7)
+    T, H, dk, dv = 20, 1, 5, 4
+    q, k, v1, g, beta = _rand_inputs(rng, T, H, dk, dv)
+    v2 = rng.standard_normal(v1.shape)
+    p1, p2 = rng.standard_normal((2, 1, H, dk, dv))
+    cu, idx = _one_seq(T)
+    a, b = 0.75, -1.5
+    o1, s1, _, _ = oracle.prefill(q, k, v1, g, beta, cu, idx, p1)
+    o2, s2, _, _ = oracle.prefill(q, k, v2, g, beta, cu, idx, p2)
+    o3, s3, _, _ = oracle.prefill(q, k, a * v1 + b * v2, g, beta, cu, idx, a * p1 + b * p2)
+    np.testing.assert_allclose(o3, a * o1 + b * o2, atol=1e-12)
+    np.testing.assert_allclose(s3, a * s1 + b * s2, atol=1e-12)
+
+
+def test_value_columns_are_independent():
+    rng = np.random.default_rng(8)
+    T, H, dk, dv = 15, 2, 4, 6
+    q, k, v, g, beta = _rand_inputs(rng, T, H, dk, dv)
+    pool = rng.standard_normal((1, H, dk, dv))
+    perm = rng.permutation(dv)
+    cu, idx = _one_seq(T)
+    o, s, _, _ = oracle.prefill(q, k, v, g, beta, cu, idx, pool)
+    op, sp, _, _ = oracle.prefill(q, k, v[..., perm], g, beta, cu, idx, pool[..., perm])
+    np.testing.assert_allclose(op, o[..., perm], atol=1e-13)
+    np.testing.assert_allclose(sp, s[..., perm], atol=1e-13)
+
+
+def test_decode_equals_one_token_prefill():
+    rng = np.random.default_rng(9)
+    N, H, dk, dv = 5, 2, 8, 8
+    q, k, v, g, beta = _rand_inputs(rng, N, H, dk, dv)
+    gate = rng.standard_normal((N, H, dv))
+    w = 1 + 0.02 * rng.standard_normal(dv)
+    pool = rng.standard_normal((9, H, dk, dv))
+    idx = np.array([4, -1, 0, 8, 2], np.int32)
+    o, p = oracle.decode(q, k, v, g, beta, idx, pool, gate=gate, norm_w=w)
+    for i in range(N):
+        if idx[i] < 0:
+            assert np.all(o[i] == 0)
+            continue
+        S = pool[idx[i]]
+        for h in range(H):
+            # single-token recurrence written via the expanded transition
+            Sn = (np.eye(dk) - beta[i, h] * np.outer(k[i, h], k[i, h])) @ (
+                np.exp(g[i, h])[:, None] * S[h]) + beta[i, h] * np.outer(k[i, h], v[i, h])
+            np.testing.assert_allclose(p[idx[i], h], Sn, atol=1e-12)
+            oh = Sn.T @ q[i, h] / math.sqrt(dk)
+            yh = oh / math.sqrt(np.mean(oh ** 2) + 1e-6) * w / (1 + np.exp(-gate[i, h]))
+            np.testing.assert_allclose(o[i, h], yh, atol=1e-12)
+
+
+def test_norm_gate_constant_row_and_scale_invariance():
+    rng = np.random.default_rng(10)
+    dv = 16
+    gate = rng.standard_normal((3, dv))
+    w = 1 + 0.02 * rng.standard_normal(dv)
+    c = np.array([[2.0] * dv, [-0.5] * dv, [1e-3] * dv])
+    y = oracle.norm_gate(c, gate, w, eps=1e-6)
+    sig = 1 / (1 + np.exp(-gate))
+    expect = (c / np.sqrt(c ** 2 + 1e-6)) * w * sig
+    np.testing.assert_allclose(y, expect, rtol=1e-12)
+    o = rng.standard_normal((4, dv))
+    np.testing.assert_allclose(oracle.norm_gate(1e3 * o, np.zeros((4, dv)), np.ones(dv), eps=0.0),
+                               oracle.norm_gate(o, np.zeros((4, dv)), np.ones(dv), eps=0.0),
+                               rtol=1e-12)
+
+
+def test_bad_index_rejected():
+    q = np.zeros((2, 1, 2, 2))[:, :, 0]
+    with pytest.raises(oracle.OracleError):
+        oracle.prefill(q, q, q, q, np.zeros((2, 1)), [0, 2], [5], np.zeros((2, 1, 2, 2)))
+
+
+# ---------------------------------------------------------------- chunk form
+@pytest.mark.parametrize("chunk,lens", [(16, [64]), (16, [37, 5, 16]), (64, [37, 128, 200]),
+                                        (64, [1, 63, 65, 64])])
+def test_chunk_form_matches_oracle(chunk, lens):
+    rng = np.random.default_rng(11 + chunk + len(lens))
+    T, H, dk, dv = sum(lens), 2, 16, 8
+    q, k, v, g, beta = _rand_inputs(rng, T, H, dk, dv)
+    pool = 0.1 * rng.standard_normal((6, H, dk, dv))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    idx = rng.permutation(6)[:len(lens)].astype(np.int32)
+    I = chunk * 2
+    out, pool_o, ck_o, _ = oracle.prefill(q, k, v, g, beta, cu, idx, pool, checkpoint_every=I)
+    out_c, pool_c, ck_c = chunk_prefill(q, k, v, g, beta, cu, idx, pool, chunk=chunk,
+                                        checkpoint_every=I)
+    np.testing.assert_allclose(out_c, out, atol=1e-10)
+    np.testing.assert_allclose(pool_c, pool_o, atol=1e-10)
+    np.testing.assert_allclose(ck_c, ck_o, atol=1e-10)
+
+
+# ---------------------------------------------------------------- planted mistakes
+def test_pins_catch_planted_mistakes():
+    """The closed forms above distinguish the recurrence from its plausible
+    mis-readings: reading the state before the write, applying the decay after
+    the delta-rule residual, or dropping beta from the write."""
+    rng = np.random.default_rng(12)
+    T, dk, dv = 6, 4, 3
+    q, k, v, g, beta = (x[:, 0] for x in _rand_inputs(rng, T, 1, dk, dv))
+    S0 = rng.standard_normal((dk, dv))
+
+    def variant(mode):
+        S = S0.copy()
+        outs = []
+        for t in range(T):
+            a = np.exp(g[t])
+            if mode == "read_before_write":
+                Sd = a[:, None] * S
+                u = beta[t] * (v[t] - Sd.T @ k[t])
+                outs.append(Sd.T @ q[t])
+                S = Sd + np.outer(k[t], u)
+            elif mode == "decay_after_residual":
+                u = beta[t] * (v[t] - S.T @ k[t])
+                S = a[:, None] * (S + np.outer(k[t], u))
+                outs.append(S.T @ q[t])
+            elif mode == "no_beta_write":
+                Sd = a[:, None] * S
+                u = v[t] - Sd.T @ k[t]
+                S = Sd + np.outer(k[t], u)
+                outs.append(S.T @ q[t])
+        return np.array(outs)
+
+    o_ref, _ = _brute_force(q, k, v, g, beta, S0, 1.0)
+    out, _, _, _ = oracle.prefill(q[:, None], k[:, None], v[:, None], g[:, None], beta[:, None],
+                                  [0, T], [0], S0[None, None], scale=1.0)
+    np.testing.assert_allclose(out[:, 0], o_ref, atol=1e-12)
+    for mode in ("read_before_write", "decay_after_residual", "no_beta_write"):
+        assert np.max(np.abs(variant(mode) - o_ref)) > 1e-3, mode
