@@ -1,0 +1,163 @@
+/*
+ * kda.h -- C ABI of libkda: Kimi Delta Attention (KDA) prefill, decode and
+ * output norm-gate on one NVIDIA GB300 (sm_103a).
+ *
+ * The method.  KDA is the gated delta rule with a per-channel decay.  For a
+ * head with key dimension dk and value dimension dv, token t updates the
+ * recurrent state S (dk x dv) and reads it out:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * Sources: "[Feature][KDA] Add Kimi K3 KDA execution" (vllm-ascend PR 14598),
+ * section "KDA execution", steps 3 (chunk prefill over a cumulative gate) and
+ * 4 (recurrent decode); "[KK] Prepare B12X Kimi KDA prefill ..." (vLLM PR
+ * 937), section "Behavior" (state-pool indices consumed in place, reusable
+ * caller-owned scratch); the FlashKDA bf16-checkpoint summary (vLLM PR
+ * 56485), motivation and implementation sections (intermediate checkpoint
+ * states whose dtype follows the state dtype; tolerances 0.03 bf16 / 0.01
+ * fp32).
+ *
+ * Conventions shared by every call.
+ *  - All tensors are dense, row-major, last dimension contiguous, and live in
+ *    device memory unless stated otherwise.  The caller owns every buffer;
+ *    the library allocates nothing and never synchronises.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls are asynchronous on that stream and make no host read of
+ *    device data, so they can be captured in a CUDA graph.
+ *  - Argument errors are detected on the host and returned; nothing is
+ *    launched then.  Errors that need device values (a bad state index, a bad
+ *    cu_seqlens entry) are latched into `*dev_status` (an int32 in device
+ *    memory, zeroed by the caller; may be NULL), and the affected sequence is
+ *    skipped with its output rows zeroed.  Kernels never trap.
+ *  - Token-major layouts: q, k, g are [T, H, dk]; v, out, gate are
+ *    [T, H, dv]; beta is [T, H].  The state pool is [num_slots, H, dk, dv].
+ *  - Supported: dk == dv in {16, 64, 128}; chunk in {16, 64} (prefill);
+ *    inputs fp32 or bf16; state fp32 or bf16.  Others -> KDA_ERR_UNSUPPORTED.
+ *  - Pointer alignment: 16 bytes for every tensor argument.
+ */
+#ifndef LIBKDA_KDA_H_
+#define LIBKDA_KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = -1, /* null/misaligned pointer, negative size, bad combination */
+  KDA_ERR_UNSUPPORTED = -2, /* a shape or dtype outside the supported set */
+  KDA_ERR_WORKSPACE = -3,   /* workspace smaller than *_workspace_bytes() asks */
+  KDA_ERR_CUDA = -4         /* a CUDA launch or attribute call failed */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Codes latched into *dev_status by the kernels (first error wins). */
+#define KDA_DEV_OK 0
+#define KDA_DEV_BAD_INDEX 1       /* state_indices[i] outside [-1, num_slots) */
+#define KDA_DEV_BAD_SEQLENS 2     /* cu_seqlens not non-decreasing within [0, T] */
+#define KDA_DEV_TIMEOUT 3         /* a bounded on-chip wait gave up */
+#define KDA_DEV_CKPT_OVERFLOW 4   /* checkpoints would exceed checkpoint_capacity */
+
+/*
+ * Bytes of caller-owned scratch kda_prefill_chunked needs for these sizes
+ * (the pages' "reusable caller-owned scratch").  May be 0.  The same
+ * workspace can be reused by consecutive calls on one stream.
+ */
+KDA_API size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk);
+
+/*
+ * Chunked varlen prefill over an indexed state pool ("[Feature][KDA] ...",
+ * "KDA execution" step 3; "[KK] Prepare B12X ...", "Behavior").
+ *
+ *  q, k, g      [T, H, dk]  in_dtype.  g is the per-channel log-decay
+ *               (alpha = exp(g)); the in-chunk cumulative sum is done here.
+ *  v            [T, H, dv]  in_dtype.
+ *  beta         [T, H]      in_dtype.
+ *  cu_seqlens   int32 [N+1], device.  Sequence i is tokens
+ *               [cu_seqlens[i], cu_seqlens[i+1]); cu_seqlens[0] == 0 and
+ *               cu_seqlens[N] == T.  Chunks restart at every sequence start;
+ *               the last chunk of a sequence may be partial.  A zero-length
+ *               sequence is a no-op (its slot is not rewritten).
+ *  state_indices int32 [N], device.  Sequence i starts from
+ *               state_pool[state_indices[i]] and its final state is written
+ *               back to that slot in place.  -1 marks a padding sequence: its
+ *               output rows are zeroed and the pool is untouched.  Indices
+ *               must be distinct within a call.
+ *  state_pool   [num_slots, H, dk, dv] state_dtype, read and written.
+ *  out          [T, H, dv] in_dtype.  o_t, or the norm-gated y_t when gate
+ *               is non-NULL.
+ *  checkpoints  [checkpoint_capacity, H, dk, dv] state_dtype, or NULL when
+ *               checkpoint_every == 0.  After every checkpoint_every tokens of
+ *               a sequence (counted from the start of this call's segment) the
+ *               state is appended; sequence i owns entries
+ *               [ckpt_offsets[i], ckpt_offsets[i+1]).  checkpoint_every must be
+ *               0 or a multiple of chunk, and checkpoint_capacity must be at
+ *               least T / checkpoint_every.
+ *  ckpt_offsets int32 [N+1], device, written (may be NULL): the exclusive
+ *               prefix sum of floor(len_i / checkpoint_every).
+ *  gate, norm_w gate [T, H, dv] in_dtype and norm_w [dv] in_dtype, or both
+ *               NULL.  When given, out = o / sqrt(mean(o^2) + eps) * norm_w *
+ *               sigmoid(gate) per (token, head) row.
+ *  scale        read-out scale; <= 0 selects 1/sqrt(dk).
+ *  workspace    caller scratch of at least kda_prefill_workspace_bytes().
+ *  dev_status   see the conventions above (may be NULL).
+ *
+ * State is carried in fp32 inside a call and rounded (to nearest even) to
+ * state_dtype only when stored: at checkpoints and at the final write-back.
+ */
+KDA_API kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, const void* g,
+                               const void* beta, kda_dtype in_dtype, const int32_t* cu_seqlens,
+                               int N, int64_t T, const int32_t* state_indices, void* state_pool,
+                               int64_t num_slots, kda_dtype state_dtype, void* out,
+                               void* checkpoints, int32_t checkpoint_every,
+                               int64_t checkpoint_capacity, int32_t* ckpt_offsets,
+                               const void* gate, const void* norm_w, float eps, int H, int dk,
+                               int dv, int chunk, float scale, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * One recurrent decode step for N sequences of one token each ("[Feature][KDA]
+ * ...", "KDA execution" step 4).  q, k, g [N, H, dk]; v, out, gate [N, H, dv];
+ * beta [N, H]; state_indices int32 [N] (device; -1 = padding row, zeroed).
+ * g is in the same log-decay form as for prefill (the pages' "normalize the
+ * recurrent gate" step is the caller's).  The state is updated in place and
+ * rounded to state_dtype at the store.  gate/norm_w as for prefill.
+ */
+KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, const void* g,
+                           const void* beta, kda_dtype in_dtype, const int32_t* state_indices,
+                           int N, void* state_pool, int64_t num_slots, kda_dtype state_dtype,
+                           void* out, const void* gate, const void* norm_w, float eps, int H,
+                           int dk, int dv, float scale, int32_t* dev_status, void* stream);
+
+/*
+ * Standalone output RMSNorm-gate ("[Feature][KDA] ...", first section:
+ * FusedRMSNormGated output normalisation and gating):
+ *     y = o / sqrt(mean_dv(o^2) + eps) * w * sigmoid(gate)
+ * o, gate, y are [rows, H, dv] in `dtype`; w is [dv] in `dtype`.  y may alias o
+ * (in place); otherwise o is preserved.
+ */
+KDA_API kda_status kda_norm_gate(const void* o, const void* gate, const void* w, float eps, void* y,
+                         int64_t rows, int H, int dv, kda_dtype dtype, void* stream);
+
+/* A static, human-readable name for a kda_status value. */
+KDA_API const char* kda_status_string(kda_status status);
+
+/* Library ABI version (major * 100 + minor). */
+KDA_API int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBKDA_KDA_H_ */

@@ -1,0 +1,152 @@
+"""Python binding of libkda (KDA prefill, decode and output norm-gate on GB300).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libkda.so``; torch supplies device memory and streams.  Each
+function carries the C entry point's name and passes torch tensors as raw
+pointers.  There is no fallback: if ``libkda.so`` is missing or fails to load,
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "load", "lib_path", "KdaError", "KDA_OK", "KDA_F32", "KDA_BF16",
+    "kda_prefill_chunked", "kda_prefill_workspace_bytes", "kda_decode_step", "kda_norm_gate",
+    "kda_status_string", "kda_version", "DEV_STATUS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libkda.so")
+_lib = None
+
+KDA_OK, KDA_F32, KDA_BF16 = 0, 0, 1
+DEV_STATUS = {0: "ok", 1: "bad state index", 2: "bad cu_seqlens", 3: "on-chip wait timeout",
+              4: "checkpoint capacity exceeded"}
+
+_P = ctypes.c_void_p
+_I32, _I64, _F32, _SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+
+_SIGNATURES = {
+    "kda_prefill_workspace_bytes": (_SZ, [ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int]),
+    "kda_prefill_chunked": (ctypes.c_int, [
+        _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _I64, _P, _P, _I64, ctypes.c_int, _P,
+        _P, _I32, _I64, _P, _P, _P, _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        _F32, _P, _SZ, _P, _P]),
+    "kda_decode_step": (ctypes.c_int, [
+        _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _P, _I64, ctypes.c_int, _P, _P, _P,
+        _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int, _F32, _P, _P]),
+    "kda_norm_gate": (ctypes.c_int, [_P, _P, _P, _F32, _P, _I64, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, _P]),
+    "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "kda_version": (ctypes.c_int, []),
+}
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {kda_status_string(status)} ({status})")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libkda.so (built by ``build.py``); raises when it is absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libkda.so not built ({_LIB_PATH}); run the package's build.py")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("libkda takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() > 0 else None
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return KDA_F32
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != KDA_OK:
+        raise KdaError(status, where)
+
+
+def kda_status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def kda_version() -> int:
+    return load().kda_version()
+
+
+def kda_prefill_workspace_bytes(N: int, T: int, H: int, dk: int, dv: int, chunk: int) -> int:
+    return int(load().kda_prefill_workspace_bytes(N, T, H, dk, dv, chunk))
+
+
+def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, *,
+                        chunk: int = 64, checkpoints=None, checkpoint_every: int = 0,
+                        ckpt_offsets=None, gate=None, norm_w=None, eps: float = 1e-6,
+                        scale: float = 0.0, workspace=None, dev_status=None, stream=None):
+    """Chunked varlen prefill (see ``include/kda.h``).  All tensors on one
+    CUDA device; ``state_pool`` is updated in place, ``out`` (and
+    ``checkpoints``/``ckpt_offsets`` when given) are written."""
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = state_indices.shape[0]
+    cap = checkpoints.shape[0] if checkpoints is not None else 0
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().kda_prefill_chunked(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(cu_seqlens), N, T,
+        _ptr(state_indices), _ptr(state_pool), state_pool.shape[0], _dtype(state_pool), _ptr(out),
+        _ptr(checkpoints), int(checkpoint_every), cap, _ptr(ckpt_offsets), _ptr(gate),
+        _ptr(norm_w), float(eps), H, dk, dv, int(chunk), float(scale), _ptr(workspace), ws_bytes,
+        _ptr(dev_status), _stream(stream))
+    _check(st, "kda_prefill_chunked")
+
+
+def kda_decode_step(q, k, v, g, beta, state_indices, state_pool, out, *, gate=None, norm_w=None,
+                    eps: float = 1e-6, scale: float = 0.0, dev_status=None, stream=None):
+    """One recurrent decode step for N one-token sequences (see ``include/kda.h``)."""
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    st = load().kda_decode_step(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(state_indices), N,
+        _ptr(state_pool), state_pool.shape[0], _dtype(state_pool), _ptr(out), _ptr(gate),
+        _ptr(norm_w), float(eps), H, dk, dv, float(scale), _ptr(dev_status), _stream(stream))
+    _check(st, "kda_decode_step")
+
+
+def kda_norm_gate(o, gate, w, y, *, eps: float = 1e-6, stream=None):
+    """y = o / sqrt(mean(o^2)+eps) * w * sigmoid(gate) over the last dim of [rows, H, dv]."""
+    rows, H, dv = o.shape
+    st = load().kda_norm_gate(_ptr(o), _ptr(gate), _ptr(w), float(eps), _ptr(y), rows, H, dv,
+                              _dtype(o), _stream(stream))
+    _check(st, "kda_norm_gate")

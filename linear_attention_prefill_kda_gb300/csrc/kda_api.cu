@@ -1,0 +1,148 @@
+// extern "C" entry points of libkda: argument validation on the host, then
+// asynchronous launches on the caller's stream.  No allocation, no
+// synchronisation, no host read of device memory.
+#include <math.h>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dtype_ok(kda_dtype d) { return d == KDA_F32 || d == KDA_BF16; }
+bool dim_ok(int d) { return d == 16 || d == 64 || d == 128; }
+
+// Every non-NULL pointer must be 16-byte aligned; required ones must be non-NULL.
+bool ptr_ok(const void* p, bool required) {
+  if (!p) return !required;
+  return aligned16(p);
+}
+
+kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int kda_version(void) { return 100; }
+
+const char* kda_status_string(kda_status s) {
+  switch (s) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case KDA_ERR_WORKSPACE: return "workspace too small";
+    case KDA_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk) {
+  if (N < 0 || T < 0 || H <= 0) return 0;
+  return kda::prefill_workspace_bytes(N, T, H, dk, dv, chunk);
+}
+
+kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, const void* g,
+                               const void* beta, kda_dtype in_dtype, const int32_t* cu_seqlens,
+                               int N, int64_t T, const int32_t* state_indices, void* state_pool,
+                               int64_t num_slots, kda_dtype state_dtype, void* out,
+                               void* checkpoints, int32_t checkpoint_every,
+                               int64_t checkpoint_capacity, int32_t* ckpt_offsets,
+                               const void* gate, const void* norm_w, float eps, int H, int dk,
+                               int dv, int chunk, float scale, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (N < 0 || T < 0 || T > INT32_MAX || H <= 0 || num_slots <= 0) return KDA_ERR_INVALID_ARG;
+  if (!dtype_ok(in_dtype) || !dtype_ok(state_dtype)) return KDA_ERR_UNSUPPORTED;
+  if (!dim_ok(dk) || dv != dk || (chunk != 16 && chunk != 64)) return KDA_ERR_UNSUPPORTED;
+  if (checkpoint_every < 0 || (checkpoint_every > 0 && checkpoint_every % chunk != 0))
+    return KDA_ERR_INVALID_ARG;
+  const bool tokens = T > 0;
+  if (!ptr_ok(q, tokens) || !ptr_ok(k, tokens) || !ptr_ok(v, tokens) || !ptr_ok(g, tokens) ||
+      !ptr_ok(beta, tokens) || !ptr_ok(out, tokens))
+    return KDA_ERR_INVALID_ARG;
+  if (!ptr_ok(cu_seqlens, true) || !ptr_ok(state_indices, N > 0) || !ptr_ok(state_pool, true))
+    return KDA_ERR_INVALID_ARG;
+  if (!ptr_ok(ckpt_offsets, false) || !ptr_ok(dev_status, false)) return KDA_ERR_INVALID_ARG;
+  if ((gate == nullptr) != (norm_w == nullptr)) return KDA_ERR_INVALID_ARG;
+  if (!ptr_ok(gate, false) || !ptr_ok(norm_w, false)) return KDA_ERR_INVALID_ARG;
+  if (gate && !(eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+  if (checkpoint_every > 0) {
+    if (!ptr_ok(checkpoints, true)) return KDA_ERR_INVALID_ARG;
+    if (checkpoint_capacity < T / checkpoint_every) return KDA_ERR_INVALID_ARG;
+  }
+  const size_t need = kda::prefill_workspace_bytes(N, T, H, dk, dv, chunk);
+  if (need > 0 && (workspace_bytes < need || !ptr_ok(workspace, true))) return KDA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    if (ckpt_offsets) return from_cuda(cudaMemsetAsync(ckpt_offsets, 0, sizeof(int32_t), st));
+    return KDA_OK;
+  }
+  kda::PrefillParams p{};
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+  p.cu_seqlens = cu_seqlens;
+  p.state_indices = state_indices;
+  p.state_pool = state_pool;
+  p.out = out;
+  p.checkpoints = checkpoints;
+  p.ckpt_offsets = ckpt_offsets;
+  p.gate = gate; p.norm_w = norm_w;
+  p.workspace = workspace;
+  p.workspace_bytes = workspace_bytes;
+  p.dev_status = dev_status;
+  p.T = T; p.num_slots = num_slots; p.checkpoint_capacity = checkpoint_capacity;
+  p.N = N; p.H = H; p.dk = dk; p.dv = dv; p.chunk = chunk; p.checkpoint_every = checkpoint_every;
+  p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)dk);
+  p.eps = eps;
+  p.in_dtype = in_dtype; p.state_dtype = state_dtype;
+  return from_cuda(kda::launch_prefill(p, st));
+}
+
+kda_status kda_decode_step(const void* q, const void* k, const void* v, const void* g,
+                           const void* beta, kda_dtype in_dtype, const int32_t* state_indices,
+                           int N, void* state_pool, int64_t num_slots, kda_dtype state_dtype,
+                           void* out, const void* gate, const void* norm_w, float eps, int H,
+                           int dk, int dv, float scale, int32_t* dev_status, void* stream) {
+  if (N < 0 || H <= 0 || num_slots <= 0) return KDA_ERR_INVALID_ARG;
+  if ((int64_t)N * H > INT32_MAX) return KDA_ERR_INVALID_ARG;
+  if (!dtype_ok(in_dtype) || !dtype_ok(state_dtype)) return KDA_ERR_UNSUPPORTED;
+  if (!dim_ok(dk) || dv != dk) return KDA_ERR_UNSUPPORTED;
+  if (N == 0) return KDA_OK;
+  if (!ptr_ok(q, true) || !ptr_ok(k, true) || !ptr_ok(v, true) || !ptr_ok(g, true) ||
+      !ptr_ok(beta, true) || !ptr_ok(out, true) || !ptr_ok(state_indices, true) ||
+      !ptr_ok(state_pool, true) || !ptr_ok(dev_status, false))
+    return KDA_ERR_INVALID_ARG;
+  if ((gate == nullptr) != (norm_w == nullptr)) return KDA_ERR_INVALID_ARG;
+  if (!ptr_ok(gate, false) || !ptr_ok(norm_w, false)) return KDA_ERR_INVALID_ARG;
+  if (gate && !(eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+  kda::DecodeParams p{};
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+  p.state_indices = state_indices;
+  p.state_pool = state_pool;
+  p.out = out;
+  p.gate = gate; p.norm_w = norm_w;
+  p.dev_status = dev_status;
+  p.num_slots = num_slots;
+  p.N = N; p.H = H; p.dk = dk; p.dv = dv;
+  p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)dk);
+  p.eps = eps;
+  p.in_dtype = in_dtype; p.state_dtype = state_dtype;
+  return from_cuda(kda::launch_decode(p, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_norm_gate(const void* o, const void* gate, const void* w, float eps, void* y,
+                         int64_t rows, int H, int dv, kda_dtype dtype, void* stream) {
+  if (rows < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype)) return KDA_ERR_UNSUPPORTED;
+  if (!dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+  if (!(eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+  if (rows == 0) return KDA_OK;
+  if ((rows * H + 7) / 8 > INT32_MAX) return KDA_ERR_INVALID_ARG;
+  if (!ptr_ok(o, true) || !ptr_ok(gate, true) || !ptr_ok(w, true) || !ptr_ok(y, true))
+    return KDA_ERR_INVALID_ARG;
+  kda::NormGateParams p{};
+  p.o = o; p.gate = gate; p.w = w; p.y = y;
+  p.rows = rows; p.H = H; p.dv = dv; p.eps = eps; p.dtype = dtype;
+  return from_cuda(kda::launch_norm_gate(p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

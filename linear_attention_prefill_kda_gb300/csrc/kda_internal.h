@@ -1,0 +1,63 @@
+// Internal launch parameters shared by the host entry points and the kernel
+// launchers.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+struct DecodeParams {
+  const void *q, *k, *v, *g, *beta;
+  const int32_t* state_indices;
+  void* state_pool;
+  void* out;
+  const void *gate, *norm_w;
+  int32_t* dev_status;
+  int64_t num_slots;
+  int N, H, dk, dv;
+  float scale, eps;
+  kda_dtype in_dtype, state_dtype;
+};
+
+struct NormGateParams {
+  const void *o, *gate, *w;
+  void* y;
+  int64_t rows;  // token rows; each holds H heads of dv
+  int H, dv;
+  float eps;
+  kda_dtype dtype;
+};
+
+struct PrefillParams {
+  const void *q, *k, *v, *g, *beta;
+  const int32_t* cu_seqlens;
+  const int32_t* state_indices;
+  void* state_pool;
+  void* out;
+  void* checkpoints;
+  int32_t* ckpt_offsets;
+  const void *gate, *norm_w;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* dev_status;
+  int64_t T, num_slots, checkpoint_capacity;
+  int N, H, dk, dv, chunk, checkpoint_every;
+  float scale, eps;
+  kda_dtype in_dtype, state_dtype;
+};
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device), so
+// later calls (including those made during stream capture) skip the
+// attribute call.
+cudaError_t set_smem_once(const void* kernel, int bytes);
+
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_norm_gate(const NormGateParams& p, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
+size_t prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk);
+
+}  // namespace kda

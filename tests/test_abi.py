@@ -1,0 +1,120 @@
+"""The C ABI on the host: libkda.so loads, exports every function that
+include/kda.h declares, and rejects bad arguments with the documented status
+before launching anything.  No GPU needed (no call here reaches a launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_prefill_kda_gb300 as kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 1 << 20  # an aligned, never-dereferenced stand-in for a device pointer
+MIS = FAKE + 4  # misaligned
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(kda.lib_path()):
+        from linear_attention_prefill_kda_gb300 import build
+        build.build()
+    return kda.load()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"kda_prefill_chunked", "kda_decode_step", "kda_norm_gate",
+            "kda_prefill_workspace_bytes", "kda_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert kda.kda_status_string(0) == "ok"
+    assert "unsupported" in kda.kda_status_string(-2)
+    assert kda.kda_version() >= 100
+
+
+def _prefill(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, in_dtype=1, cu=FAKE, N=2, T=100, idx=FAKE,
+             pool=FAKE, slots=4, sdt=0, out=FAKE, ck=None, every=0, cap=0, offs=None, gate=None,
+             w=None, eps=1e-6, H=2, dk=64, dv=64, chunk=64, scale=0.0, ws=None, wsb=0, st=None)
+    a.update(over)
+    return lib.kda_prefill_chunked(
+        a["q"], a["k"], a["v"], a["g"], a["beta"], a["in_dtype"], a["cu"], a["N"], a["T"],
+        a["idx"], a["pool"], a["slots"], a["sdt"], a["out"], a["ck"], a["every"], a["cap"],
+        a["offs"], a["gate"], a["w"], a["eps"], a["H"], a["dk"], a["dv"], a["chunk"], a["scale"],
+        a["ws"], a["wsb"], a["st"], None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dk=32, dv=32), -2), (dict(dv=128), -2), (dict(chunk=32), -2), (dict(in_dtype=5), -2),
+    (dict(sdt=7), -2), (dict(N=-1), -1), (dict(T=-5), -1), (dict(H=0), -1), (dict(slots=0), -1),
+    (dict(q=None), -1), (dict(pool=None), -1), (dict(cu=None), -1), (dict(k=MIS), -1),
+    (dict(out=MIS), -1), (dict(every=32), -1), (dict(every=128, ck=None, cap=10), -1),
+    (dict(every=64, ck=FAKE, cap=0), -1), (dict(gate=FAKE), -1), (dict(w=FAKE), -1),
+    (dict(gate=FAKE, w=FAKE, eps=-1.0), -1), (dict(st=MIS), -1),
+])
+def test_prefill_rejects(lib, over, expect):
+    assert _prefill(lib, **over) == expect
+
+
+def _decode(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, in_dtype=1, idx=FAKE, N=4, pool=FAKE,
+             slots=8, sdt=0, out=FAKE, gate=None, w=None, eps=1e-6, H=2, dk=128, dv=128,
+             scale=0.0, st=None)
+    a.update(over)
+    return lib.kda_decode_step(a["q"], a["k"], a["v"], a["g"], a["beta"], a["in_dtype"], a["idx"],
+                               a["N"], a["pool"], a["slots"], a["sdt"], a["out"], a["gate"],
+                               a["w"], a["eps"], a["H"], a["dk"], a["dv"], a["scale"], a["st"],
+                               None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dk=64), -2), (dict(dk=96, dv=96), -2), (dict(in_dtype=3), -2), (dict(N=-2), -1),
+    (dict(H=-1), -1), (dict(slots=0), -1), (dict(idx=None), -1), (dict(v=MIS), -1),
+    (dict(gate=FAKE), -1), (dict(w=FAKE), -1),
+])
+def test_decode_rejects(lib, over, expect):
+    assert _decode(lib, **over) == expect
+
+
+def test_empty_calls_are_noops(lib):
+    assert _decode(lib, N=0, q=None, k=None, v=None, g=None, beta=None, idx=None, out=None) == 0
+    assert lib.kda_norm_gate(FAKE, FAKE, FAKE, 1e-6, FAKE, 0, 4, 128, 1, None) == 0
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((FAKE, FAKE, FAKE, 1e-6, FAKE, 10, 4, 48, 1), -2),
+    ((FAKE, FAKE, FAKE, 1e-6, FAKE, 10, 4, 128, 9), -2),
+    ((None, FAKE, FAKE, 1e-6, FAKE, 10, 4, 128, 1), -1),
+    ((FAKE, FAKE, MIS, 1e-6, FAKE, 10, 4, 128, 1), -1),
+    ((FAKE, FAKE, FAKE, -1.0, FAKE, 10, 4, 128, 1), -1),
+    ((FAKE, FAKE, FAKE, 1e-6, FAKE, -1, 4, 128, 1), -1),
+])
+def test_norm_gate_rejects(lib, args, expect):
+    assert lib.kda_norm_gate(*args, None) == expect
+
+
+def test_workspace_query(lib):
+    assert kda.kda_prefill_workspace_bytes(8, 4096, 32, 128, 128, 64) >= 0
+    assert lib.kda_prefill_workspace_bytes(-1, 10, 2, 64, 64, 64) == 0
+
+
+def test_binding_refuses_missing_library(monkeypatch, tmp_path):
+    """No silent fallback: without libkda.so every call raises."""
+    monkeypatch.setattr(kda, "_lib", None)
+    monkeypatch.setattr(kda, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        kda.kda_version()

@@ -1,0 +1,281 @@
+"""GPU parity: libkda through its C ABI against the fp64 oracle on the same
+seeded inputs.  Values within the tolerance rule of kda_testutil; indexing,
+checkpoint placement, padding rows and untouched pool slots bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from kda_testutil import (excess_error, max_abs, oracle_prefill, run_prefill, to_dev, tol_for)
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _check_prefill(kda, w, d, *, heads=None, ckpt=True):
+    pool0 = d["pool"].clone()
+    out, pool, ck, offs, status = run_prefill(kda, d, w, DEV, ckpt=ckpt)
+    assert int(status.item()) == 0, kda.DEV_STATUS[int(status.item())]
+    o_ref, p_ref, ck_ref, offs_ref = oracle_prefill(oracle, d, w, ckpt=ckpt, heads=heads)
+    tol = tol_for(w.state_dtype)
+    hsel = slice(None) if heads is None else heads
+    idx = d["state_indices"].tolist()
+    lens = (d["cu_seqlens"][1:] - d["cu_seqlens"][:-1]).tolist()
+    # outputs
+    assert excess_error(out[:, hsel], o_ref) <= tol
+    # touched slots, untouched slots bit-exact
+    touched = [s for s, L in zip(idx, lens) if s >= 0 and L > 0]
+    pool_cpu = pool.cpu()
+    for s in range(w.num_slots):
+        if s in touched:
+            assert excess_error(pool_cpu[s][hsel], p_ref[s]) <= tol, s
+        else:
+            assert torch.equal(pool_cpu[s], pool0[s]), f"slot {s} modified"
+    # checkpoints: offsets bit-exact, values within tolerance
+    if ckpt and w.checkpoint_every:
+        assert offs.cpu().numpy().tolist() == offs_ref.tolist()
+        n = int(offs_ref[-1])
+        if n:
+            real = []
+            for i, s in enumerate(idx):
+                if s >= 0:
+                    real.extend(range(int(offs_ref[i]), int(offs_ref[i + 1])))
+            assert excess_error(ck[real][:, hsel], ck_ref[real]) <= tol
+    return out, pool
+
+
+def test_prefill_tiny(kda_gpu):
+    _check_prefill(kda_gpu, W.TINY, W.make_prefill(W.TINY))
+
+
+def test_prefill_varlen(kda_gpu):
+    _check_prefill(kda_gpu, W.VARLEN, W.make_prefill(W.VARLEN))
+
+
+def test_prefill_sched_full(kda_gpu):
+    _check_prefill(kda_gpu, W.SCHED, W.make_prefill(W.SCHED))
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("chunk,d", [(64, 64), (64, 128), (16, 64), (16, 128), (64, 16), (16, 16)])
+def test_prefill_edge_lengths(kda_gpu, chunk, d, state_dtype):
+    """Empty segments, lengths 1, C-1, C, C+1, a padding sequence (-1) and the
+    highest slot id, with checkpoints every 2C."""
+    lens = (0, 1, chunk - 1, chunk, chunk + 1, 7, 3 * chunk + 5)
+    w = W.VARLEN.replace(seqlens=lens, H=3, dk=d, dv=d, chunk=chunk, checkpoint_every=2 * chunk,
+                         state_dtype=state_dtype, num_slots=12, seed=40 + d + chunk)
+    d_ = W.make_prefill(w)
+    idx = d_["state_indices"].clone()
+    idx[5] = -1
+    idx[6] = w.num_slots - 1
+    idx[:5] = torch.tensor([0, 3, 5, 7, 9], dtype=torch.int32)
+    d_["state_indices"] = idx
+    out, _ = _check_prefill(kda_gpu, w, d_)
+    t0, t1 = int(d_["cu_seqlens"][5]), int(d_["cu_seqlens"][6])
+    assert torch.count_nonzero(out[t0:t1].float()).item() == 0  # padding rows exactly zero
+
+
+def test_prefill_gate_fp32_and_chunk16(kda_gpu):
+    w = W.SCHED.replace(seqlens=(100, 37, 256), H=4, dk=64, dv=64, chunk=16, checkpoint_every=32,
+                        in_dtype=torch.float32, num_slots=8, slot_range=None, seed=77)
+    _check_prefill(kda_gpu, w, W.make_prefill(w))
+
+
+def test_prefill_extreme_decay(kda_gpu):
+    """g = -1e30 on some tokens (alpha = 0 exactly) must erase history without
+    producing inf/nan."""
+    w = W.VARLEN.replace(seqlens=(130,), H=2, in_dtype=torch.float32, seed=91, checkpoint_every=0)
+    d = W.make_prefill(w)
+    d["g"][10] = -1e30
+    d["g"][64, :, :5] = -1e30
+    d["g"][100:103] = -40.0
+    out, _ = _check_prefill(kda_gpu, w, d, ckpt=False)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_prefill_bad_index_latches_status(kda_gpu):
+    w = W.VARLEN.replace(seqlens=(20, 30), H=2, seed=5, checkpoint_every=0)
+    d = W.make_prefill(w)
+    d["state_indices"] = torch.tensor([1, w.num_slots + 3], dtype=torch.int32)
+    pool0 = d["pool"].clone()
+    out, pool, _, _, status = run_prefill(kda_gpu, d, w, DEV, ckpt=False)
+    assert int(status.item()) == 1
+    assert torch.count_nonzero(out[20:].float()).item() == 0
+    p = pool.cpu()
+    for s in range(w.num_slots):
+        if s != 1:
+            assert torch.equal(p[s], pool0[s])
+
+
+def test_prefill_longprompt_bf16_state(kda_gpu):
+    """One 32768-token sequence as 8 calls of 4096 carrying bf16 state through
+    the pool, against the one-shot fp64 oracle (sampled heads) and against a
+    single 32768-token call; checkpoint positions bit-exact."""
+    w = W.LONGPROMPT
+    d = W.make_prefill(w)
+    heads = [0, 11, 22, 31]
+    pool_init = d["pool"].clone()
+    slot = int(d["state_indices"][0])
+    T, seg = w.T, 4096
+    dev_pool = pool_init.to(DEV)
+    idx = d["state_indices"].to(DEV)
+    outs, cks = [], []
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for c in range(T // seg):
+        sl = slice(c * seg, (c + 1) * seg)
+        t = {k: d[k][sl].to(DEV) for k in ("q", "k", "v", "g", "beta")}
+        out = torch.empty(seg, w.H, w.dv, device=DEV, dtype=w.in_dtype)
+        ck = torch.empty(seg // w.checkpoint_every, w.H, w.dk, w.dv, device=DEV, dtype=w.state_dtype)
+        kda_gpu.kda_prefill_chunked(t["q"], t["k"], t["v"], t["g"], t["beta"],
+                                    W.cu_from_lengths([seg]).to(DEV), idx, dev_pool, out,
+                                    chunk=w.chunk, checkpoints=ck,
+                                    checkpoint_every=w.checkpoint_every, dev_status=status)
+        outs.append(out)
+        cks.append(ck)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    out8 = torch.cat(outs)
+    ck8 = torch.cat(cks)
+    # one-shot GPU call
+    pool1 = pool_init.to(DEV)
+    out1, pool1, ck1, offs1, st1 = run_prefill(kda_gpu, dict(d, pool=pool_init.clone()), w, DEV)
+    assert int(st1.item()) == 0
+    assert offs1.cpu().tolist() == [0, T // w.checkpoint_every]
+    assert ck1.shape[0] == ck8.shape[0] == T // w.checkpoint_every
+    tol = tol_for(w.state_dtype)
+    # the two GPU runs agree
+    assert max_abs(out8, out1.double().cpu().numpy()) <= tol
+    assert max_abs(ck8, ck1.double().cpu().numpy()) <= tol
+    # against the fp64 oracle (sampled heads)
+    o_ref, p_ref, ck_ref, _ = oracle_prefill(oracle, d, w, heads=heads)
+    assert excess_error(out8[:, heads], o_ref) <= tol
+    assert excess_error(out1[:, heads], o_ref) <= tol
+    assert excess_error(ck8[:, heads], ck_ref) <= tol
+    assert excess_error(dev_pool[slot][heads], p_ref[slot]) <= tol
+    assert excess_error(pool1[slot][heads], p_ref[slot]) <= tol
+
+
+def test_decode_full_64_steps(kda_gpu):
+    """256 sequences x 64 in-place steps on a 1024-slot fp32 pool; the oracle
+    follows a sample of 16 sequences (all heads) at every step."""
+    w = W.DECODE
+    pd = W.make_decode_pool(w)
+    pool0 = pd["pool"]
+    idx = pd["state_indices"]
+    sample = list(range(0, w.N, w.N // 16))
+    ref_pool = pool0[idx[sample].long()].double().numpy().copy()
+    ref_idx = np.arange(len(sample), dtype=np.int32)
+    dev_pool = pool0.to(DEV)
+    didx = idx.to(DEV)
+    nw = pd["norm_w"].to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = torch.empty(w.N, w.H, w.dv, device=DEV, dtype=w.in_dtype)
+    tol = tol_for(w.state_dtype)
+    worst = 0.0
+    for step in range(w.steps):
+        sd = W.make_decode_step(w, step)
+        t = to_dev(sd, DEV)
+        kda_gpu.kda_decode_step(t["q"], t["k"], t["v"], t["g"], t["beta"], didx, dev_pool, out,
+                                gate=t["gate"], norm_w=nw, eps=pd["eps"], dev_status=status)
+        y_ref, ref_pool = oracle.decode(*(sd[k][sample] for k in ("q", "k", "v", "g", "beta")),
+                                        ref_idx, ref_pool, gate=sd["gate"][sample],
+                                        norm_w=pd["norm_w"], eps=pd["eps"])
+        worst = max(worst, excess_error(out[sample], y_ref))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert worst <= tol, worst
+    final = dev_pool[didx[sample].long()]
+    assert excess_error(final, ref_pool) <= tol
+    # slots outside the batch are untouched, byte for byte
+    mask = torch.ones(w.num_slots, dtype=torch.bool)
+    mask[idx.long()] = False
+    assert torch.equal(dev_pool[mask.to(DEV)].cpu(), pool0[mask])
+
+
+@pytest.mark.parametrize("d", [16, 64, 128])
+@pytest.mark.parametrize("in_dtype,state_dtype", [(torch.float32, torch.float32),
+                                                  (torch.bfloat16, torch.bfloat16),
+                                                  (torch.float32, torch.bfloat16)])
+def test_decode_small(kda_gpu, d, in_dtype, state_dtype):
+    w = W.DECODE.replace(N=9, H=3, dk=d, dv=d, in_dtype=in_dtype, state_dtype=state_dtype,
+                         num_slots=20, seed=300 + d)
+    pd = W.make_decode_pool(w)
+    sd = W.make_decode_step(w, 0)
+    idx = torch.tensor([3, 0, 7, 12, -1, 19, 5, 8, 2], dtype=torch.int32)  # -1 pads, 19 = top slot
+    pool = pd["pool"].to(DEV)
+    t = to_dev(sd, DEV)
+    out = torch.full((w.N, w.H, w.dv), float("nan"), device=DEV, dtype=in_dtype)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for gated in (False, True):
+        pool = pd["pool"].to(DEV)
+        kda_gpu.kda_decode_step(t["q"], t["k"], t["v"], t["g"], t["beta"], idx.to(DEV), pool, out,
+                                gate=t["gate"] if gated else None,
+                                norm_w=pd["norm_w"].to(DEV) if gated else None, eps=pd["eps"],
+                                dev_status=status)
+        torch.cuda.synchronize()
+        y_ref, p_ref = oracle.decode(sd["q"], sd["k"], sd["v"], sd["g"], sd["beta"], idx,
+                                     pd["pool"], gate=sd["gate"] if gated else None,
+                                     norm_w=pd["norm_w"] if gated else None, eps=pd["eps"])
+        tol = tol_for(state_dtype)
+        assert int(status.item()) == 0
+        assert excess_error(out, y_ref) <= tol
+        assert torch.count_nonzero(out[4].float()).item() == 0
+        assert excess_error(pool, p_ref) <= tol
+
+
+@pytest.mark.parametrize("dv", [16, 64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("inplace", [False, True])
+def test_norm_gate(kda_gpu, dv, dtype, inplace):
+    gen = torch.Generator().manual_seed(dv)
+    o = torch.randn(37, 5, dv, generator=gen).to(dtype)
+    gate = torch.randn(37, 5, dv, generator=gen).to(dtype)
+    w = (1 + 0.02 * torch.randn(dv, generator=gen)).to(dtype)
+    ref = oracle.norm_gate(o, gate, w, eps=1e-6)
+    od, gd, wd = o.to(DEV), gate.to(DEV), w.to(DEV)
+    y = od if inplace else torch.empty_like(od)
+    kda_gpu.kda_norm_gate(od, gd, wd, y, eps=1e-6)
+    torch.cuda.synchronize()
+    assert excess_error(y, ref) <= 1e-5 if dtype == torch.float32 else excess_error(y, ref) <= 1e-2
+    if not inplace:
+        assert torch.equal(od.cpu(), o)  # input preserved
+
+
+def test_graph_capture_replay(kda_gpu):
+    """A prefill and a decode step captured in one CUDA graph and replayed give
+    the eager results (the ABI makes no host sync or host read)."""
+    w = W.VARLEN
+    d = W.make_prefill(w)
+    t = to_dev(d, DEV)
+    out = torch.empty(w.T, w.H, w.dv, device=DEV, dtype=w.in_dtype)
+    pool_init = t["pool"].clone()
+    dw = W.DECODE.replace(N=4, H=w.H, dk=w.dk, dv=w.dv, num_slots=w.num_slots)
+    sd = to_dev(W.make_decode_step(dw, 0), DEV)
+    dout = torch.empty(dw.N, dw.H, dw.dv, device=DEV, dtype=dw.in_dtype)
+    didx = torch.tensor([0, 5, 9, 15], dtype=torch.int32, device=DEV)
+    nw = torch.ones(w.dv, device=DEV, dtype=w.in_dtype)
+
+    def step(stream=None):
+        kda_gpu.kda_prefill_chunked(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"],
+                                    t["state_indices"], t["pool"], out, chunk=w.chunk,
+                                    scale=d["scale"], stream=stream)
+        kda_gpu.kda_decode_step(sd["q"], sd["k"], sd["v"], sd["g"], sd["beta"], didx, t["pool"],
+                                dout, gate=sd["gate"], norm_w=nw, stream=stream)
+
+    step()
+    torch.cuda.synchronize()
+    out_e, dout_e, pool_e = out.clone(), dout.clone(), t["pool"].clone()
+    t["pool"].copy_(pool_init)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            step(stream=s)
+    torch.cuda.synchronize()
+    t["pool"].copy_(pool_init)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_e) and torch.equal(dout, dout_e) and torch.equal(t["pool"], pool_e)
