@@ -1,0 +1,424 @@
+"""libkda benchmark: KDA prefill tokens/s and decode seq-steps/s on one GB300.
+
+Workloads (seeded synthetic inputs, no dataset):
+  prefill  scheduler step -- 4096 tokens as 8 sequences (min 64), H=32,
+           dk=dv=128, bf16 inputs, fp32 512-slot pool (slots from the top half),
+           chunk 64, checkpoints every 256 tokens, fused RMSNorm-gate.
+  decode   256 sequences x 1 token, H=32, dk=dv=128, bf16 inputs, fp32
+           1024-slot pool, fused RMSNorm-gate.
+A step is one prefill call followed by one decode step; each is timed in its
+own loop with CUDA events on the launching stream, the L2 flushed (a 256 MiB
+write) before every timed prefill call (the decode step streams 1.07 GB, far
+above L2).  ``value`` is prefill tokens/s; the decode figures sit under
+``decode``.  ``--impl reference`` times the fp64 CPU oracle on the same
+workload instead.  Under torchrun each rank runs an independent replica (the
+path has no exchange step) and rank 0 reports the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "KDA prefill tokens/s + decode seq-steps/s on 1 GB300; % of tensor/HBM roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def prefill_algorithmic(w, d):
+    """Bytes every prefill call must move, and its FLOPs (triangular-aware)."""
+    T, H, dk, dv, C = w.T, w.H, w.dk, w.dv, w.chunk
+    ib = 2 if w.in_dtype == torch.bfloat16 else 4
+    sb = 2 if w.state_dtype == torch.bfloat16 else 4
+    lens = [int(x) for x in (d["cu_seqlens"][1:] - d["cu_seqlens"][:-1]).tolist()]
+    n_ck = sum(L // w.checkpoint_every for L in lens) if w.checkpoint_every else 0
+    n_seq = sum(1 for L in lens if L > 0)
+    b = T * H * (2 * dk + dk + dv) * ib            # q, k, g, v
+    b += T * H * ib                                 # beta
+    b += T * H * dv * ib                            # out
+    if w.gate:
+        b += T * H * dv * ib + dv * ib              # gate, norm weight
+    b += 2 * n_seq * H * dk * dv * sb               # state read + write
+    b += n_ck * H * dk * dv * sb                    # checkpoints
+    # FLOPs per chunk-head with n rows: decay-weighted KK^T and QK^T (2 n^2 dk
+    # halves), the solve and the six n x d x d / n x n x d products.
+    fl = 0
+    for L in lens:
+        for c0 in range(0, L, C):
+            n = min(C, L - c0)
+            tri = n * (n + 1) / 2
+            fl += H * (2 * 2 * tri * dk          # A_kk, A_qk
+                       + 2 * tri * dv            # A_qk U
+                       + n * n * n / 3           # forward substitution
+                       + 2 * n * dk * dv * 3     # K S, Q S, K^T U
+                       + 4 * n * dk)             # decay scaling
+    return int(b), float(fl)
+
+
+def decode_algorithmic(w):
+    ib = 2 if w.in_dtype == torch.bfloat16 else 4
+    sb = 2 if w.state_dtype == torch.bfloat16 else 4
+    b = 2 * w.N * w.H * w.dk * w.dv * sb
+    b += w.N * w.H * (3 * w.dk + w.dv + 1 + w.dv) * ib  # q k g v beta out
+    if w.gate:
+        b += w.N * w.H * w.dv * ib + w.dv * ib
+    b += w.N * 4
+    fl = w.N * w.H * (7 * w.dk * w.dv)
+    return int(b), float(fl)
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import linear_attention_prefill_kda_gb300 as kda
+    ws, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    kda.load()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pk = peaks()
+
+    # ---------------- prefill (scheduler step)
+    w = W.SCHED
+    d = W.make_prefill(w)
+    t = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    T = w.T
+    cap = T // w.checkpoint_every
+    ck = torch.empty(cap, w.H, w.dk, w.dv, device=dev, dtype=w.state_dtype)
+    offs = torch.empty(w.N + 1, dtype=torch.int32, device=dev)
+    out = torch.empty(T, w.H, w.dv, device=dev, dtype=w.in_dtype)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    wsb = kda.kda_prefill_workspace_bytes(w.N, T, w.H, w.dk, w.dv, w.chunk)
+    wspace = torch.empty(wsb, dtype=torch.uint8, device=dev) if wsb else None
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def prefill_call(src=t, o=out):
+        kda.kda_prefill_chunked(src["q"], src["k"], src["v"], src["g"], src["beta"],
+                                t["cu_seqlens"], t["state_indices"], t["pool"], o, chunk=w.chunk,
+                                checkpoints=ck, checkpoint_every=w.checkpoint_every,
+                                ckpt_offsets=offs, gate=src["gate"], norm_w=t["norm_w"],
+                                eps=d["eps"], scale=d["scale"], workspace=wspace,
+                                dev_status=status, stream=stream)
+
+    # ---------------- decode
+    dw = W.DECODE
+    pd = W.make_decode_pool(dw)
+    dpool = pd["pool"].to(dev)
+    didx = pd["state_indices"].to(dev)
+    dnw = pd["norm_w"].to(dev)
+    dsteps = [{k: v.to(dev) for k, v in W.make_decode_step(dw, s).items()} for s in range(4)]
+    dout = torch.empty(dw.N, dw.H, dw.dv, device=dev, dtype=dw.in_dtype)
+
+    def decode_call(i):
+        s = dsteps[i % len(dsteps)]
+        kda.kda_decode_step(s["q"], s["k"], s["v"], s["g"], s["beta"], didx, dpool, dout,
+                            gate=s["gate"], norm_w=dnw, eps=pd["eps"], dev_status=status,
+                            stream=stream)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        prefill_call()
+        decode_call(0)
+    barrier()
+
+    with ClockSampler(local) as clk:
+        # prefill: per-iteration events around the call, L2 flushed before each
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            prefill_call()
+            ends[i].record(stream)
+        barrier()
+        pre_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        # decode: back-to-back steps (each streams 1.07 GB through HBM)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        e0.record(stream)
+        for i in range(args.steps):
+            decode_call(i)
+        e1.record(stream)
+        barrier()
+        dec_ms_total = e0.elapsed_time(e1)
+    clocks = clk.summary()
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {kda.DEV_STATUS.get(st)}")
+
+    pre_ms_mean = sum(pre_ms) / len(pre_ms)
+    dec_ms = dec_ms_total / args.steps
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([pre_ms_mean, dec_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        pre_ms_mean, dec_ms = tt.tolist()
+
+    # ---------------- e2e through the public API with host buffers
+    names = ["q", "k", "v", "g", "beta", "gate"]
+    host = {k: d[k].pin_memory() for k in names}
+    staged = {k: torch.empty_like(t[k]) for k in names}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    d2h = out_host.numel() * out_host.element_size()
+    for _ in range(2):
+        for k in names:
+            staged[k].copy_(host[k], non_blocking=True)
+        prefill_call(staged)
+        out_host.copy_(out, non_blocking=True)
+    barrier()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.steps):
+        for k in names:
+            staged[k].copy_(host[k], non_blocking=True)
+        prefill_call(staged)
+        out_host.copy_(out, non_blocking=True)
+    x1.record(stream)
+    barrier()
+    e2e_ms = x0.elapsed_time(x1) / args.steps
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = tt.item()
+
+    pre_bytes, pre_flops = prefill_algorithmic(w, d)
+    dec_bytes, dec_flops = decode_algorithmic(dw)
+    pre_gbs = pre_bytes / (pre_ms_mean * 1e-3) / 1e9
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    pre_tflops = pre_flops / (pre_ms_mean * 1e-3) / 1e12
+    tokens_s = ws * T / (pre_ms_mean * 1e-3)
+    seqsteps_s = ws * dw.N / (dec_ms * 1e-3)
+    result = {
+        "metric": METRIC,
+        "value": round(tokens_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(pre_ms_mean + dec_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 in / f32 accumulate",
+        "data": "synthetic (seeded; distributions of the workload definitions)",
+        "config": {"workload": w.name, "prefill_tokens": T, "sequences": list(w.seqlens),
+                   "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
+                   "checkpoint_every": w.checkpoint_every, "state_dtype": "f32",
+                   "fused_norm_gate": True, "decode_workload": dw.name,
+                   "l2": "flushed (256 MiB write) before each timed prefill call; decode "
+                         "streams 1.07 GB per step (> L2)",
+                   "parallelism": f"replicas x{ws}"},
+        "prefill_ms": round(pre_ms_mean, 4),
+        "roofline": {"bound": "hbm", "achieved": round(pre_gbs, 1), "peak": pk["hbm"],
+                     "unit": "GB/s", "frac": round(pre_gbs / pk["hbm"], 4),
+                     "traffic": None, "peak_source": pk["source"],
+                     "algorithmic_bytes": pre_bytes, "algorithmic_flops": pre_flops,
+                     "achieved_tflops": round(pre_tflops, 2),
+                     "tensor_frac_of_bf16_peak": round(pre_tflops / pk["bf16"], 4)},
+        "decode": {"value": round(seqsteps_s, 1), "unit": "seq-steps/s",
+                   "ms_per_step": round(dec_ms, 4),
+                   "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": pk["hbm"],
+                                "unit": "GB/s", "frac": round(dec_gbs / pk["hbm"], 4),
+                                "traffic": None, "algorithmic_bytes": dec_bytes}},
+        "e2e": {"value": round(ws * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (prefill_launches(kda, w) + 1),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, d, budget_s=args.cpu_seconds)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+def prefill_launches(kda, w) -> int:
+    """Kernels one prefill call launches (the norm-gate is a second launch when
+    the prefill kernel does not fuse it)."""
+    import linear_attention_prefill_kda_gb300 as k
+    return int(getattr(k, "PREFILL_LAUNCHES", lambda w: 2)(w))
+
+
+# ----------------------------------------------------------------- CPU oracle
+def _compact(d):
+    """The workload with its pool reduced to the slots it touches (the oracle
+    widens the pool to fp64; untouched slots do not enter the arithmetic)."""
+    idx = d["state_indices"].long()
+    dd = dict(d)
+    dd["pool"] = d["pool"][idx].clone()
+    dd["state_indices"] = torch.arange(len(idx), dtype=torch.int32)
+    return dd
+
+
+def _oracle_prefill_once(w, dd, nthreads=0):
+    import oracle
+    return oracle.prefill(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["cu_seqlens"],
+                          dd["state_indices"], dd["pool"], checkpoint_every=w.checkpoint_every,
+                          gate=dd["gate"], norm_w=dd["norm_w"], eps=dd["eps"], scale=dd["scale"],
+                          nthreads=nthreads)
+
+
+def cpu_baseline(w, d, budget_s=15.0):
+    import oracle
+    dd = _compact(d)
+    cores = oracle.max_threads()
+    n, t_total = 0, 0.0
+    while t_total < budget_s and n < 50:
+        t0 = time.perf_counter()
+        _oracle_prefill_once(w, dd)
+        t_total += time.perf_counter() - t0
+        n += 1
+    return {"value": round(n * w.T / t_total, 1), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n} full calls of {w.name} (fp64 C oracle, OpenMP over (sequence, head), "
+                      f"pool reduced to the 8 touched slots), {t_total:.1f} s on "
+                      f"{os.cpu_count()} host cores"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    w = W.SCHED
+    d = W.make_prefill(w)
+    dd = _compact(d)
+    for _ in range(args.warmup):
+        _oracle_prefill_once(w, dd)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _oracle_prefill_once(w, dd)
+        times.append(time.perf_counter() - t0)
+    mean = sum(times) / len(times)
+    val = w.T / mean
+    cores = oracle.max_threads()
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(val, 1), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "prefill_tokens": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                   "chunk": w.chunk, "checkpoint_every": w.checkpoint_every},
+        "cpu_baseline": {"value": round(val, 1), "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"each step one full {w.name} call (fp64 C oracle, pool reduced "
+                                   f"to the touched slots)"},
+        "e2e": {"value": round(val, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["libkda", "reference"], default="libkda")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -29,7 +29,8 @@ struct NormGateParams {
   int64_t rows;  // token rows; each holds H heads of dv
   int H, dv;
   float eps;
-  kda_dtype dtype;
+  kda_dtype dtype;  // of gate, w and y (and of o unless o_f32)
+  bool o_f32;       // o is fp32 scratch regardless of dtype
 };
 
 struct PrefillParams {
@@ -43,6 +44,7 @@ struct PrefillParams {
   const void *gate, *norm_w;
   void* workspace;
   size_t workspace_bytes;
+  float* o_scratch;  // when set, the prefill kernel writes raw o here in fp32
   int32_t* dev_status;
   int64_t T, num_slots, checkpoint_capacity;
   int N, H, dk, dv, chunk, checkpoint_every;

@@ -10,7 +10,9 @@
 namespace kda {
 namespace {
 
-template <int DV, typename T>
+// o is read as TO (the ABI dtype, or fp32 when the prefill kept its raw
+// output in fp32 scratch); gate, w and y are T.
+template <int DV, typename T, typename TO>
 __global__ void __launch_bounds__(256) norm_gate_kernel(NormGateParams p) {
   constexpr int LANES = DV / 4;  // active lanes, 4 elements each
   static_assert(DV % 4 == 0 && LANES <= 32, "dv must be a multiple of 4 and <= 128");
@@ -18,7 +20,7 @@ __global__ void __launch_bounds__(256) norm_gate_kernel(NormGateParams p) {
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int64_t nrows = p.rows * p.H;
   if (row >= nrows) return;
-  const T* o = reinterpret_cast<const T*>(p.o) + row * DV;
+  const TO* o = reinterpret_cast<const TO*>(p.o) + row * DV;
   const T* gt = reinterpret_cast<const T*>(p.gate) + row * DV;
   T* y = reinterpret_cast<T*>(p.y) + row * DV;
   float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -43,9 +45,11 @@ cudaError_t launch_ng_d(const NormGateParams& p, cudaStream_t stream) {
   const int64_t blocks = (nrows + 7) / 8;
   if (blocks == 0) return cudaSuccess;
   if (p.dtype == KDA_F32)
-    norm_gate_kernel<DV, float><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    norm_gate_kernel<DV, float, float><<<(unsigned)blocks, 256, 0, stream>>>(p);
+  else if (p.o_f32)
+    norm_gate_kernel<DV, bf16, float><<<(unsigned)blocks, 256, 0, stream>>>(p);
   else
-    norm_gate_kernel<DV, bf16><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    norm_gate_kernel<DV, bf16, bf16><<<(unsigned)blocks, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -32,17 +32,30 @@ cudaError_t set_smem_once(const void* kernel, int bytes) {
   return cudaSuccess;
 }
 
+// The CUDA-core kernel splits dv into slabs of 64 columns, so the norm-gate
+// runs as a second pass.  With bf16 inputs the raw output is kept in fp32
+// scratch (T x H x dv floats) for that pass, so that it is not rounded to
+// bf16 before normalisation.
+static bool needs_o_scratch(int dv, kda_dtype in_dtype) { (void)dv; return in_dtype != KDA_F32; }
+
 size_t prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk) {
-  (void)N; (void)T; (void)H; (void)dk; (void)dv; (void)chunk;
-  return 0;
+  (void)N; (void)dk; (void)chunk;
+  if (!needs_o_scratch(dv, KDA_BF16)) return 0;
+  const size_t bytes = (size_t)T * (size_t)H * (size_t)dv * sizeof(float);
+  return (bytes + 255) & ~(size_t)255;
 }
 
-cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream) {
+cudaError_t launch_prefill(const PrefillParams& p_in, cudaStream_t stream) {
+  PrefillParams p = p_in;
+  const bool scratch = p.gate && p.T > 0 && needs_o_scratch(p.dv, p.in_dtype);
+  p.o_scratch = scratch ? reinterpret_cast<float*>(p.workspace) : nullptr;
   cudaError_t e = launch_prefill_simt(p, stream);
   if (e != cudaSuccess) return e;
   if (p.gate && p.T > 0) {
     NormGateParams ng{};
-    ng.o = p.out; ng.gate = p.gate; ng.w = p.norm_w; ng.y = p.out;
+    ng.o = scratch ? static_cast<const void*>(p.o_scratch) : p.out;
+    ng.o_f32 = scratch;
+    ng.gate = p.gate; ng.w = p.norm_w; ng.y = p.out;
     ng.rows = p.T; ng.H = p.H; ng.dv = p.dv; ng.eps = p.eps; ng.dtype = p.in_dtype;
     e = launch_norm_gate(ng, stream);
   }

@@ -230,9 +230,14 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(PrefillParams p)
       for (int a = 0; a < RM; ++a) {
         const int r = ty + 16 * a;
         if (r < n) {
-          TI* dst = gout + ((t0 + c0 + r) * H + head) * DV + v0 + tx * RN;
+          const int64_t off = ((t0 + c0 + r) * H + head) * DV + v0 + tx * RN;
+          if (p.o_scratch) {
 #pragma unroll
-          for (int b = 0; b < RN; ++b) dst[b] = from_f32<TI>(p.scale * acc[a][b]);
+            for (int b = 0; b < RN; ++b) p.o_scratch[off + b] = p.scale * acc[a][b];
+          } else {
+#pragma unroll
+            for (int b = 0; b < RN; ++b) gout[off + b] = from_f32<TI>(p.scale * acc[a][b]);
+          }
         }
       }
     }
