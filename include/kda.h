@@ -70,9 +70,11 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 #define KDA_DEV_CKPT_OVERFLOW 4   /* checkpoints would exceed checkpoint_capacity */
 
 /*
- * Bytes of caller-owned scratch kda_prefill_chunked needs for these sizes
- * (the pages' "reusable caller-owned scratch").  May be 0.  The same
- * workspace can be reused by consecutive calls on one stream.
+ * Bytes of caller-owned scratch that always suffice for kda_prefill_chunked
+ * with these sizes (the pages' "reusable caller-owned scratch"), whatever the
+ * dtypes and the gate option.  A call may need less (or none); it returns
+ * KDA_ERR_WORKSPACE when what it needs is not provided.  The same workspace
+ * can be reused by consecutive calls on one stream.
  */
 KDA_API size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk);
 

@@ -70,7 +70,7 @@ kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, cons
     if (!ptr_ok(checkpoints, true)) return KDA_ERR_INVALID_ARG;
     if (checkpoint_capacity < T / checkpoint_every) return KDA_ERR_INVALID_ARG;
   }
-  const size_t need = kda::prefill_workspace_bytes(N, T, H, dk, dv, chunk);
+  const size_t need = kda::prefill_workspace_needed(N, T, H, dk, dv, chunk, in_dtype, gate != nullptr);
   if (need > 0 && (workspace_bytes < need || !ptr_ok(workspace, true))) return KDA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (N == 0) {

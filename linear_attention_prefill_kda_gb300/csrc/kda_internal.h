@@ -60,6 +60,10 @@ cudaError_t set_smem_once(const void* kernel, int bytes);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_norm_gate(const NormGateParams& p, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
+// Upper bound over every option (what kda_prefill_workspace_bytes reports).
 size_t prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk);
+// What one call with these options actually uses (<= the bound).
+size_t prefill_workspace_needed(int N, int64_t T, int H, int dk, int dv, int chunk, kda_dtype in_dtype,
+                                bool gate);
 
 }  // namespace kda

@@ -45,6 +45,12 @@ size_t prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chun
   return (bytes + 255) & ~(size_t)255;
 }
 
+size_t prefill_workspace_needed(int N, int64_t T, int H, int dk, int dv, int chunk, kda_dtype in_dtype,
+                                bool gate) {
+  if (!gate || !needs_o_scratch(dv, in_dtype)) return 0;
+  return prefill_workspace_bytes(N, T, H, dk, dv, chunk);
+}
+
 cudaError_t launch_prefill(const PrefillParams& p_in, cudaStream_t stream) {
   PrefillParams p = p_in;
   const bool scratch = p.gate && p.T > 0 && needs_o_scratch(p.dv, p.in_dtype);
