@@ -328,10 +328,8 @@ def run_gpu(args):
 
 
 def prefill_launches(kda, w) -> int:
-    """Kernels one prefill call launches (the norm-gate is a second launch when
-    the prefill kernel does not fuse it)."""
-    import linear_attention_prefill_kda_gb300 as k
-    return int(getattr(k, "PREFILL_LAUNCHES", lambda w: 2)(w))
+    """Kernels one prefill call launches."""
+    return int(kda.prefill_launches(w.dk, w.dv, w.chunk, w.in_dtype, w.gate))
 
 
 # ----------------------------------------------------------------- CPU oracle

@@ -17,7 +17,7 @@ import torch
 __all__ = [
     "load", "lib_path", "KdaError", "KDA_OK", "KDA_F32", "KDA_BF16",
     "kda_prefill_chunked", "kda_prefill_workspace_bytes", "kda_decode_step", "kda_norm_gate",
-    "kda_status_string", "kda_version", "DEV_STATUS",
+    "kda_status_string", "kda_version", "DEV_STATUS", "prefill_launches",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -109,6 +109,15 @@ def kda_version() -> int:
 
 def kda_prefill_workspace_bytes(N: int, T: int, H: int, dk: int, dv: int, chunk: int) -> int:
     return int(load().kda_prefill_workspace_bytes(N, T, H, dk, dv, chunk))
+
+
+def prefill_launches(dk: int, dv: int, chunk: int, in_dtype, gate: bool) -> int:
+    """Kernel launches one kda_prefill_chunked call makes: the tensor-core path
+    (dk = dv = 128, chunk 64, bf16) runs an intra-chunk and a state kernel; the
+    CUDA-core path runs one kernel plus a norm-gate pass when gated."""
+    if dk == 128 and dv == 128 and chunk == 64 and in_dtype == torch.bfloat16:
+        return 2
+    return 2 if gate else 1
 
 
 def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, *,

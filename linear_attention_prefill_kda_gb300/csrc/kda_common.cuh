@@ -71,4 +71,11 @@ __device__ __forceinline__ void latch_status(int32_t* status, int code) {
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
 
+// Floor applied to the per-token log-decay g by the chunked prefill kernels.
+// exp(-30) = 9.4e-14, so a token below the floor still erases the history to
+// within 1e-13 of the state; the floor keeps the in-chunk prefix sums of g
+// bounded (|G| <= 30 * chunk) so that their fp32 rounding stays ~1e-4 in the
+// exponent instead of swallowing the small decays that follow a huge one.
+constexpr float kLogDecayFloor = -30.0f;
+
 }  // namespace kda

@@ -9,6 +9,15 @@
 namespace kda {
 
 cudaError_t launch_prefill_simt(const PrefillParams& p, cudaStream_t stream);
+bool prefill_tc_supported(const PrefillParams& p);
+size_t prefill_tc_workspace_bytes(int N, int64_t T, int H);
+cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream);
+
+static bool tc_shape(int dk, int dv, int chunk, kda_dtype in_dtype) {
+  PrefillParams q{};
+  q.dk = dk; q.dv = dv; q.chunk = chunk; q.in_dtype = in_dtype;
+  return prefill_tc_supported(q);
+}
 
 cudaError_t set_smem_once(const void* kernel, int bytes) {
   constexpr int kMaxEntries = 256;
@@ -39,19 +48,23 @@ cudaError_t set_smem_once(const void* kernel, int bytes) {
 static bool needs_o_scratch(int dv, kda_dtype in_dtype) { (void)dv; return in_dtype != KDA_F32; }
 
 size_t prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk) {
-  (void)N; (void)dk; (void)chunk;
-  if (!needs_o_scratch(dv, KDA_BF16)) return 0;
-  const size_t bytes = (size_t)T * (size_t)H * (size_t)dv * sizeof(float);
+  size_t bytes = (size_t)T * (size_t)H * (size_t)dv * sizeof(float);  // raw-output scratch
+  if (tc_shape(dk, dv, chunk, KDA_BF16)) {
+    const size_t tc = prefill_tc_workspace_bytes(N, T, H);
+    if (tc > bytes) bytes = tc;
+  }
   return (bytes + 255) & ~(size_t)255;
 }
 
 size_t prefill_workspace_needed(int N, int64_t T, int H, int dk, int dv, int chunk, kda_dtype in_dtype,
                                 bool gate) {
+  if (tc_shape(dk, dv, chunk, in_dtype)) return prefill_tc_workspace_bytes(N, T, H);
   if (!gate || !needs_o_scratch(dv, in_dtype)) return 0;
-  return prefill_workspace_bytes(N, T, H, dk, dv, chunk);
+  return ((size_t)T * (size_t)H * (size_t)dv * sizeof(float) + 255) & ~(size_t)255;
 }
 
 cudaError_t launch_prefill(const PrefillParams& p_in, cudaStream_t stream) {
+  if (prefill_tc_supported(p_in)) return launch_prefill_tc(p_in, stream);
   PrefillParams p = p_in;
   const bool scratch = p.gate && p.T > 0 && needs_o_scratch(p.dv, p.in_dtype);
   p.o_scratch = scratch ? reinterpret_cast<float*>(p.workspace) : nullptr;

@@ -19,7 +19,7 @@
 // o_t = scale S_t^T q_t exactly in exact arithmetic.  State pool indexing,
 // padding and checkpoints follow the ABI contract in kda.h.
 //
-// Launch: one CTA per (value slab of BV columns, head, sequence); the columns
+// Launch: one CTA per (sequence, head, value slab of BV columns); the columns
 // of S evolve independently given q, k, g, beta, so slabs need no exchange.
 #include "kda_common.cuh"
 #include "kda_internal.h"
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(PrefillParams p)
 
   const int tid = threadIdx.x;
   const int ty = tid / 16, tx = tid % 16;
-  const int slab = blockIdx.x, head = blockIdx.y, seq = blockIdx.z;
+  const int seq = blockIdx.x, head = blockIdx.y, slab = blockIdx.z;
   const int v0 = slab * BV;
   const int H = p.H;
 
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(PrefillParams p)
         const int64_t off = ((t0 + c0 + r) * H + head) * DK + c;
         kv = to_f32(gk[off]);
         qv = to_f32(gq[off]);
-        gvv = to_f32(gg[off]);
+        gvv = fmaxf(to_f32(gg[off]), kLogDecayFloor);
       }
       sK[r * L::LDK + c] = kv;
       sQ[r * L::LDK + c] = qv;
@@ -296,7 +296,7 @@ cudaError_t launch_simt_t(const PrefillParams& p, cudaStream_t stream) {
   auto kern = prefill_simt_kernel<D, D, C, BV, TI, TS>;
   const cudaError_t attr = set_smem_once(reinterpret_cast<const void*>(kern), (int)L::BYTES);
   if (attr != cudaSuccess) return attr;
-  dim3 grid(D / BV, p.H, p.N);
+  dim3 grid(p.N, p.H, D / BV);
   kern<<<grid, kThreads, L::BYTES, stream>>>(p);
   return cudaGetLastError();
 }

@@ -76,16 +76,27 @@ def test_prefill_edge_lengths(kda_gpu, chunk, d, state_dtype):
     assert torch.count_nonzero(out[t0:t1].float()).item() == 0  # padding rows exactly zero
 
 
+def test_prefill_tc_shape_mixed(kda_gpu):
+    """The tensor-core shape (d=128, chunk 64, bf16) with short, partial and
+    multi-chunk sequences, bf16 state, checkpoints and the fused norm-gate."""
+    w = W.SCHED.replace(seqlens=(1, 63, 64, 65, 0, 200, 511), H=4, num_slots=16, slot_range=None,
+                        state_dtype=torch.bfloat16, checkpoint_every=128, seed=123)
+    _check_prefill(kda_gpu, w, W.make_prefill(w))
+
+
 def test_prefill_gate_fp32_and_chunk16(kda_gpu):
     w = W.SCHED.replace(seqlens=(100, 37, 256), H=4, dk=64, dv=64, chunk=16, checkpoint_every=32,
                         in_dtype=torch.float32, num_slots=8, slot_range=None, seed=77)
     _check_prefill(kda_gpu, w, W.make_prefill(w))
 
 
-def test_prefill_extreme_decay(kda_gpu):
+@pytest.mark.parametrize("d,in_dtype", [(64, torch.float32), (128, torch.bfloat16)])
+def test_prefill_extreme_decay(kda_gpu, d, in_dtype):
     """g = -1e30 on some tokens (alpha = 0 exactly) must erase history without
-    producing inf/nan."""
-    w = W.VARLEN.replace(seqlens=(130,), H=2, in_dtype=torch.float32, seed=91, checkpoint_every=0)
+    producing inf/nan (the d=128 bf16 case exercises the exact fallback of the
+    factorised decay in the tensor-core path)."""
+    w = W.VARLEN.replace(seqlens=(130, 70), H=2, dk=d, dv=d, in_dtype=in_dtype, seed=91,
+                         checkpoint_every=0)
     d = W.make_prefill(w)
     d["g"][10] = -1e30
     d["g"][64, :, :5] = -1e30
@@ -122,6 +133,8 @@ def test_prefill_longprompt_bf16_state(kda_gpu):
     idx = d["state_indices"].to(DEV)
     outs, cks = [], []
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(kda_gpu.kda_prefill_workspace_bytes(1, seg, w.H, w.dk, w.dv, w.chunk),
+                     dtype=torch.uint8, device=DEV)
     for c in range(T // seg):
         sl = slice(c * seg, (c + 1) * seg)
         t = {k: d[k][sl].to(DEV) for k in ("q", "k", "v", "g", "beta")}
@@ -130,7 +143,8 @@ def test_prefill_longprompt_bf16_state(kda_gpu):
         kda_gpu.kda_prefill_chunked(t["q"], t["k"], t["v"], t["g"], t["beta"],
                                     W.cu_from_lengths([seg]).to(DEV), idx, dev_pool, out,
                                     chunk=w.chunk, checkpoints=ck,
-                                    checkpoint_every=w.checkpoint_every, dev_status=status)
+                                    checkpoint_every=w.checkpoint_every, workspace=ws,
+                                    dev_status=status)
         outs.append(out)
         cks.append(ck)
     torch.cuda.synchronize()
@@ -242,13 +256,16 @@ def test_norm_gate(kda_gpu, dv, dtype, inplace):
         assert torch.equal(od.cpu(), o)  # input preserved
 
 
-def test_graph_capture_replay(kda_gpu):
+@pytest.mark.parametrize("dim", [64, 128])
+def test_graph_capture_replay(kda_gpu, dim):
     """A prefill and a decode step captured in one CUDA graph and replayed give
     the eager results (the ABI makes no host sync or host read)."""
-    w = W.VARLEN
+    w = W.VARLEN.replace(dk=dim, dv=dim)
     d = W.make_prefill(w)
     t = to_dev(d, DEV)
     out = torch.empty(w.T, w.H, w.dv, device=DEV, dtype=w.in_dtype)
+    wsb = kda_gpu.kda_prefill_workspace_bytes(w.N, w.T, w.H, w.dk, w.dv, w.chunk)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=DEV)
     pool_init = t["pool"].clone()
     dw = W.DECODE.replace(N=4, H=w.H, dk=w.dk, dv=w.dv, num_slots=w.num_slots)
     sd = to_dev(W.make_decode_step(dw, 0), DEV)
@@ -259,7 +276,7 @@ def test_graph_capture_replay(kda_gpu):
     def step(stream=None):
         kda_gpu.kda_prefill_chunked(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"],
                                     t["state_indices"], t["pool"], out, chunk=w.chunk,
-                                    scale=d["scale"], stream=stream)
+                                    scale=d["scale"], workspace=ws, stream=stream)
         kda_gpu.kda_decode_step(sd["q"], sd["k"], sd["v"], sd["g"], sd["beta"], didx, t["pool"],
                                 dout, gate=sd["gate"], norm_w=nw, stream=stream)
 
