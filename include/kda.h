@@ -152,6 +152,30 @@ KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, 
 KDA_API kda_status kda_norm_gate(const void* o, const void* gate, const void* w, float eps, void* y,
                          int64_t rows, int H, int dv, kda_dtype dtype, void* stream);
 
+/*
+ * Chunked prefill without caller scratch.  The pages have no counterpart of
+ * this entry point; it serves callers that cannot allocate device memory where
+ * they run the prefill (for example code running under strict-mode stream
+ * capture, where cudaMalloc is an error, or runtimes confined to a fixed
+ * memory arena).  Arguments and results are those of kda_prefill_chunked,
+ * minus the workspace: the library uses its own device array of
+ * KDA_STATIC_SCRATCH_BYTES bytes instead, which every GPU that loads the
+ * library holds until the process exits.  A call whose scratch need
+ * (kda_prefill_workspace_bytes bounds it) exceeds that size returns
+ * KDA_ERR_WORKSPACE without launching.  The first call on each device looks up
+ * the array's device address and caches it, so make that first call before
+ * any stream capture starts.  Every call shares the array: calls whose kernels
+ * overlap on the GPU (different streams, or different host threads) race on it
+ * and must be serialised by the caller.  No allocation happens in this call.
+ */
+#define KDA_STATIC_SCRATCH_BYTES ((size_t)128 << 20)
+KDA_API kda_status kda_prefill_chunked_static_scratch(
+    const void* q, const void* k, const void* v, const void* g, const void* beta, kda_dtype in_dtype,
+    const int32_t* cu_seqlens, int N, int64_t T, const int32_t* state_indices, void* state_pool,
+    int64_t num_slots, kda_dtype state_dtype, void* out, void* checkpoints, int32_t checkpoint_every,
+    int64_t checkpoint_capacity, int32_t* ckpt_offsets, const void* gate, const void* norm_w, float eps,
+    int H, int dk, int dv, int chunk, float scale, int32_t* dev_status, void* stream);
+
 /* A static, human-readable name for a kda_status value. */
 KDA_API const char* kda_status_string(kda_status status);
 

@@ -18,6 +18,7 @@ __all__ = [
     "load", "lib_path", "KdaError", "KDA_OK", "KDA_F32", "KDA_BF16",
     "kda_prefill_chunked", "kda_prefill_workspace_bytes", "kda_decode_step", "kda_norm_gate",
     "kda_status_string", "kda_version", "DEV_STATUS", "prefill_launches",
+    "kda_prefill_chunked_static_scratch", "STATIC_SCRATCH_BYTES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -25,6 +26,7 @@ _LIB_PATH = os.path.join(_HERE, "libkda.so")
 _lib = None
 
 KDA_OK, KDA_F32, KDA_BF16 = 0, 0, 1
+STATIC_SCRATCH_BYTES = 128 << 20  # KDA_STATIC_SCRATCH_BYTES in include/kda.h
 DEV_STATUS = {0: "ok", 1: "bad state index", 2: "bad cu_seqlens", 3: "on-chip wait timeout",
               4: "checkpoint capacity exceeded"}
 
@@ -43,6 +45,10 @@ _SIGNATURES = {
         _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int, _F32, _P, _P]),
     "kda_norm_gate": (ctypes.c_int, [_P, _P, _P, _F32, _P, _I64, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, _P]),
+    "kda_prefill_chunked_static_scratch": (ctypes.c_int, [
+        _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _I64, _P, _P, _I64, ctypes.c_int, _P,
+        _P, _I32, _I64, _P, _P, _P, _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        _F32, _P, _P]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kda_version": (ctypes.c_int, []),
 }
@@ -139,6 +145,27 @@ def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_indices, state_pool,
         _ptr(norm_w), float(eps), H, dk, dv, int(chunk), float(scale), _ptr(workspace), ws_bytes,
         _ptr(dev_status), _stream(stream))
     _check(st, "kda_prefill_chunked")
+
+
+def kda_prefill_chunked_static_scratch(q, k, v, g, beta, cu_seqlens, state_indices, state_pool,
+                                       out, *, chunk: int = 64, checkpoints=None,
+                                       checkpoint_every: int = 0, ckpt_offsets=None, gate=None,
+                                       norm_w=None, eps: float = 1e-6, scale: float = 0.0,
+                                       dev_status=None, stream=None):
+    """kda_prefill_chunked for callers that cannot allocate: the library's own
+    device array (STATIC_SCRATCH_BYTES) replaces the workspace.  Calls share
+    that array, so calls that overlap on the GPU race; see include/kda.h."""
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = state_indices.shape[0]
+    cap = checkpoints.shape[0] if checkpoints is not None else 0
+    st = load().kda_prefill_chunked_static_scratch(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(cu_seqlens), N, T,
+        _ptr(state_indices), _ptr(state_pool), state_pool.shape[0], _dtype(state_pool), _ptr(out),
+        _ptr(checkpoints), int(checkpoint_every), cap, _ptr(ckpt_offsets), _ptr(gate),
+        _ptr(norm_w), float(eps), H, dk, dv, int(chunk), float(scale), _ptr(dev_status),
+        _stream(stream))
+    _check(st, "kda_prefill_chunked_static_scratch")
 
 
 def kda_decode_step(q, k, v, g, beta, state_indices, state_pool, out, *, gate=None, norm_w=None,

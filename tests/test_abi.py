@@ -118,3 +118,15 @@ def test_binding_refuses_missing_library(monkeypatch, tmp_path):
     monkeypatch.setattr(kda, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         kda.kda_version()
+
+
+def test_static_scratch_entry_rejects_oversize_on_host(lib):
+    """The no-allocation prefill refuses a problem whose scratch exceeds its
+    fixed array before touching the device."""
+    rc = lib.kda_prefill_chunked_static_scratch(
+        FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, 65536, FAKE, FAKE, 4, 0, FAKE, None, 0, 0, None,
+        None, None, 1e-6, 32, 128, 128, 64, 0.0, None, None)
+    assert rc == -3
+    assert lib.kda_prefill_chunked_static_scratch(
+        FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, 100, FAKE, FAKE, 4, 0, FAKE, None, 0, 0, None,
+        None, None, 1e-6, 2, 96, 96, 64, 0.0, None, None) == -2
