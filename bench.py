@@ -188,14 +188,19 @@ def run_gpu(args):
 
     # ---------------- decode
     dw = W.DECODE
-    pd = W.make_decode_pool(dw)
-    dpool = pd["pool"].to(dev)
-    didx = pd["state_indices"].to(dev)
-    dnw = pd["norm_w"].to(dev)
-    dsteps = [{k: v.to(dev) for k, v in W.make_decode_step(dw, s).items()} for s in range(4)]
-    dout = torch.empty(dw.N, dw.H, dw.dv, device=dev, dtype=dw.in_dtype)
+    with_decode = args.workload in ("both", "decode")
+    with_prefill = args.workload in ("both", "prefill")
+    if with_decode:
+        pd = W.make_decode_pool(dw)
+        dpool = pd["pool"].to(dev)
+        didx = pd["state_indices"].to(dev)
+        dnw = pd["norm_w"].to(dev)
+        dsteps = [{k: v.to(dev) for k, v in W.make_decode_step(dw, s).items()} for s in range(4)]
+        dout = torch.empty(dw.N, dw.H, dw.dv, device=dev, dtype=dw.in_dtype)
 
     def decode_call(i):
+        if not with_decode:
+            return
         s = dsteps[i % len(dsteps)]
         kda.kda_decode_step(s["q"], s["k"], s["v"], s["g"], s["beta"], didx, dpool, dout,
                             gate=s["gate"], norm_w=dnw, eps=pd["eps"], dev_status=status,
@@ -208,7 +213,8 @@ def run_gpu(args):
         torch.cuda.synchronize()
 
     for _ in range(args.warmup):
-        prefill_call()
+        if with_prefill:
+            prefill_call()
         decode_call(0)
     barrier()
 
@@ -217,13 +223,13 @@ def run_gpu(args):
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         barrier()
-        for i in range(args.steps):
+        for i in range(args.steps if with_prefill else 0):
             flush.fill_(float(i))
             starts[i].record(stream)
             prefill_call()
             ends[i].record(stream)
         barrier()
-        pre_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        pre_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)] if with_prefill else [float("nan")]
         # decode: back-to-back steps (each streams 1.07 GB through HBM)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
@@ -253,7 +259,7 @@ def run_gpu(args):
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(host[k].numel() * host[k].element_size() for k in names)
     d2h = out_host.numel() * out_host.element_size()
-    for _ in range(2):
+    for _ in range(2 if with_prefill else 0):
         for k in names:
             staged[k].copy_(host[k], non_blocking=True)
         prefill_call(staged)
@@ -261,7 +267,7 @@ def run_gpu(args):
     barrier()
     x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     x0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(args.steps if with_prefill else 0):
         for k in names:
             staged[k].copy_(host[k], non_blocking=True)
         prefill_call(staged)
@@ -277,11 +283,18 @@ def run_gpu(args):
 
     pre_bytes, pre_flops = prefill_algorithmic(w, d)
     dec_bytes, dec_flops = decode_algorithmic(dw)
-    pre_gbs = pre_bytes / (pre_ms_mean * 1e-3) / 1e9
-    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
-    pre_tflops = pre_flops / (pre_ms_mean * 1e-3) / 1e12
-    tokens_s = ws * T / (pre_ms_mean * 1e-3)
-    seqsteps_s = ws * dw.N / (dec_ms * 1e-3)
+    def rate(num, ms):  # per second; NaN when that part was not timed
+        return num / (ms * 1e-3) if ms and ms > 0 and ms == ms else float("nan")
+
+    if not with_decode:
+        dec_ms = float("nan")
+    if not with_prefill:
+        e2e_ms = float("nan")
+    pre_gbs = rate(pre_bytes, pre_ms_mean) / 1e9
+    dec_gbs = rate(dec_bytes, dec_ms) / 1e9
+    pre_tflops = rate(pre_flops, pre_ms_mean) / 1e12
+    tokens_s = rate(ws * T, pre_ms_mean)
+    seqsteps_s = rate(ws * dw.N, dec_ms)
     result = {
         "metric": METRIC,
         "value": round(tokens_s, 1),
@@ -289,7 +302,7 @@ def run_gpu(args):
         "n_gpus": ws,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(pre_ms_mean + dec_ms, 4),
+        "ms_per_step": round(sum(x for x in (pre_ms_mean, dec_ms) if x == x), 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -314,9 +327,9 @@ def run_gpu(args):
                    "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": pk["hbm"],
                                 "unit": "GB/s", "frac": round(dec_gbs / pk["hbm"], 4),
                                 "traffic": None, "algorithmic_bytes": dec_bytes}},
-        "e2e": {"value": round(ws * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(rate(ws * T, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (prefill_launches(kda, w) + 1),
+        "gpu_launches": args.steps * (prefill_launches(kda, w) * with_prefill + with_decode),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -402,6 +415,16 @@ def run_reference(args):
     }
 
 
+def _nan_to_none(x):
+    if isinstance(x, float) and x != x:
+        return None
+    if isinstance(x, dict):
+        return {k: _nan_to_none(v) for k, v in x.items()}
+    if isinstance(x, list):
+        return [_nan_to_none(v) for v in x]
+    return x
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -410,12 +433,14 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["libkda", "reference"], default="libkda")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["both", "prefill", "decode"], default="both",
+                    help="time both parts (default) or one of them (for profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
-        print(json.dumps(res), flush=True)
+        print(json.dumps(_nan_to_none(res)), flush=True)
 
 
 if __name__ == "__main__":

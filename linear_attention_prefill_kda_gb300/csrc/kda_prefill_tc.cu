@@ -46,7 +46,7 @@ constexpr int kThreads = 256;
 // ---- per (chunk slot, head) workspace block --------------------------------
 constexpr uint32_t WS_PA = 0;         // fp16 K-major [128 x 128] (SBO 2048): W rows 0-63, Q e^G rows 64-127
 constexpr uint32_t WS_KLT = 32768;    // fp16 MN-major [M=c 128 x K=j 64] (K stride 2048)
-constexpr uint32_t WS_U0 = 49152;     // fp16 row-major [64][128]
+constexpr uint32_t WS_U0 = 49152;     // fp16 [v/8][64 rows][8]: byte (v/8)*1024 + r*16 + (v%8)*2
 constexpr uint32_t WS_AQK = 65536;    // fp16 K-major [64 x 64] (SBO 1024)
 constexpr uint32_t WS_DECAY = 73728;  // fp32 [128]
 constexpr uint32_t WS_BYTES = 74240;
@@ -124,24 +124,34 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity) {
 // Kernel 1: intra-chunk terms, one CTA per (chunk slot, head)
 // =====================================================================
 namespace intra {
-constexpr uint32_t S_AROW_HI = 0;       // bf16 K-major [128 x 128] (SBO 2048)
+// One 96 KB region, reused phase by phase (two CTAs fit on an SM):
+//  phase 1 (cumulative gate as L G):
+constexpr uint32_t S_GOP = 0;           // bf16 MN-major [K=j 64 x N=c 128] raw g (K stride 2048)
+constexpr uint32_t S_LOP = 16384;       // bf16 K-major [128 x 64] (SBO 1024): L[m][j] = (j <= m % 64)
+//  phase 2 (decay-weighted K K^T and Q K^T):
+constexpr uint32_t S_AROW_HI = 0;       // bf16 K-major [128 x 128] (SBO 2048): K e^(G-Gm) ; Q e^(G-Gm)
 constexpr uint32_t S_AROW_LO = 32768;
-constexpr uint32_t S_BCOL_HI = 65536;   // bf16 K-major [64 x 128] (SBO 2048)
+constexpr uint32_t S_BCOL_HI = 65536;   // bf16 K-major [64 x 128] (SBO 2048): K e^(Gm-G)
 constexpr uint32_t S_BCOL_LO = 81920;
-constexpr uint32_t S_KW = 98304;        // bf16 MN-major [K=j 64 x N=c 128] (K stride 2048)
-constexpr uint32_t S_VB = 114688;       // bf16 MN-major [K=j 64 x N=v 128]
-constexpr uint32_t S_TP = 131072;       // bf16 K-major [128 x 64] (SBO 1024), rows 64-127 zero
-constexpr uint32_t S_END = 147456;
-// After the A product completes, the operand area [0, 98304) is reused:
+constexpr uint32_t S_REGION = 98304;
+//  phase 3 (solve and W, U0):
 constexpr uint32_t S_AKK = 0;           // fp32 [64][65]   beta-scaled strictly-lower A
 constexpr uint32_t S_TF = 16640;        // fp32 [64][65]   (I + A)^-1
 constexpr uint32_t S_MB = 33280;        // fp32 [3][16][17] block products of the solve
-// exact path scratch inside [0, S_KW): bf16 k, q [64][128], fp32 G [64][128],
-// fp32 A_kk, A_qk [64][64]
-constexpr uint32_t S_FK = 0, S_FQ = 16384, S_FG = 32768, S_FAKK = 65536, S_FAQK = 65536 + 16384;
-static_assert(S_FAQK + 16384 <= S_KW, "exact-path scratch must not reach the live operands");
-constexpr uint32_t SMEM_BYTES = S_END + 64 * 4 /*beta*/ + 4 * 64 * 4 /*carry*/ + 4 * 64 * 4 /*Gm*/ +
-                                4 * 64 * 4 /*Gl*/ + 64 /*misc*/;
+constexpr uint32_t S_KW = 49152;        // bf16 MN-major [K=j 64 x N=c 128]: K e^G
+constexpr uint32_t S_VB = 65536;        // bf16 MN-major [K=j 64 x N=v 128]: V
+constexpr uint32_t S_TP = 81920;        // bf16 K-major [128 x 64] (SBO 1024): T Diag(beta), rows 64-127 zero
+//  exact path (extreme decay) instead of phase 2:
+constexpr uint32_t S_FK = 0, S_FQ = 16384, S_FG = 32768, S_FAKK = 65536, S_FAQK = 81920;
+static_assert(S_MB + 3 * 16 * 17 * 4 <= S_KW, "solve scratch overlaps the W operand");
+// per-chunk scalars after the region
+constexpr uint32_t S_BETA = S_REGION;          // fp32 [64]
+constexpr uint32_t S_GM = S_BETA + 256;        // fp32 [128] G at the middle row m
+constexpr uint32_t S_GL = S_GM + 512;          // fp32 [128] G at the last row
+constexpr uint32_t S_EGM = S_GL + 512;         // fp32 [128] e^(G_m)
+constexpr uint32_t S_EGLM = S_EGM + 512;       // fp32 [128] e^(G_last - G_m)
+constexpr uint32_t S_MISC = S_EGLM + 512;      // int [4]
+constexpr uint32_t SMEM_BYTES = S_MISC + 64;
 }  // namespace intra
 
 // Element-wise exact A for chunks with extreme decay (rare): no factorisation.
@@ -163,14 +173,15 @@ __device__ void intra_exact_A(const bf16* fk, const bf16* fq, const float* fg, i
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) kda_intra_kernel(PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p) {
   using namespace intra;
   extern __shared__ __align__(1024) uint8_t sm[];
-  float* s_beta = reinterpret_cast<float*>(sm + S_END);
-  float* s_carry = s_beta + 64;       // [side*2+hh][64]
-  float* s_gm = s_carry + 4 * 64;     // [side*2+hh][64]
-  float* s_gl = s_gm + 4 * 64;        // [side*2+hh][64]
-  int* s_misc = reinterpret_cast<int*>(s_gl + 4 * 64);
+  float* s_beta = reinterpret_cast<float*>(sm + S_BETA);
+  float* s_gm = reinterpret_cast<float*>(sm + S_GM);
+  float* s_gl = reinterpret_cast<float*>(sm + S_GL);
+  float* s_egm = reinterpret_cast<float*>(sm + S_EGM);
+  float* s_eglm = reinterpret_cast<float*>(sm + S_EGLM);
+  int* s_misc = reinterpret_cast<int*>(sm + S_MISC);
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t s_tmem;
 
@@ -178,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_intra_kernel(PrefillParams p)
   const int side = (warp >> 1) & 1;  // 0: key rows (TMEM lanes 0-63), 1: query rows (64-127)
   const int hh = warp >> 2;          // channel half
   const int r = 32 * (warp & 1) + lane;
+  const int lane_base = 64 * side + 32 * (warp & 1);
   const int head = blockIdx.y;
   const int64_t slot = blockIdx.x;
   const int H = p.H;
@@ -192,7 +204,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_intra_kernel(PrefillParams p)
     }
     int seq = -1, kchunk = 0, n = 0;
     if (found >= 0) {
-      // skip over zero-length sequences sharing the same first slot
       const int64_t t0 = p.cu_seqlens[found], t1 = p.cu_seqlens[found + 1];
       const int64_t kk = slot - (t0 / C + found);
       const int64_t len = t1 - t0;
@@ -223,142 +234,139 @@ __global__ void __launch_bounds__(kThreads, 1) kda_intra_kernel(PrefillParams p)
     tc::mbar_init(&bar, 1);
     tc::mbar_fence_init();
   }
-  // zero the lower half of T' (rows 64-127) once
-  for (int i = tid; i < 8192 / 16; i += kThreads)
-    reinterpret_cast<uint4*>(sm + S_TP + 8192)[i] = make_uint4(0, 0, 0, 0);
-
-  // ---- raw loads for this thread's row and 64 channels ----
-  const bf16* gq = reinterpret_cast<const bf16*>(p.q);
-  const bf16* gk = reinterpret_cast<const bf16*>(p.k);
-  const bf16* gg = reinterpret_cast<const bf16*>(p.g);
-  const bf16* gv = reinterpret_cast<const bf16*>(p.v);
   const bool valid = r < n;
   const int64_t rowoff = ((tb + r) * H + head) * (int64_t)D + hh * 64;
-  uint4 xr[8];  // k (side 0) or q (side 1), 8 channels per uint4
-  float G[64];
-  {
-    const bf16* src = side == 0 ? gk : gq;
+  const bf16* gsrc = reinterpret_cast<const bf16*>(side == 0 ? p.k : p.q);
+  uint4 xr[8];  // k (side 0) or q (side 1) for this row's 64 channels
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    xr[i] = valid ? __ldg(reinterpret_cast<const uint4*>(gsrc + rowoff) + i) : make_uint4(0, 0, 0, 0);
+  if (side == 0) {
+    // raw g (floored) -> B operand of the cumulative-sum product
+    const bf16* gg = reinterpret_cast<const bf16*>(p.g);
+    const __nv_bfloat162 floor2 = __float2bfloat162_rn(kLogDecayFloor);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      xr[i] = valid ? __ldg(reinterpret_cast<const uint4*>(src + rowoff) + i) : make_uint4(0, 0, 0, 0);
-      const uint4 gr = valid ? __ldg(reinterpret_cast<const uint4*>(gg + rowoff) + i) : make_uint4(0, 0, 0, 0);
-      unpack_bf8(gr, G + 8 * i);
+      uint4 gr = valid ? __ldg(reinterpret_cast<const uint4*>(gg + rowoff) + i) : make_uint4(0, 0, 0, 0);
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&gr);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) G[8 * i + u] = fmaxf(G[8 * i + u], kLogDecayFloor);
+      for (int u = 0; u < 4; ++u) h[u] = __hmax2(h[u], floor2);
+      *reinterpret_cast<uint4*>(sm + S_GOP + mnmaj(hh * 64 + 8 * i, r, 2048)) = gr;
     }
-    if (side == 1) {  // stage V (bf16, exact) in the MN-major B layout of U0 = T' V
+    if (hh == 0) s_beta[r] = valid ? __bfloat162float(reinterpret_cast<const bf16*>(p.beta)[(tb + r) * H + head]) : 0.f;
+  } else {
+    // L[m][j] = 1 for j <= m % 64 (rows 64-127 repeat rows 0-63), bf16 K-major
+    const int qi = hh * 64 + r;  // 0..127 over the query-side threads
+    for (int u = qi; u < 1024; u += 128) {
+      {
+        const int m = u >> 3, jg = u & 7, mm = m & 63;
+        uint32_t w[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 vr = valid ? __ldg(reinterpret_cast<const uint4*>(gv + rowoff) + i) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sm + S_VB + mnmaj(hh * 64 + 8 * i, r, 2048)) = vr;
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t lo = (8 * jg + 2 * e) <= mm ? 0x3F80u : 0u;
+          const uint32_t hi = (8 * jg + 2 * e + 1) <= mm ? 0x3F80u : 0u;
+          w[e] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(sm + S_LOP + kmaj(m, 8 * jg, 1024)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-    if (side == 0 && hh == 0)
-      s_beta[r] = valid ? __bfloat162float(reinterpret_cast<const bf16*>(p.beta)[(tb + r) * H + head]) : 0.f;
   }
-  // ---- in-chunk cumulative sum over rows (warp scan over 32 rows + carry) ----
+  tc::fence_proxy_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+  // ---- G = L g : inclusive in-chunk cumulative sum, rows duplicated for both sides ----
+  if (tid == 0) {
+    constexpr uint32_t idG = tc::idesc_f16(128, 128, true, false, true);
+    const uint32_t la = tc::smem_u32(sm + S_LOP), gb = tc::smem_u32(sm + S_GOP);
 #pragma unroll
-  for (int c = 0; c < 64; ++c) {
+    for (int kk = 0; kk < C / 16; ++kk)
+      tc::mma_f16(tmem, tc::sdesc(la + kk * 256, 128, 1024), tc::sdesc(gb + kk * 4096, 2048, 128), idG, kk > 0);
+    tc::mma_commit(&bar);
+  }
+  uint32_t phase = 0;
+  bool ok = cta_wait(&bar, phase);
+  phase ^= 1;
+  tc::fence_after_sync();
+  const int m = min(C / 2 - 1, n - 1);
+  if (ok && side == 0 && (r == m || r == n - 1)) {
+    float g32[32];
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, G[c], d);
-      if (lane >= d) G[c] += y;
+    for (int part = 0; part < 2; ++part) {
+      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, hh * 64 + 32 * part), g32);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) {
+        if (r == m) s_gm[hh * 64 + 32 * part + u] = g32[u];
+        if (r == n - 1) s_gl[hh * 64 + 32 * part + u] = g32[u];
+      }
     }
   }
-  const int grp = side * 2 + hh;
-  if ((warp & 1) == 0 && lane == 31) {
-#pragma unroll
-    for (int c = 0; c < 64; ++c) s_carry[grp * 64 + c] = G[c];
-  }
   __syncthreads();
-  if ((warp & 1) == 1) {
-#pragma unroll
-    for (int c = 0; c < 64; ++c) G[c] += s_carry[grp * 64 + c];
+  if (!ok) {
+    if (tid == 0) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+    return;
   }
-  const int m = min(C / 2 - 1, n - 1);
-  if (r == m) {
-#pragma unroll
-    for (int c = 0; c < 64; ++c) s_gm[grp * 64 + c] = G[c];
+  if (tid < D) {
+    s_egm[tid] = __expf(s_gm[tid]);
+    s_eglm[tid] = __expf(s_gl[tid] - s_gm[tid]);
+    reinterpret_cast<float*>(ws + WS_DECAY)[tid] = __expf(s_gl[tid]);
   }
-  if (r == n - 1) {
-#pragma unroll
-    for (int c = 0; c < 64; ++c) s_gl[grp * 64 + c] = G[c];
-  }
-  __syncthreads();
-  // range check for the factorised path
-  {
+  {  // range check for the factorised path
     bool big = false;
+    float g32[32];
 #pragma unroll
-    for (int c = 0; c < 64; ++c) big |= fabsf(G[c] - s_gm[grp * 64 + c]) > 60.f;
+    for (int part = 0; part < 2; ++part) {
+      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, hh * 64 + 32 * part), g32);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) big |= fabsf(g32[u] - s_gm[hh * 64 + 32 * part + u]) > 60.f;
+    }
     if (big) atomicOr(&s_misc[3], 1);
   }
   __syncthreads();
-  tc::fence_after_sync();
   const bool exact = s_misc[3] != 0;
-  const uint32_t tmem = s_tmem;
 
-  // ---- operands ----
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float x[8];
-    unpack_bf8(xr[i], x);
-    const int c0 = hh * 64 + 8 * i;
-    float e_m[8], v1[8], v2[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int c = 8 * i + u;
-      e_m[u] = expf(G[c] - s_gm[grp * 64 + c]);  // e^(G - G_m)
-    }
-    if (side == 0) {
-      // K e^(G-Gm) -> A rows 0-63 ; K e^(Gm-G) -> B rows ; K e^G -> KW ; K e^(Gl-G) -> KLT
-#pragma unroll
-      for (int u = 0; u < 8; ++u) v1[u] = x[u] * e_m[u];
-      uint4 hi, lo;
-      if (!exact) {
-        split_bf8(v1, hi, lo);
-        *reinterpret_cast<uint4*>(sm + S_AROW_HI + kmaj(r, c0, 2048)) = hi;
-        *reinterpret_cast<uint4*>(sm + S_AROW_LO + kmaj(r, c0, 2048)) = lo;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v2[u] = x[u] / e_m[u];
-        split_bf8(v2, hi, lo);
-        *reinterpret_cast<uint4*>(sm + S_BCOL_HI + kmaj(r, c0, 2048)) = hi;
-        *reinterpret_cast<uint4*>(sm + S_BCOL_LO + kmaj(r, c0, 2048)) = lo;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int c = 8 * i + u;
-        v1[u] = x[u] * expf(G[c]);
-        v2[u] = x[u] * expf(s_gl[grp * 64 + c] - G[c]);
-      }
-      *reinterpret_cast<uint4*>(sm + S_KW + mnmaj(c0, r, 2048)) = pack_bf8(v1);
-      *reinterpret_cast<uint4*>(ws + WS_KLT + mnmaj(c0, r, 2048)) = pack_half8(v2);
-    } else {
-      // Q e^(G-Gm) -> A rows 64-127 ; Q e^G -> [W; Q e^G] rows 64-127 (workspace)
-      if (!exact) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v1[u] = x[u] * e_m[u];
-        uint4 hi, lo;
-        split_bf8(v1, hi, lo);
-        *reinterpret_cast<uint4*>(sm + S_AROW_HI + kmaj(64 + r, c0, 2048)) = hi;
-        *reinterpret_cast<uint4*>(sm + S_AROW_LO + kmaj(64 + r, c0, 2048)) = lo;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) v1[u] = x[u] * expf(G[8 * i + u]);
-      *reinterpret_cast<uint4*>(ws + WS_PA + kmaj(64 + r, c0, 2048)) = pack_half8(v1);
-    }
-  }
-  if (side == 0 && r == 0) {
-    float* dec = reinterpret_cast<float*>(ws + WS_DECAY);
-#pragma unroll
-    for (int c = 0; c < 64; ++c) dec[hh * 64 + c] = expf(s_gl[grp * 64 + c]);
-  }
-
-  float* s_akk = reinterpret_cast<float*>(sm + S_AKK);
-  float* s_tf = reinterpret_cast<float*>(sm + S_TF);
-  float a32[32];
-  bool ok = true;
-  uint32_t phase = 0;
+  // ---- operands of the decay-weighted products (and the global-only ones) ----
+  // e_m = e^(G - G_m), e_i = e^(G_m - G): both <= e^60 on this path.
   if (!exact) {
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      float g32[32];
+      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, hh * 64 + 32 * part), g32);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int i = part * 4 + q4;
+        const int c0 = hh * 64 + 8 * i;
+        float x[8], v1[8], v2[8];
+        unpack_bf8(xr[i], x);
+        uint4 hi, lo;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v1[u] = x[u] * __expf(g32[8 * q4 + u] - s_gm[c0 + u]);
+        split_bf8(v1, hi, lo);
+        const int arow = side == 0 ? r : 64 + r;
+        *reinterpret_cast<uint4*>(sm + S_AROW_HI + kmaj(arow, c0, 2048)) = hi;
+        *reinterpret_cast<uint4*>(sm + S_AROW_LO + kmaj(arow, c0, 2048)) = lo;
+        if (side == 0) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v2[u] = x[u] * __expf(s_gm[c0 + u] - g32[8 * q4 + u]);
+          split_bf8(v2, hi, lo);
+          *reinterpret_cast<uint4*>(sm + S_BCOL_HI + kmaj(r, c0, 2048)) = hi;
+          *reinterpret_cast<uint4*>(sm + S_BCOL_LO + kmaj(r, c0, 2048)) = lo;
+          // (K e^(G_last - G))^T, fp16 MN-major, straight to the workspace
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v2[u] *= s_eglm[c0 + u];
+          *reinterpret_cast<uint4*>(ws + WS_KLT + mnmaj(c0, r, 2048)) = pack_half8(v2);
+        } else {
+          // Q e^G -> rows 64-127 of [W; Q e^G] in the workspace
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v1[u] *= s_egm[c0 + u];
+          *reinterpret_cast<uint4*>(ws + WS_PA + kmaj(64 + r, c0, 2048)) = pack_half8(v1);
+        }
+      }
+    }
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -370,59 +378,106 @@ __global__ void __launch_bounds__(kThreads, 1) kda_intra_kernel(PrefillParams p)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t o = kk * 256;
-        tc::mma_f16(tmem, tc::sdesc(ah + o, 128, 2048), tc::sdesc(bh + o, 128, 2048), idA, kk > 0);
-        tc::mma_f16(tmem, tc::sdesc(ah + o, 128, 2048), tc::sdesc(bl + o, 128, 2048), idA, true);
-        tc::mma_f16(tmem, tc::sdesc(al + o, 128, 2048), tc::sdesc(bh + o, 128, 2048), idA, true);
+        tc::mma_f16(tmem + 128, tc::sdesc(ah + o, 128, 2048), tc::sdesc(bh + o, 128, 2048), idA, kk > 0);
+        tc::mma_f16(tmem + 128, tc::sdesc(ah + o, 128, 2048), tc::sdesc(bl + o, 128, 2048), idA, true);
+        tc::mma_f16(tmem + 128, tc::sdesc(al + o, 128, 2048), tc::sdesc(bh + o, 128, 2048), idA, true);
       }
       tc::mma_commit(&bar);
     }
-    ok = cta_wait(&bar, phase);
-    phase ^= 1;
-    tc::fence_after_sync();
-    if (ok) tc::tmem_ld32(tc::tmem_addr(tmem, 64 * side + (warp & 1) * 32, hh * 32), a32);
-    tc::fence_before_sync();
-    __syncthreads();
   } else {
-    // exact element-wise path: stage k, q and G for every row
+    // exact element-wise path: stage k, q, G for every row, write the
+    // global-only operands with direct exponentials
     bf16* fk = reinterpret_cast<bf16*>(sm + S_FK);
     bf16* fq = reinterpret_cast<bf16*>(sm + S_FQ);
     float* fg = reinterpret_cast<float*>(sm + S_FG);
-    float* fakk = reinterpret_cast<float*>(sm + S_FAKK);
-    float* faqk = reinterpret_cast<float*>(sm + S_FAQK);
-    __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int c0 = hh * 64 + 8 * i;
-      *reinterpret_cast<uint4*>((side == 0 ? fk : fq) + r * D + c0) = xr[i];
-      if (side == 0) {
+    for (int part = 0; part < 2; ++part) {
+      float g32[32];
+      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, hh * 64 + 32 * part), g32);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) fg[r * D + c0 + u] = G[8 * i + u];
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int i = part * 4 + q4;
+        const int c0 = hh * 64 + 8 * i;
+        float x[8], v1[8];
+        unpack_bf8(xr[i], x);
+        *reinterpret_cast<uint4*>((side == 0 ? fk : fq) + r * D + c0) = xr[i];
+        if (side == 0) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            fg[r * D + c0 + u] = g32[8 * q4 + u];
+            v1[u] = x[u] * expf(s_gl[c0 + u] - g32[8 * q4 + u]);
+          }
+          *reinterpret_cast<uint4*>(ws + WS_KLT + mnmaj(c0, r, 2048)) = pack_half8(v1);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v1[u] = x[u] * expf(g32[8 * q4 + u]);
+          *reinterpret_cast<uint4*>(ws + WS_PA + kmaj(64 + r, c0, 2048)) = pack_half8(v1);
+        }
       }
     }
     __syncthreads();
-    intra_exact_A(fk, fq, fg, n, fakk, faqk);
+    intra_exact_A(fk, fq, fg, n, reinterpret_cast<float*>(sm + S_FAKK), reinterpret_cast<float*>(sm + S_FAQK));
+  }
+  float a32[32];
+  float kwv[64];  // K e^G for this row's 64 channels (key side)
+  if (!exact) {
+    ok = cta_wait(&bar, phase);
+    phase ^= 1;
+    tc::fence_after_sync();
+    if (ok) {
+      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, 128 + hh * 32), a32);
+      if (side == 0) {
+        // K e^G = (K e^(G-Gm)) e^(G_m), from the hi+lo operand still in place
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c0 = hh * 64 + 8 * i;
+          float h8[8], l8[8];
+          unpack_bf8(*reinterpret_cast<const uint4*>(sm + S_AROW_HI + kmaj(r, c0, 2048)), h8);
+          unpack_bf8(*reinterpret_cast<const uint4*>(sm + S_AROW_LO + kmaj(r, c0, 2048)), l8);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) kwv[8 * i + u] = (h8[u] + l8[u]) * s_egm[c0 + u];
+        }
+      }
+    }
+  } else {
     __syncthreads();
+    const float* fakk = reinterpret_cast<const float*>(sm + S_FAKK);
+    const float* faqk = reinterpret_cast<const float*>(sm + S_FAQK);
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
       const int j = hh * 32 + u;
       a32[u] = side == 0 ? fakk[r * C + j] : faqk[r * C + j];
     }
-    __syncthreads();
+    if (side == 0) {
+      const bf16* fk = reinterpret_cast<const bf16*>(sm + S_FK);
+      const float* fg = reinterpret_cast<const float*>(sm + S_FG);
+#pragma unroll
+      for (int u = 0; u < 64; ++u)
+        kwv[u] = __bfloat162float(fk[r * D + hh * 64 + u]) * expf(fg[r * D + hh * 64 + u]);
+    }
   }
+  tc::fence_before_sync();
+  __syncthreads();  // region reads done; phase-3 buffers may be written
   if (!ok) {
     if (tid == 0) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
     return;
   }
-  // ---- A_kk (beta-scaled, strictly lower) to smem; A_qk (lower) to workspace ----
+  float* s_akk = reinterpret_cast<float*>(sm + S_AKK);
+  float* s_tf = reinterpret_cast<float*>(sm + S_TF);
   if (side == 0) {
+    // A_kk (beta-scaled, strictly lower) to smem; K e^G -> W operand
     const float br = s_beta[r];
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
       const int j = hh * 32 + u;
       s_akk[r * 65 + j] = (j < r) ? br * a32[u] : 0.f;
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      *reinterpret_cast<uint4*>(sm + S_KW + mnmaj(hh * 64 + 8 * i, r, 2048)) = pack_bf8(kwv + 8 * i);
   } else {
+    // A_qk (lower) to the workspace; V -> the B operand of U0 = T' V
 #pragma unroll
     for (int g8 = 0; g8 < 4; ++g8) {
       float x[8];
@@ -433,20 +488,30 @@ __global__ void __launch_bounds__(kThreads, 1) kda_intra_kernel(PrefillParams p)
       }
       *reinterpret_cast<uint4*>(ws + WS_AQK + kmaj(r, hh * 32 + 8 * g8, 1024)) = pack_half8(x);
     }
+    const bf16* gv = reinterpret_cast<const bf16*>(p.v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 vr = valid ? __ldg(reinterpret_cast<const uint4*>(gv + rowoff) + i) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sm + S_VB + mnmaj(hh * 64 + 8 * i, r, 2048)) = vr;
+    }
   }
   for (int i = tid; i < 64 * 65; i += kThreads) s_tf[i] = 0.f;
+  for (int i = tid; i < 8192 / 16; i += kThreads)
+    reinterpret_cast<uint4*>(sm + S_TP + 8192)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   // ---- T = (I + A)^-1 : 16x16 diagonal blocks, then off-diagonal blocks ----
   if (tid < 64) {
+    // column jj of the inverse of the unit lower-triangular 16x16 block b:
+    // x_rr = [rr == jj] - sum_{ii < rr} A[rr][ii] x_ii  (x_ii = 0 for ii < jj)
     const int b = tid >> 4, jj = tid & 15;
+    const float* ab = s_akk + (16 * b) * 65 + 16 * b;
     float x[16];
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) {
-      float s = rr == jj ? 1.f : 0.f;
-      if (rr > jj) {
-        for (int ii = jj; ii < rr; ++ii) s -= s_akk[(16 * b + rr) * 65 + 16 * b + ii] * x[ii];
-      }
-      x[rr] = rr >= jj ? s : 0.f;
+      float sacc = rr == jj ? 1.f : 0.f;
+#pragma unroll
+      for (int ii = 0; ii < rr; ++ii) sacc -= ab[rr * 65 + ii] * x[ii];
+      x[rr] = rr >= jj ? sacc : 0.f;
     }
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) s_tf[(16 * b + rr) * 65 + 16 * b + jj] = x[rr];
@@ -459,19 +524,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_intra_kernel(PrefillParams p)
     for (int e = tid; e < npairs * 256; e += kThreads) {
       const int pi = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
       const int bj = pi, bi = pi + dist;
-      float s = 0.f;
-      for (int kk = 16 * bj; kk < 16 * bi; ++kk) s += s_akk[(16 * bi + rr) * 65 + kk] * s_tf[kk * 65 + 16 * bj + cc];
-      s_mb[pi * 272 + rr * 17 + cc] = s;
+      float sacc = 0.f;
+      for (int kk = 16 * bj; kk < 16 * bi; ++kk) sacc += s_akk[(16 * bi + rr) * 65 + kk] * s_tf[kk * 65 + 16 * bj + cc];
+      s_mb[pi * 272 + rr * 17 + cc] = sacc;
     }
     __syncthreads();
     // T[bi][bj] = -T[bi][bi] M
     for (int e = tid; e < npairs * 256; e += kThreads) {
       const int pi = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
       const int bj = pi, bi = pi + dist;
-      float s = 0.f;
+      float sacc = 0.f;
 #pragma unroll
-      for (int l = 0; l < 16; ++l) s += s_tf[(16 * bi + rr) * 65 + 16 * bi + l] * s_mb[pi * 272 + l * 17 + cc];
-      s_tf[(16 * bi + rr) * 65 + 16 * bj + cc] = -s;
+      for (int l = 0; l < 16; ++l) sacc += s_tf[(16 * bi + rr) * 65 + 16 * bi + l] * s_mb[pi * 272 + l * 17 + cc];
+      s_tf[(16 * bi + rr) * 65 + 16 * bj + cc] = -sacc;
     }
     __syncthreads();
   }
@@ -507,19 +572,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_intra_kernel(PrefillParams p)
   ok = cta_wait(&bar, phase);
   tc::fence_after_sync();
   if (ok && side == 0) {
-    // W rows 0-63 of [W; Q e^G] (fp16 K-major) and U0 (fp16 row-major)
+    // W rows 0-63 of [W; Q e^G] (fp16 K-major) and U0 (fp16, [v/8][row][8])
     float w32[32];
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
       const int cbase = hh * 64 + part * 32;
-      tc::tmem_ld32(tc::tmem_addr(tmem, (warp & 1) * 32, cbase), w32);
+      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, cbase), w32);
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8)
         *reinterpret_cast<uint4*>(ws + WS_PA + kmaj(r, cbase + 8 * g8, 2048)) = pack_half8(w32 + 8 * g8);
-      tc::tmem_ld32(tc::tmem_addr(tmem, (warp & 1) * 32, 128 + cbase), w32);
+      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, 128 + cbase), w32);
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8)
-        *reinterpret_cast<uint4*>(ws + WS_U0 + (r * 128 + cbase + 8 * g8) * 2) = pack_half8(w32 + 8 * g8);
+        *reinterpret_cast<uint4*>(ws + WS_U0 + ((cbase + 8 * g8) >> 3) * 1024 + r * 16) = pack_half8(w32 + 8 * g8);
     }
   }
   if (!ok && tid == 0) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
@@ -561,11 +626,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   using namespace state;
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ __align__(8) uint64_t bar_ld[2];
-  __shared__ __align__(8) uint64_t bar_mma;
+  __shared__ __align__(8) uint64_t bar_p, bar_s, bar_o;
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, hh = warp >> 2;
   const int lrow = 32 * quad + lane;  // TMEM lane == state row c
+  const bool qside = quad >= 2;       // lanes 64-127: output rows
+  const int orow = lrow - 64;
   const int seq = blockIdx.x, head = blockIdx.y;
   const int H = p.H;
 
@@ -581,11 +648,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   const uint8_t* wsb = reinterpret_cast<const uint8_t*>(p.workspace);
   auto ws_block = [&](int k) { return wsb + ((slot0 + k) * H + head) * (int64_t)WS_BYTES; };
 
-  if (warp == 0) tc::tmem_alloc(&s_tmem, 256);
+  if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
   if (tid == 0) {
     tc::mbar_init(&bar_ld[0], 1);
     tc::mbar_init(&bar_ld[1], 1);
-    tc::mbar_init(&bar_mma, 1);
+    tc::mbar_init(&bar_p, 1);
+    tc::mbar_init(&bar_s, 1);
+    tc::mbar_init(&bar_o, 1);
     tc::mbar_fence_init();
   }
   for (int i = tid; i < 8192 / 16; i += kThreads) {
@@ -595,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   float* s_nw = reinterpret_cast<float*>(sm + S_NW);
   float* s_ss = reinterpret_cast<float*>(sm + S_SS);
   if (p.gate && tid < D) s_nw[tid] = __bfloat162float(reinterpret_cast<const bf16*>(p.norm_w)[tid]);
-  // state row lrow, columns [64 hh, 64 hh + 64)
+  // state row lrow, columns [64 hh, 64 hh + 64), fp32 in registers for the whole call
   TS* slot_state = reinterpret_cast<TS*>(p.state_pool) + ((int64_t)si.slot * H + head) * (D * D);
   float S[64];
   load_state_row(slot_state + lrow * D + hh * 64, S);
@@ -604,16 +673,27 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
-  const uint32_t tP = tmem, tS = tmem + 128;
+  const uint32_t tS = tmem + 256;  // tP ping-pong: tmem + 128 * (k & 1)
 
-  auto issue_load = [&](int k) {
+  // A chunk's operands arrive in two bulk copies on one mbarrier: PA|KLT|U0
+  // (read by the P and state products and the residual) and AQK|DECAY (read by
+  // the output product and the state update).  The second part of chunk k+1
+  // is issued only once the output product of chunk k-1, which reads the same
+  // stage, is known to be complete.
+  auto issue_load_main = [&](int k) {
     uint8_t* st = sm + (k & 1) * STAGE;
     uint64_t* b = &bar_ld[k & 1];
     tc::mbar_arrive_expect_tx(b, WS_COPY0 + WS_COPY1);
     tc::bulk_g2s(st, ws_block(k), WS_COPY0, b);
-    tc::bulk_g2s(st + ST_AQK, ws_block(k) + WS_AQK, WS_COPY1, b);
   };
-  if (tid == 0) issue_load(0);
+  auto issue_load_tail = [&](int k) {
+    uint8_t* st = sm + (k & 1) * STAGE;
+    tc::bulk_g2s(st + ST_AQK, ws_block(k) + WS_AQK, WS_COPY1, &bar_ld[k & 1]);
+  };
+  if (tid == 0) {
+    issue_load_main(0);
+    issue_load_tail(0);
+  }
   int last_issued = 0, last_landed = -1;  // bulk copies in flight: (last_landed, last_issued]
 
   auto write_sop = [&]() {
@@ -625,13 +705,63 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
 
   const bf16* ggate = reinterpret_cast<const bf16*>(p.gate);
   bf16* gout = reinterpret_cast<bf16*>(p.out);
-  uint32_t mma_phase = 0;
+  uint4 graw[8];  // gate row of the chunk whose output is pending
+
+  // Output epilogue of chunk kp (query-side warps only; they synchronise among
+  // themselves with named barrier 1): read scale * O from TMEM, RMSNorm-gate,
+  // store bf16 rows.
+  auto epilogue = [&](int kp, bool ok_o) {
+    const int c0 = kp * C;
+    const int n = min(C, len - c0);
+    const uint32_t tP = tmem + 128 * (kp & 1);
+    float o[64];
+    if (ok_o) {
+      float t32[32];
+      tc::tmem_ld32(tc::tmem_addr(tP, 32 * quad, hh * 64), t32);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) o[u] = p.scale * t32[u];
+      tc::tmem_ld32(tc::tmem_addr(tP, 32 * quad, hh * 64 + 32), t32);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) o[32 + u] = p.scale * t32[u];
+    }
+    if (p.gate) {
+      float ss = 0.f;
+#pragma unroll
+      for (int u = 0; u < 64; ++u) ss += o[u] * o[u];
+      s_ss[hh * 64 + orow] = ss;
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+    }
+    if (ok_o && orow < n) {
+      bf16* dst = gout + ((t0 + c0 + orow) * H + head) * D + hh * 64;
+      float inv = 1.f;
+      if (p.gate) inv = rsqrtf((s_ss[orow] + s_ss[64 + orow]) * (1.f / (float)D) + p.eps);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float y[8];
+        if (p.gate) {
+          float gt[8];
+          unpack_bf8(graw[i], gt);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            y[u] = o[8 * i + u] * inv * s_nw[hh * 64 + 8 * i + u] * __fdividef(1.f, 1.f + __expf(-gt[u]));
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) y[u] = o[8 * i + u];
+        }
+        reinterpret_cast<uint4*>(dst)[i] = pack_bf8(y);
+      }
+    }
+    if (p.gate) asm volatile("bar.sync 1, 128;" ::: "memory");  // s_ss reusable
+  };
+
+  uint32_t ph = 0;  // phase parity shared by bar_p, bar_s and bar_o (each completes once per chunk)
   bool ok = true;
   int k = 0;
   for (; k < nchunks; ++k) {
     const int c0 = k * C;
     const int n = min(C, len - c0);
     uint8_t* st = sm + (k & 1) * STAGE;
+    const uint32_t tP = tmem + 128 * (k & 1);
     tc::fence_proxy_async();
     tc::fence_before_sync();
     ok = cta_wait(&bar_ld[k & 1], (k >> 1) & 1);
@@ -640,84 +770,77 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     tc::fence_after_sync();
     if (k + 1 < nchunks) last_issued = k + 1;
     if (tid == 0) {
-      if (k + 1 < nchunks) issue_load(k + 1);
+      if (k + 1 < nchunks) issue_load_main(k + 1);
       // P = [W; Q e^G] S  -> tP (rows 0-63: W S, rows 64-127: Q e^G S)
       constexpr uint32_t idP = tc::idesc_f16(128, 128, false, false, true);
       const uint32_t pa = tc::smem_u32(st + ST_PA), so = tc::smem_u32(sm + S_SOP);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         tc::mma_f16(tP, tc::sdesc(pa + kk * 256, 128, 2048), tc::sdesc(so + kk * 4096, 2048, 128), idP, kk > 0);
-      tc::mma_commit(&bar_mma);
+      tc::mma_commit(&bar_p);
     }
-    // prefetch this chunk's gate row (query-side threads own output rows)
-    uint4 graw[8];
-    const int orow = lrow - 64;
-    const bool qside = quad >= 2;
-    if (p.gate && qside) {
+    bool ok_w = true;
+    if (qside) {
+      // while the P product runs: finish the previous chunk's output rows
+      if (k > 0) {
+        const bool ok_o = tc::mbar_wait(&bar_o, ph ^ 1);
+        tc::fence_after_sync();
+        ok_w = ok_o;
+        epilogue(k - 1, ok_o);
+      }
+      if (p.gate) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        graw[i] = orow < n ? __ldg(reinterpret_cast<const uint4*>(ggate + ((t0 + c0 + orow) * H + head) * D + hh * 64) + i)
-                           : make_uint4(0, 0, 0, 0);
-    }
-    ok = cta_wait(&bar_mma, mma_phase & 1);
-    ++mma_phase;
-    if (!ok) break;
-    tc::fence_after_sync();
-    // U = U0 - W S (key-side rows 0-63) -> fp16 MN-major B operand
-    if (!qside) {
-      float ws32[32], u0[8];
+        for (int i = 0; i < 8; ++i)
+          graw[i] = orow < n ? __ldg(reinterpret_cast<const uint4*>(ggate + ((t0 + c0 + orow) * H + head) * D +
+                                                                    hh * 64) + i)
+                             : make_uint4(0, 0, 0, 0);
+      }
+    } else {
+      // U = U0 - W S (key-side rows 0-63) -> fp16 MN-major B operand
+      ok_w = tc::mbar_wait(&bar_p, ph);
+      tc::fence_after_sync();
+      if (ok_w) {
+        float ws32[32], u0[8];
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const int cb = hh * 64 + part * 32;
-        tc::tmem_ld32(tc::tmem_addr(tP, 32 * quad, cb), ws32);
+        for (int part = 0; part < 2; ++part) {
+          const int cb = hh * 64 + part * 32;
+          tc::tmem_ld32(tc::tmem_addr(tP, 32 * quad, cb), ws32);
 #pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) {
-          unpack_half8(*reinterpret_cast<const uint4*>(st + ST_U0 + (lrow * 128 + cb + 8 * g8) * 2), u0);
+          for (int g8 = 0; g8 < 4; ++g8) {
+            unpack_half8(*reinterpret_cast<const uint4*>(st + ST_U0 + ((cb + 8 * g8) >> 3) * 1024 + lrow * 16), u0);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) u0[u] -= ws32[8 * g8 + u];
-          *reinterpret_cast<uint4*>(sm + S_UOP + mnmaj(cb + 8 * g8, lrow, 2048)) = pack_half8(u0);
+            for (int u = 0; u < 8; ++u) u0[u] -= ws32[8 * g8 + u];
+            *reinterpret_cast<uint4*>(sm + S_UOP + mnmaj(cb + 8 * g8, lrow, 2048)) = pack_half8(u0);
+          }
         }
       }
     }
     tc::fence_proxy_async();
     tc::fence_before_sync();
-    __syncthreads();
+    ok = __syncthreads_and(ok_w) != 0;
+    if (!ok) break;
     tc::fence_after_sync();
     if (tid == 0) {
+      // every thread passed the barrier, so the output product of chunk k-1
+      // (which the query side waited for) no longer reads the other stage
+      if (k + 1 < nchunks) issue_load_tail(k + 1);
       constexpr uint32_t idO = tc::idesc_f16(128, 128, false, false, true);
       constexpr uint32_t idS = tc::idesc_f16(128, 128, false, true, true);
       const uint32_t z = tc::smem_u32(st + ST_ZERO), uo = tc::smem_u32(sm + S_UOP),
                      kl = tc::smem_u32(st + ST_KLT);
 #pragma unroll
-      for (int kk = 0; kk < C / 16; ++kk) {
-        const uint64_t b = tc::sdesc(uo + kk * 4096, 2048, 128);
-        tc::mma_f16(tP, tc::sdesc(z + kk * 256, 128, 1024), b, idO, true);
-        tc::mma_f16(tS, tc::sdesc(kl + kk * 4096, 2048, 128), b, idS, kk > 0);
-      }
-      tc::mma_commit(&bar_mma);
-    }
-    ok = cta_wait(&bar_mma, mma_phase & 1);
-    ++mma_phase;
-    if (!ok) break;
-    tc::fence_after_sync();
-    // ---- output rows (query side): scale, RMSNorm-gate, store ----
-    float o[64];
-    if (qside) {
-      float t32[32];
-      tc::tmem_ld32(tc::tmem_addr(tP, 32 * quad, hh * 64), t32);
+      for (int kk = 0; kk < C / 16; ++kk)
+        tc::mma_f16(tS, tc::sdesc(kl + kk * 4096, 2048, 128), tc::sdesc(uo + kk * 4096, 2048, 128), idS, kk > 0);
+      tc::mma_commit(&bar_s);
 #pragma unroll
-      for (int u = 0; u < 32; ++u) o[u] = p.scale * t32[u];
-      tc::tmem_ld32(tc::tmem_addr(tP, 32 * quad, hh * 64 + 32), t32);
-#pragma unroll
-      for (int u = 0; u < 32; ++u) o[32 + u] = p.scale * t32[u];
-      if (p.gate) {
-        float ss = 0.f;
-#pragma unroll
-        for (int u = 0; u < 64; ++u) ss += o[u] * o[u];
-        s_ss[hh * 64 + orow] = ss;
-      }
+      for (int kk = 0; kk < C / 16; ++kk)
+        tc::mma_f16(tP, tc::sdesc(z + kk * 256, 128, 1024), tc::sdesc(uo + kk * 4096, 2048, 128), idO, true);
+      tc::mma_commit(&bar_o);
     }
     // ---- state carry: S <- Diag(e^G_last) S + (K e^(G_last-G))^T U ----
+    ok = cta_wait(&bar_s, ph);
+    if (!ok) break;
+    tc::fence_after_sync();
     {
       const float d = reinterpret_cast<const float*>(st + ST_DECAY)[lrow];
       float t32[32];
@@ -728,27 +851,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
         for (int u = 0; u < 32; ++u) S[part * 32 + u] = d * S[part * 32 + u] + t32[u];
       }
     }
-    __syncthreads();  // norm partial sums visible
-    if (qside && orow < n) {
-      bf16* dst = gout + ((t0 + c0 + orow) * H + head) * D + hh * 64;
-      float inv = 1.f;
-      if (p.gate) inv = rsqrtf((s_ss[orow] + s_ss[64 + orow]) / (float)D + p.eps);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float y[8];
-        if (p.gate) {
-          float gt[8];
-          unpack_bf8(graw[i], gt);
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            y[u] = o[8 * i + u] * inv * s_nw[hh * 64 + 8 * i + u] * sigmoidf_(gt[u]);
-        } else {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) y[u] = o[8 * i + u];
-        }
-        reinterpret_cast<uint4*>(dst)[i] = pack_bf8(y);
-      }
-    }
     // checkpoint after every checkpoint_every tokens of this segment
     if (si.ckpt_ok && p.checkpoint_every > 0 && (c0 + n) % p.checkpoint_every == 0) {
       const int64_t mck = si.ckpt_off + (c0 + n) / p.checkpoint_every - 1;
@@ -756,6 +858,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
       store_state_row(dst, S);
     }
     write_sop();
+    ph ^= 1;
+  }
+  if (ok && nchunks > 0 && qside) {
+    const bool ok_o = tc::mbar_wait(&bar_o, ph ^ 1);
+    tc::fence_after_sync();
+    epilogue(nchunks - 1, ok_o);
+    if (!ok_o) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
   }
   if (!ok) {
     if (tid == 0) {
@@ -768,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 }  // namespace tcp
