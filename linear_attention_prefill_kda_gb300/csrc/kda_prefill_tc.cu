@@ -290,15 +290,20 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   phase ^= 1;
   tc::fence_after_sync();
   const int m = min(C / 2 - 1, n - 1);
-  if (ok && side == 0 && (r == m || r == n - 1)) {
+  // tcgen05.ld is warp-collective (.sync.aligned): whole key-side warps load,
+  // and only the lanes of rows m and n-1 store.
+  if (ok && side == 0) {
     float g32[32];
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
       tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, hh * 64 + 32 * part), g32);
+      if (r == m) {
 #pragma unroll
-      for (int u = 0; u < 32; ++u) {
-        if (r == m) s_gm[hh * 64 + 32 * part + u] = g32[u];
-        if (r == n - 1) s_gl[hh * 64 + 32 * part + u] = g32[u];
+        for (int u = 0; u < 32; ++u) s_gm[hh * 64 + 32 * part + u] = g32[u];
+      }
+      if (r == n - 1) {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) s_gl[hh * 64 + 32 * part + u] = g32[u];
       }
     }
   }
@@ -633,8 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   const int lrow = 32 * quad + lane;  // TMEM lane == state row c
   const bool qside = quad >= 2;       // lanes 64-127: output rows
   const int orow = lrow - 64;
-  const int seq = blockIdx.x, head = blockIdx.y;
+  // 1D grid, sequence-major: every head of a sequence is launched together
   const int H = p.H;
+  const int seq = (int)(blockIdx.x / (unsigned)H), head = (int)(blockIdx.x % (unsigned)H);
 
   SeqInfo si;
   if (!seq_prologue(p, seq, head, true, si)) {
@@ -783,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     if (qside) {
       // while the P product runs: finish the previous chunk's output rows
       if (k > 0) {
-        const bool ok_o = tc::mbar_wait(&bar_o, ph ^ 1);
+        const bool ok_o = __all_sync(0xffffffffu, tc::mbar_wait(&bar_o, ph ^ 1));
         tc::fence_after_sync();
         ok_w = ok_o;
         epilogue(k - 1, ok_o);
@@ -797,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
       }
     } else {
       // U = U0 - W S (key-side rows 0-63) -> fp16 MN-major B operand
-      ok_w = tc::mbar_wait(&bar_p, ph);
+      ok_w = __all_sync(0xffffffffu, tc::mbar_wait(&bar_p, ph));
       tc::fence_after_sync();
       if (ok_w) {
         float ws32[32], u0[8];
@@ -861,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     ph ^= 1;
   }
   if (ok && nchunks > 0 && qside) {
-    const bool ok_o = tc::mbar_wait(&bar_o, ph ^ 1);
+    const bool ok_o = __all_sync(0xffffffffu, tc::mbar_wait(&bar_o, ph ^ 1));
     tc::fence_after_sync();
     epilogue(nchunks - 1, ok_o);
     if (!ok_o) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
@@ -904,7 +910,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  dim3 g2((unsigned)p.N, (unsigned)p.H);
+  dim3 g2((unsigned)((int64_t)p.N * p.H));
   if (p.state_dtype == KDA_F32)
     tcp::kda_state_kernel<float><<<g2, tcp::kThreads, tcp::state::SMEM_BYTES, stream>>>(p);
   else
