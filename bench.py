@@ -109,6 +109,34 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA sources of the library (identifies the kernels a
+    recorded ncu traffic figure belongs to)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_attention_prefill_kda_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(name: str):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json)
+    for the current kernel sources, else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    if rec.get("csrc_sha256") != kernel_source_hash():
+        return None
+    v = rec.get(name)
+    return None if v is None else int(v)
+
+
 def prefill_algorithmic(w, d):
     """Bytes every prefill call must move, and its FLOPs (triangular-aware)."""
     T, H, dk, dv, C = w.T, w.H, w.dk, w.dv, w.chunk
@@ -318,7 +346,8 @@ def run_gpu(args):
         "prefill_ms": round(pre_ms_mean, 4),
         "roofline": {"bound": "hbm", "achieved": round(pre_gbs, 1), "peak": pk["hbm"],
                      "unit": "GB/s", "frac": round(pre_gbs / pk["hbm"], 4),
-                     "traffic": None, "peak_source": pk["source"],
+                     "traffic": recorded_traffic("prefill_call_dram_bytes"),
+                     "peak_source": pk["source"],
                      "algorithmic_bytes": pre_bytes, "algorithmic_flops": pre_flops,
                      "achieved_tflops": round(pre_tflops, 2),
                      "tensor_frac_of_bf16_peak": round(pre_tflops / pk["bf16"], 4)},
@@ -326,7 +355,8 @@ def run_gpu(args):
                    "ms_per_step": round(dec_ms, 4),
                    "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": pk["hbm"],
                                 "unit": "GB/s", "frac": round(dec_gbs / pk["hbm"], 4),
-                                "traffic": None, "algorithmic_bytes": dec_bytes}},
+                                "traffic": recorded_traffic("decode_step_dram_bytes"),
+                                "algorithmic_bytes": dec_bytes}},
         "e2e": {"value": round(rate(ws * T, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * (prefill_launches(kda, w) * with_prefill + with_decode),

@@ -52,7 +52,7 @@ kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, cons
                                int dv, int chunk, float scale, void* workspace,
                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
   if (N < 0 || T < 0 || T > INT32_MAX || H <= 0 || H > 65535 || num_slots <= 0) return KDA_ERR_INVALID_ARG;
-  if ((int64_t)N * H > INT32_MAX) return KDA_ERR_INVALID_ARG;
+  if ((int64_t)N * H > INT32_MAX || (T / 16 + N) * (int64_t)H > INT32_MAX) return KDA_ERR_INVALID_ARG;
   if (!dtype_ok(in_dtype) || !dtype_ok(state_dtype)) return KDA_ERR_UNSUPPORTED;
   if (!dim_ok(dk) || dv != dk || (chunk != 16 && chunk != 64)) return KDA_ERR_UNSUPPORTED;
   if (checkpoint_every < 0 || (checkpoint_every > 0 && checkpoint_every % chunk != 0))

@@ -190,9 +190,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   const int hh = warp >> 2;          // channel half
   const int r = 32 * (warp & 1) + lane;
   const int lane_base = 64 * side + 32 * (warp & 1);
-  const int head = blockIdx.y;
-  const int64_t slot = blockIdx.x;
+  // 1D grid over (slot, head), head fastest, slots in reverse: the chunks of
+  // the first sequences are produced last, so their workspace blocks are still
+  // in L2 when the state kernel, which starts with those sequences, reads them.
   const int H = p.H;
+  const int head = (int)(blockIdx.x % (unsigned)H);
+  const int64_t slot = num_slots_bound(p.T, p.N) - 1 - (int64_t)(blockIdx.x / (unsigned)H);
 
   // ---- locate (sequence, chunk) of this slot: slot_first(i) = cu[i]/C + i ----
   if (tid == 0) {
@@ -259,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     const int qi = hh * 64 + r;  // 0..127 over the query-side threads
     for (int u = qi; u < 1024; u += 128) {
       {
-        const int m = u >> 3, jg = u & 7, mm = m & 63;
+        const int m = u & 127, jg = u >> 7, mm = m & 63;
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -320,23 +323,13 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     s_eglm[tid] = __expf(s_gl[tid] - s_gm[tid]);
     reinterpret_cast<float*>(ws + WS_DECAY)[tid] = __expf(s_gl[tid]);
   }
-  {  // range check for the factorised path
-    bool big = false;
-    float g32[32];
-#pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, hh * 64 + 32 * part), g32);
-#pragma unroll
-      for (int u = 0; u < 32; ++u) big |= fabsf(g32[u] - s_gm[hh * 64 + 32 * part + u]) > 60.f;
-    }
-    if (big) atomicOr(&s_misc[3], 1);
-  }
   __syncthreads();
-  const bool exact = s_misc[3] != 0;
 
   // ---- operands of the decay-weighted products (and the global-only ones) ----
-  // e_m = e^(G - G_m), e_i = e^(G_m - G): both <= e^60 on this path.
-  if (!exact) {
+  // e_m = e^(G - G_m), e_i = e^(G_m - G).  A chunk where some |G - G_m| > 60
+  // is redone on the exact path below (these values are then discarded).
+  {
+    bool big = false;
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
       float g32[32];
@@ -345,18 +338,23 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
       for (int q4 = 0; q4 < 4; ++q4) {
         const int i = part * 4 + q4;
         const int c0 = hh * 64 + 8 * i;
-        float x[8], v1[8], v2[8];
+        float x[8], v1[8], v2[8], dg[8];
         unpack_bf8(xr[i], x);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          dg[u] = g32[8 * q4 + u] - s_gm[c0 + u];
+          big |= fabsf(dg[u]) > 60.f;
+        }
         uint4 hi, lo;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v1[u] = x[u] * __expf(g32[8 * q4 + u] - s_gm[c0 + u]);
+        for (int u = 0; u < 8; ++u) v1[u] = x[u] * __expf(dg[u]);
         split_bf8(v1, hi, lo);
         const int arow = side == 0 ? r : 64 + r;
         *reinterpret_cast<uint4*>(sm + S_AROW_HI + kmaj(arow, c0, 2048)) = hi;
         *reinterpret_cast<uint4*>(sm + S_AROW_LO + kmaj(arow, c0, 2048)) = lo;
         if (side == 0) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u) v2[u] = x[u] * __expf(s_gm[c0 + u] - g32[8 * q4 + u]);
+          for (int u = 0; u < 8; ++u) v2[u] = x[u] * __expf(-dg[u]);
           split_bf8(v2, hi, lo);
           *reinterpret_cast<uint4*>(sm + S_BCOL_HI + kmaj(r, c0, 2048)) = hi;
           *reinterpret_cast<uint4*>(sm + S_BCOL_LO + kmaj(r, c0, 2048)) = lo;
@@ -372,6 +370,11 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
         }
       }
     }
+    if (big) atomicOr(&s_misc[3], 1);
+  }
+  __syncthreads();
+  const bool exact = s_misc[3] != 0;
+  if (!exact) {
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -431,8 +434,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     tc::fence_after_sync();
     if (ok) {
       tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, 128 + hh * 32), a32);
-      if (side == 0) {
-        // K e^G = (K e^(G-Gm)) e^(G_m), from the hi+lo operand still in place
+      if (side == 1) {
+        // K e^G = (K e^(G-Gm)) e^(G_m) for key row r, from the hi+lo operand
+        // still in place (the query-side threads have the lighter load)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int c0 = hh * 64 + 8 * i;
@@ -453,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
       const int j = hh * 32 + u;
       a32[u] = side == 0 ? fakk[r * C + j] : faqk[r * C + j];
     }
-    if (side == 0) {
+    if (side == 1) {
       const bf16* fk = reinterpret_cast<const bf16*>(sm + S_FK);
       const float* fg = reinterpret_cast<const float*>(sm + S_FG);
 #pragma unroll
@@ -471,17 +475,18 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   float* s_akk = reinterpret_cast<float*>(sm + S_AKK);
   float* s_tf = reinterpret_cast<float*>(sm + S_TF);
   if (side == 0) {
-    // A_kk (beta-scaled, strictly lower) to smem; K e^G -> W operand
+    // A_kk (beta-scaled, strictly lower) to smem
     const float br = s_beta[r];
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
       const int j = hh * 32 + u;
       s_akk[r * 65 + j] = (j < r) ? br * a32[u] : 0.f;
     }
+  } else {
+    // K e^G (key row r) -> W operand
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       *reinterpret_cast<uint4*>(sm + S_KW + mnmaj(hh * 64 + 8 * i, r, 2048)) = pack_bf8(kwv + 8 * i);
-  } else {
     // A_qk (lower) to the workspace; V -> the B operand of U0 = T' V
 #pragma unroll
     for (int g8 = 0; g8 < 4; ++g8) {
@@ -905,7 +910,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int64_t slots = tcp::num_slots_bound(p.T, p.N);
   if (p.T > 0 && slots > 0) {
-    dim3 g1((unsigned)slots, (unsigned)p.H);
+    dim3 g1((unsigned)(slots * p.H));
     tcp::kda_intra_kernel<<<g1, tcp::kThreads, tcp::intra::SMEM_BYTES, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
