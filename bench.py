@@ -45,6 +45,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank values over all ranks (identity without a
+    process group).  The replicas share nothing else: no data-path collective."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replica_rate(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput of `world` independent replicas: all units over the
+    slowest rank's time."""
+    return world * units_per_rank / (ms_max * 1e-3) if ms_max and ms_max > 0 else float("nan")
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -274,11 +291,7 @@ def run_gpu(args):
 
     pre_ms_mean = sum(pre_ms) / len(pre_ms)
     dec_ms = dec_ms_total / args.steps
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([pre_ms_mean, dec_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        pre_ms_mean, dec_ms = tt.tolist()
+    pre_ms_mean, dec_ms = max_over_ranks([pre_ms_mean, dec_ms], dev)
 
     # ---------------- e2e through the public API with host buffers
     names = ["q", "k", "v", "g", "beta", "gate"]
@@ -303,11 +316,7 @@ def run_gpu(args):
     x1.record(stream)
     barrier()
     e2e_ms = x0.elapsed_time(x1) / args.steps
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = tt.item()
+    (e2e_ms,) = max_over_ranks([e2e_ms], dev)
 
     pre_bytes, pre_flops = prefill_algorithmic(w, d)
     dec_bytes, dec_flops = decode_algorithmic(dw)
@@ -321,8 +330,8 @@ def run_gpu(args):
     pre_gbs = rate(pre_bytes, pre_ms_mean) / 1e9
     dec_gbs = rate(dec_bytes, dec_ms) / 1e9
     pre_tflops = rate(pre_flops, pre_ms_mean) / 1e12
-    tokens_s = rate(ws * T, pre_ms_mean)
-    seqsteps_s = rate(ws * dw.N, dec_ms)
+    tokens_s = replica_rate(T, ws, pre_ms_mean)
+    seqsteps_s = replica_rate(dw.N, ws, dec_ms)
     result = {
         "metric": METRIC,
         "value": round(tokens_s, 1),
@@ -357,7 +366,7 @@ def run_gpu(args):
                                 "unit": "GB/s", "frac": round(dec_gbs / pk["hbm"], 4),
                                 "traffic": recorded_traffic("decode_step_dram_bytes"),
                                 "algorithmic_bytes": dec_bytes}},
-        "e2e": {"value": round(rate(ws * T, e2e_ms), 1), "unit": "tokens/s",
+        "e2e": {"value": round(replica_rate(T, ws, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * (prefill_launches(kda, w) * with_prefill + with_decode),
         "clocks": clocks,
