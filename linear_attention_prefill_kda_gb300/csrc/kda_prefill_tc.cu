@@ -49,7 +49,8 @@ constexpr uint32_t WS_KLT = 32768;    // fp16 MN-major [M=c 128 x K=j 64] (K str
 constexpr uint32_t WS_U0 = 49152;     // fp16 [v/8][64 rows][8]: byte (v/8)*1024 + r*16 + (v%8)*2
 constexpr uint32_t WS_AQK = 65536;    // fp16 K-major [64 x 64] (SBO 1024)
 constexpr uint32_t WS_DECAY = 73728;  // fp32 [128]
-constexpr uint32_t WS_BYTES = 74240;
+constexpr uint32_t WS_GW = 74240;     // fp16 [v/8][64 rows][8]: w * sigmoid(gate) (when gated)
+constexpr uint32_t WS_BYTES = 90624;
 constexpr uint32_t WS_COPY0 = 65536;  // PA | KLT | U0
 constexpr uint32_t WS_COPY1 = 8704;   // AQK | DECAY
 
@@ -170,6 +171,28 @@ __device__ void intra_exact_A(const bf16* fk, const bf16* fq, const float* fg, i
     }
     akk[r * C + j] = j < r ? a : 0.f;
     aqk[r * C + j] = aq;
+  }
+}
+
+// w * sigmoid(gate) for row r, channels [c0, c0 + 32) of a chunk -> fp16 in the
+// workspace (the output epilogue of the state kernel then needs two multiplies).
+__device__ __forceinline__ void gated_weight_rows(const PrefillParams& p, uint8_t* ws, int64_t tb, int head,
+                                                  int n, int r, int c0) {
+  const bf16* gg = reinterpret_cast<const bf16*>(p.gate) + ((tb + r) * p.H + head) * D + c0;
+  const bf16* gw = reinterpret_cast<const bf16*>(p.norm_w) + c0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float x[8], w8[8];
+    if (r < n) {
+      unpack_bf8(__ldg(reinterpret_cast<const uint4*>(gg) + i), x);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] = 0.f;
+    }
+    unpack_bf8(__ldg(reinterpret_cast<const uint4*>(gw) + i), w8);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) x[u] = w8[u] / (1.f + __expf(-x[u]));
+    *reinterpret_cast<uint4*>(ws + WS_GW + ((c0 + 8 * i) >> 3) * 1024 + r * 16) = pack_half8(x);
   }
 }
 
@@ -392,7 +415,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
       }
       tc::mma_commit(&bar);
     }
+    if (p.gate) gated_weight_rows(p, ws, tb, head, n, r, 64 * hh + 32 * side);
   } else {
+    if (p.gate) gated_weight_rows(p, ws, tb, head, n, r, 64 * hh + 32 * side);
     // exact element-wise path: stage k, q, G for every row, write the
     // global-only operands with direct exponentials
     bf16* fk = reinterpret_cast<bf16*>(sm + S_FK);
@@ -672,9 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     reinterpret_cast<uint4*>(sm + ST_ZERO)[i] = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4*>(sm + STAGE + ST_ZERO)[i] = make_uint4(0, 0, 0, 0);
   }
-  float* s_nw = reinterpret_cast<float*>(sm + S_NW);
   float* s_ss = reinterpret_cast<float*>(sm + S_SS);
-  if (p.gate && tid < D) s_nw[tid] = __bfloat162float(reinterpret_cast<const bf16*>(p.norm_w)[tid]);
   // state row lrow, columns [64 hh, 64 hh + 64), fp32 in registers for the whole call
   TS* slot_state = reinterpret_cast<TS*>(p.state_pool) + ((int64_t)si.slot * H + head) * (D * D);
   float S[64];
@@ -714,9 +737,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   };
   write_sop();
 
-  const bf16* ggate = reinterpret_cast<const bf16*>(p.gate);
   bf16* gout = reinterpret_cast<bf16*>(p.out);
-  uint4 graw[8];  // gate row of the chunk whose output is pending
+  uint4 graw[8];  // w * sigmoid(gate) (fp16) of the output row whose epilogue is pending
 
   // Output epilogue of chunk kp (query-side warps only; they synchronise among
   // themselves with named barrier 1): read scale * O from TMEM, RMSNorm-gate,
@@ -751,10 +773,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
         float y[8];
         if (p.gate) {
           float gt[8];
-          unpack_bf8(graw[i], gt);
+          unpack_half8(graw[i], gt);
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            y[u] = o[8 * i + u] * inv * s_nw[hh * 64 + 8 * i + u] * __fdividef(1.f, 1.f + __expf(-gt[u]));
+          for (int u = 0; u < 8; ++u) y[u] = o[8 * i + u] * inv * gt[u];
         } else {
 #pragma unroll
           for (int u = 0; u < 8; ++u) y[u] = o[8 * i + u];
@@ -765,6 +786,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     if (p.gate) asm volatile("bar.sync 1, 128;" ::: "memory");  // s_ss reusable
   };
 
+  int64_t pending_ck = -1;  // checkpoint entry whose store is still to be issued
+  auto store_pending_ck = [&]() {
+    if (pending_ck >= 0) {
+      TS* dst = reinterpret_cast<TS*>(p.checkpoints) + (pending_ck * H + head) * (int64_t)(D * D) + lrow * D + hh * 64;
+      store_state_row(dst, S);
+      pending_ck = -1;
+    }
+  };
   uint32_t ph = 0;  // phase parity shared by bar_p, bar_s and bar_o (each completes once per chunk)
   bool ok = true;
   int k = 0;
@@ -790,6 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
         tc::mma_f16(tP, tc::sdesc(pa + kk * 256, 128, 2048), tc::sdesc(so + kk * 4096, 2048, 128), idP, kk > 0);
       tc::mma_commit(&bar_p);
     }
+    store_pending_ck();
     bool ok_w = true;
     if (qside) {
       // while the P product runs: finish the previous chunk's output rows
@@ -802,8 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
       if (p.gate) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          graw[i] = orow < n ? __ldg(reinterpret_cast<const uint4*>(ggate + ((t0 + c0 + orow) * H + head) * D +
-                                                                    hh * 64) + i)
+          graw[i] = orow < n ? __ldg(reinterpret_cast<const uint4*>(ws_block(k) + WS_GW + (hh * 8 + i) * 1024 +
+                                                                    orow * 16))
                              : make_uint4(0, 0, 0, 0);
       }
     } else {
@@ -862,12 +892,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
         for (int u = 0; u < 32; ++u) S[part * 32 + u] = d * S[part * 32 + u] + t32[u];
       }
     }
-    // checkpoint after every checkpoint_every tokens of this segment
-    if (si.ckpt_ok && p.checkpoint_every > 0 && (c0 + n) % p.checkpoint_every == 0) {
-      const int64_t mck = si.ckpt_off + (c0 + n) / p.checkpoint_every - 1;
-      TS* dst = reinterpret_cast<TS*>(p.checkpoints) + (mck * H + head) * (int64_t)(D * D) + lrow * D + hh * 64;
-      store_state_row(dst, S);
-    }
+    // checkpoint after every checkpoint_every tokens of this segment; the
+    // registers keep this state until the next chunk's update, so the store is
+    // issued there, overlapping that chunk's first product
+    if (si.ckpt_ok && p.checkpoint_every > 0 && (c0 + n) % p.checkpoint_every == 0)
+      pending_ck = si.ckpt_off + (c0 + n) / p.checkpoint_every - 1;
     write_sop();
     ph ^= 1;
   }
@@ -884,6 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
       for (int j = last_landed + 1; j <= last_issued; ++j) tc::mbar_wait(&bar_ld[j & 1], (j >> 1) & 1);
     }
   } else {
+    store_pending_ck();
     store_state_row(slot_state + lrow * D + hh * 64, S);
   }
   tc::fence_before_sync();
