@@ -191,7 +191,7 @@ __device__ __forceinline__ void gated_weight_rows(const PrefillParams& p, uint8_
     }
     unpack_bf8(__ldg(reinterpret_cast<const uint4*>(gw) + i), w8);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) x[u] = w8[u] / (1.f + __expf(-x[u]));
+    for (int u = 0; u < 8; ++u) x[u] = __fdividef(w8[u], 1.f + __expf(-x[u]));
     *reinterpret_cast<uint4*>(ws + WS_GW + ((c0 + 8 * i) >> 3) * 1024 + r * 16) = pack_half8(x);
   }
 }
@@ -500,19 +500,73 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   float* s_akk = reinterpret_cast<float*>(sm + S_AKK);
   float* s_tf = reinterpret_cast<float*>(sm + S_TF);
   if (side == 0) {
-    // A_kk (beta-scaled, strictly lower) to smem
+    // ---- key-side warps (0, 1, 4, 5; named barrier 2): T = (I + A)^-1 ----
+    const int kt = (warp >> 2) * 64 + (warp & 1) * 32 + lane;  // 0..127
     const float br = s_beta[r];
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
       const int j = hh * 32 + u;
       s_akk[r * 65 + j] = (j < r) ? br * a32[u] : 0.f;
     }
+    for (int i = kt; i < 64 * 65; i += 128) s_tf[i] = 0.f;
+    asm volatile("bar.sync 2, 128;" ::: "memory");
+    if (kt < 64) {
+      // column jj of the inverse of the unit lower-triangular 16x16 block b:
+      // x_rr = [rr == jj] - sum_{ii < rr} A[rr][ii] x_ii  (x_ii = 0 for ii < jj)
+      const int b = kt >> 4, jj = kt & 15;
+      const float* ab = s_akk + (16 * b) * 65 + 16 * b;
+      float x[16];
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) {
+        float sacc = rr == jj ? 1.f : 0.f;
+#pragma unroll
+        for (int ii = 0; ii < rr; ++ii) sacc -= ab[rr * 65 + ii] * x[ii];
+        x[rr] = rr >= jj ? sacc : 0.f;
+      }
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) s_tf[(16 * b + rr) * 65 + 16 * b + jj] = x[rr];
+    }
+    asm volatile("bar.sync 2, 128;" ::: "memory");
+    float* s_mb = reinterpret_cast<float*>(sm + S_MB);
+    for (int dist = 1; dist < 4; ++dist) {
+      const int npairs = 4 - dist;
+      // M = sum_{bk=bj}^{bi-1} A[bi][bk] T[bk][bj]
+      for (int e = kt; e < npairs * 256; e += 128) {
+        const int pi = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+        const int bj = pi, bi = pi + dist;
+        float sacc = 0.f;
+        for (int kk = 16 * bj; kk < 16 * bi; ++kk)
+          sacc += s_akk[(16 * bi + rr) * 65 + kk] * s_tf[kk * 65 + 16 * bj + cc];
+        s_mb[pi * 272 + rr * 17 + cc] = sacc;
+      }
+      asm volatile("bar.sync 2, 128;" ::: "memory");
+      // T[bi][bj] = -T[bi][bi] M
+      for (int e = kt; e < npairs * 256; e += 128) {
+        const int pi = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+        const int bj = pi, bi = pi + dist;
+        float sacc = 0.f;
+#pragma unroll
+        for (int l = 0; l < 16; ++l) sacc += s_tf[(16 * bi + rr) * 65 + 16 * bi + l] * s_mb[pi * 272 + l * 17 + cc];
+        s_tf[(16 * bi + rr) * 65 + 16 * bj + cc] = -sacc;
+      }
+      asm volatile("bar.sync 2, 128;" ::: "memory");
+    }
+    // T' = T Diag(beta) -> bf16 K-major [128 x 64] rows 0-63
+#pragma unroll
+    for (int g8 = 0; g8 < 4; ++g8) {
+      float x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = hh * 32 + 8 * g8 + u;
+        x[u] = s_tf[r * 65 + j] * s_beta[j];
+      }
+      *reinterpret_cast<uint4*>(sm + S_TP + kmaj(r, hh * 32 + 8 * g8, 1024)) = pack_bf8(x);
+    }
   } else {
-    // K e^G (key row r) -> W operand
+    // ---- query-side warps, concurrently: K e^G -> W operand, A_qk -> workspace, V -> U0 operand
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       *reinterpret_cast<uint4*>(sm + S_KW + mnmaj(hh * 64 + 8 * i, r, 2048)) = pack_bf8(kwv + 8 * i);
-    // A_qk (lower) to the workspace; V -> the B operand of U0 = T' V
 #pragma unroll
     for (int g8 = 0; g8 < 4; ++g8) {
       float x[8];
@@ -529,64 +583,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
       const uint4 vr = valid ? __ldg(reinterpret_cast<const uint4*>(gv + rowoff) + i) : make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(sm + S_VB + mnmaj(hh * 64 + 8 * i, r, 2048)) = vr;
     }
-  }
-  for (int i = tid; i < 64 * 65; i += kThreads) s_tf[i] = 0.f;
-  for (int i = tid; i < 8192 / 16; i += kThreads)
-    reinterpret_cast<uint4*>(sm + S_TP + 8192)[i] = make_uint4(0, 0, 0, 0);
-  __syncthreads();
-  // ---- T = (I + A)^-1 : 16x16 diagonal blocks, then off-diagonal blocks ----
-  if (tid < 64) {
-    // column jj of the inverse of the unit lower-triangular 16x16 block b:
-    // x_rr = [rr == jj] - sum_{ii < rr} A[rr][ii] x_ii  (x_ii = 0 for ii < jj)
-    const int b = tid >> 4, jj = tid & 15;
-    const float* ab = s_akk + (16 * b) * 65 + 16 * b;
-    float x[16];
-#pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-      float sacc = rr == jj ? 1.f : 0.f;
-#pragma unroll
-      for (int ii = 0; ii < rr; ++ii) sacc -= ab[rr * 65 + ii] * x[ii];
-      x[rr] = rr >= jj ? sacc : 0.f;
-    }
-#pragma unroll
-    for (int rr = 0; rr < 16; ++rr) s_tf[(16 * b + rr) * 65 + 16 * b + jj] = x[rr];
-  }
-  __syncthreads();
-  float* s_mb = reinterpret_cast<float*>(sm + S_MB);
-  for (int dist = 1; dist < 4; ++dist) {
-    const int npairs = 4 - dist;
-    // M = sum_{bk=bj}^{bi-1} A[bi][bk] T[bk][bj]
-    for (int e = tid; e < npairs * 256; e += kThreads) {
-      const int pi = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-      const int bj = pi, bi = pi + dist;
-      float sacc = 0.f;
-      for (int kk = 16 * bj; kk < 16 * bi; ++kk) sacc += s_akk[(16 * bi + rr) * 65 + kk] * s_tf[kk * 65 + 16 * bj + cc];
-      s_mb[pi * 272 + rr * 17 + cc] = sacc;
-    }
-    __syncthreads();
-    // T[bi][bj] = -T[bi][bi] M
-    for (int e = tid; e < npairs * 256; e += kThreads) {
-      const int pi = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-      const int bj = pi, bi = pi + dist;
-      float sacc = 0.f;
-#pragma unroll
-      for (int l = 0; l < 16; ++l) sacc += s_tf[(16 * bi + rr) * 65 + 16 * bi + l] * s_mb[pi * 272 + l * 17 + cc];
-      s_tf[(16 * bi + rr) * 65 + 16 * bj + cc] = -sacc;
-    }
-    __syncthreads();
-  }
-  // ---- T' = T Diag(beta) -> bf16 K-major [128 x 64] rows 0-63 ----
-  if (side == 0) {
-#pragma unroll
-    for (int g8 = 0; g8 < 4; ++g8) {
-      float x[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = hh * 32 + 8 * g8 + u;
-        x[u] = s_tf[r * 65 + j] * s_beta[j];
-      }
-      *reinterpret_cast<uint4*>(sm + S_TP + kmaj(r, hh * 32 + 8 * g8, 1024)) = pack_bf8(x);
-    }
+    const int qt = hh * 64 + r;  // 0..127
+    for (int i = qt; i < 8192 / 16; i += 128)
+      reinterpret_cast<uint4*>(sm + S_TP + 8192)[i] = make_uint4(0, 0, 0, 0);
   }
   tc::fence_proxy_async();
   tc::fence_before_sync();
