@@ -196,6 +196,25 @@ __device__ __forceinline__ void gated_weight_rows(const PrefillParams& p, uint8_
   }
 }
 
+// The constant lower-triangular ones operand L[m][j] = (j <= m % 64) of the
+// cumulative-sum product, as the byte image of its bf16 K-major [128 x 64]
+// shared-memory layout (SBO 1024), built at compile time and fetched by each
+// CTA with one bulk copy.
+struct LTable {
+  uint32_t w[4096];
+};
+constexpr LTable make_ltable() {
+  LTable t{};
+  for (int m = 0; m < 128; ++m)
+    for (int k = 0; k < 64; k += 2) {
+      const uint32_t lo = k <= (m & 63) ? 0x3F80u : 0u, hi = k + 1 <= (m & 63) ? 0x3F80u : 0u;
+      const int byte = (m >> 3) * 1024 + (k >> 3) * 128 + (m & 7) * 16 + (k & 7) * 2;
+      t.w[byte / 4] = lo | (hi << 16);
+    }
+  return t;
+}
+__device__ __align__(16) const LTable g_ltable = make_ltable();
+
 __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p) {
   using namespace intra;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -205,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   float* s_egm = reinterpret_cast<float*>(sm + S_EGM);
   float* s_eglm = reinterpret_cast<float*>(sm + S_EGLM);
   int* s_misc = reinterpret_cast<int*>(sm + S_MISC);
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t bar, bar_l;
   __shared__ uint32_t s_tmem;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -220,30 +239,35 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   const int head = (int)(blockIdx.x % (unsigned)H);
   const int64_t slot = num_slots_bound(p.T, p.N) - 1 - (int64_t)(blockIdx.x / (unsigned)H);
 
-  // ---- locate (sequence, chunk) of this slot: slot_first(i) = cu[i]/C + i ----
-  if (tid == 0) {
-    int lo = 0, hi = p.N - 1, found = -1;
-    while (lo <= hi) {
-      const int mid = (lo + hi) >> 1;
-      const int64_t first = (int64_t)p.cu_seqlens[mid] / C + mid;
-      if (first <= slot) { found = mid; lo = mid + 1; } else { hi = mid - 1; }
-    }
-    int seq = -1, kchunk = 0, n = 0;
-    if (found >= 0) {
-      const int64_t t0 = p.cu_seqlens[found], t1 = p.cu_seqlens[found + 1];
-      const int64_t kk = slot - (t0 / C + found);
-      const int64_t len = t1 - t0;
-      if (t0 >= 0 && len > 0 && t1 <= p.T && kk >= 0 && kk * C < len && p.state_indices[found] >= 0 &&
-          p.state_indices[found] < p.num_slots) {
-        seq = found;
-        kchunk = (int)kk;
-        n = (int)(len - kk * C < C ? len - kk * C : C);
+  // ---- locate (sequence, chunk) of this slot: sequence i owns the slots
+  //      [first(i), first(i+1)) with first(i) = cu[i]/C + i (strictly
+  //      increasing in i); warp 0 scans 32 sequences per step ----
+  if (warp == 0) {
+    if (lane == 0) s_misc[0] = -1;
+    __syncwarp();
+    for (int base = 0; base < p.N; base += 32) {
+      const int i = base + lane;
+      bool mine = false;
+      if (i < p.N) {
+        const int64_t t0 = p.cu_seqlens[i];
+        const int64_t nx = i + 1 < p.N ? (int64_t)p.cu_seqlens[i + 1] / C + i + 1 : INT64_MAX;
+        mine = t0 / C + i <= slot && slot < nx;
       }
+      const unsigned who = __ballot_sync(0xffffffffu, mine);
+      if (mine) {
+        const int64_t t0 = p.cu_seqlens[i], t1 = p.cu_seqlens[i + 1];
+        const int64_t kk = slot - (t0 / C + i);
+        const int64_t len = t1 - t0;
+        if (t0 >= 0 && len > 0 && t1 <= p.T && kk * C < len && p.state_indices[i] >= 0 &&
+            p.state_indices[i] < p.num_slots) {
+          s_misc[0] = i;
+          s_misc[1] = (int)kk;
+          s_misc[2] = (int)(len - kk * C < C ? len - kk * C : C);
+        }
+      }
+      if (who) break;
     }
-    s_misc[0] = seq;
-    s_misc[1] = kchunk;
-    s_misc[2] = n;
-    s_misc[3] = 0;  // range flag
+    if (lane == 0) s_misc[3] = 0;  // range flag
   }
   __syncthreads();
   const int seq = s_misc[0];
@@ -258,7 +282,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   }
   if (tid == 0) {
     tc::mbar_init(&bar, 1);
+    tc::mbar_init(&bar_l, 1);
     tc::mbar_fence_init();
+    tc::mbar_arrive_expect_tx(&bar_l, sizeof(LTable));
+    tc::bulk_g2s(sm + S_LOP, &g_ltable, sizeof(LTable), &bar_l);
   }
   const bool valid = r < n;
   const int64_t rowoff = ((tb + r) * H + head) * (int64_t)D + hh * 64;
@@ -267,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
 #pragma unroll
   for (int i = 0; i < 8; ++i)
     xr[i] = valid ? __ldg(reinterpret_cast<const uint4*>(gsrc + rowoff) + i) : make_uint4(0, 0, 0, 0);
+
   if (side == 0) {
     // raw g (floored) -> B operand of the cumulative-sum product
     const bf16* gg = reinterpret_cast<const bf16*>(p.g);
@@ -280,22 +308,6 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
       *reinterpret_cast<uint4*>(sm + S_GOP + mnmaj(hh * 64 + 8 * i, r, 2048)) = gr;
     }
     if (hh == 0) s_beta[r] = valid ? __bfloat162float(reinterpret_cast<const bf16*>(p.beta)[(tb + r) * H + head]) : 0.f;
-  } else {
-    // L[m][j] = 1 for j <= m % 64 (rows 64-127 repeat rows 0-63), bf16 K-major
-    const int qi = hh * 64 + r;  // 0..127 over the query-side threads
-    for (int u = qi; u < 1024; u += 128) {
-      {
-        const int m = u & 127, jg = u >> 7, mm = m & 63;
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t lo = (8 * jg + 2 * e) <= mm ? 0x3F80u : 0u;
-          const uint32_t hi = (8 * jg + 2 * e + 1) <= mm ? 0x3F80u : 0u;
-          w[e] = lo | (hi << 16);
-        }
-        *reinterpret_cast<uint4*>(sm + S_LOP + kmaj(m, 8 * jg, 1024)) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
   }
   tc::fence_proxy_async();
   tc::fence_before_sync();
@@ -303,7 +315,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
   // ---- G = L g : inclusive in-chunk cumulative sum, rows duplicated for both sides ----
-  if (tid == 0) {
+  bool ok_l = true;
+  if (tid == 0) ok_l = tc::mbar_wait(&bar_l, 0);  // the L operand has landed
+  if (tid == 0 && ok_l) {
     constexpr uint32_t idG = tc::idesc_f16(128, 128, true, false, true);
     const uint32_t la = tc::smem_u32(sm + S_LOP), gb = tc::smem_u32(sm + S_GOP);
 #pragma unroll
@@ -312,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     tc::mma_commit(&bar);
   }
   uint32_t phase = 0;
-  bool ok = cta_wait(&bar, phase);
+  bool ok = cta_wait(&bar, phase) && __syncthreads_and(ok_l);
   phase ^= 1;
   tc::fence_after_sync();
   const int m = min(C / 2 - 1, n - 1);
@@ -508,7 +522,6 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
       const int j = hh * 32 + u;
       s_akk[r * 65 + j] = (j < r) ? br * a32[u] : 0.f;
     }
-    for (int i = kt; i < 64 * 65; i += 128) s_tf[i] = 0.f;
     asm volatile("bar.sync 2, 128;" ::: "memory");
     if (kt < 64) {
       // column jj of the inverse of the unit lower-triangular 16x16 block b:
@@ -527,27 +540,45 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
       for (int rr = 0; rr < 16; ++rr) s_tf[(16 * b + rr) * 65 + 16 * b + jj] = x[rr];
     }
     asm volatile("bar.sync 2, 128;" ::: "memory");
+    // off-diagonal 16x16 blocks, nearest the diagonal first:
+    //   M = sum_{bk=bj}^{bi-1} A[bi][bk] T[bk][bj],  T[bi][bj] = -T[bi][bi] M
+    // each thread owns 2x2 output tiles (rows rr, rr+8; columns cc, cc+8)
     float* s_mb = reinterpret_cast<float*>(sm + S_MB);
     for (int dist = 1; dist < 4; ++dist) {
-      const int npairs = 4 - dist;
-      // M = sum_{bk=bj}^{bi-1} A[bi][bk] T[bk][bj]
-      for (int e = kt; e < npairs * 256; e += 128) {
-        const int pi = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+      const int ntiles = (4 - dist) * 64;
+      for (int t = kt; t < ntiles; t += 128) {
+        const int pi = t >> 6, rr = (t >> 3) & 7, cc = t & 7;
         const int bj = pi, bi = pi + dist;
-        float sacc = 0.f;
-        for (int kk = 16 * bj; kk < 16 * bi; ++kk)
-          sacc += s_akk[(16 * bi + rr) * 65 + kk] * s_tf[kk * 65 + 16 * bj + cc];
-        s_mb[pi * 272 + rr * 17 + cc] = sacc;
+        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+        for (int bk = bj; bk < bi; ++bk) {
+          const float* ar0 = s_akk + (16 * bi + rr) * 65 + 16 * bk;
+          const float* ar1 = ar0 + 8 * 65;
+          const float* tcol = s_tf + (16 * bk) * 65 + 16 * bj + cc;
+#pragma unroll
+          for (int l = 0; l < 16; ++l) {
+            const float x0 = ar0[l], x1 = ar1[l], y0 = tcol[l * 65], y1 = tcol[l * 65 + 8];
+            a00 += x0 * y0; a01 += x0 * y1; a10 += x1 * y0; a11 += x1 * y1;
+          }
+        }
+        float* mb = s_mb + pi * 272;
+        mb[rr * 17 + cc] = a00; mb[rr * 17 + cc + 8] = a01;
+        mb[(rr + 8) * 17 + cc] = a10; mb[(rr + 8) * 17 + cc + 8] = a11;
       }
       asm volatile("bar.sync 2, 128;" ::: "memory");
-      // T[bi][bj] = -T[bi][bi] M
-      for (int e = kt; e < npairs * 256; e += 128) {
-        const int pi = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+      for (int t = kt; t < ntiles; t += 128) {
+        const int pi = t >> 6, rr = (t >> 3) & 7, cc = t & 7;
         const int bj = pi, bi = pi + dist;
-        float sacc = 0.f;
+        const float* tr0 = s_tf + (16 * bi + rr) * 65 + 16 * bi;
+        const float* tr1 = tr0 + 8 * 65;
+        const float* mb = s_mb + pi * 272 + cc;
+        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
 #pragma unroll
-        for (int l = 0; l < 16; ++l) sacc += s_tf[(16 * bi + rr) * 65 + 16 * bi + l] * s_mb[pi * 272 + l * 17 + cc];
-        s_tf[(16 * bi + rr) * 65 + 16 * bj + cc] = -sacc;
+        for (int l = 0; l < 16; ++l) {
+          const float x0 = tr0[l], x1 = tr1[l], y0 = mb[l * 17], y1 = mb[l * 17 + 8];
+          a00 += x0 * y0; a01 += x0 * y1; a10 += x1 * y0; a11 += x1 * y1;
+        }
+        float* dst = s_tf + (16 * bi + rr) * 65 + 16 * bj + cc;
+        dst[0] = -a00; dst[8] = -a01; dst[8 * 65] = -a10; dst[8 * 65 + 8] = -a11;
       }
       asm volatile("bar.sync 2, 128;" ::: "memory");
     }
@@ -558,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int j = hh * 32 + 8 * g8 + u;
-        x[u] = s_tf[r * 65 + j] * s_beta[j];
+        x[u] = j <= r ? s_tf[r * 65 + j] * s_beta[j] : 0.f;  // blocks above the diagonal are never written
       }
       *reinterpret_cast<uint4*>(sm + S_TP + kmaj(r, hh * 32 + 8 * g8, 1024)) = pack_bf8(x);
     }
