@@ -62,6 +62,10 @@ typedef enum {
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
+/* Activation of the output gate in the RMSNorm-gate: sigmoid(x) or SiLU,
+ * x * sigmoid(x) (the two activations the pages' norm-gate coverage names). */
+typedef enum { KDA_GATE_SIGMOID = 0, KDA_GATE_SILU = 1 } kda_gate_act;
+
 /* Codes latched into *dev_status by the kernels (first error wins). */
 #define KDA_DEV_OK 0
 #define KDA_DEV_BAD_INDEX 1       /* state_indices[i] outside [-1, num_slots) */
@@ -96,6 +100,12 @@ KDA_API size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int 
  *               back to that slot in place.  -1 marks a padding sequence: its
  *               output rows are zeroed and the pool is untouched.  Indices
  *               must be distinct within a call.
+ *  has_initial_state int32 [N], device, or NULL (every sequence has state).
+ *               0 marks a sequence without initial state -- a new prompt
+ *               ("[Feature][KDA] ...", section "Metadata construction": a
+ *               one-token prompt without state is still prefill): it starts
+ *               from S = 0 whatever its slot holds, and its final state is
+ *               written to the slot as usual.
  *  state_pool   [num_slots, H, dk, dv] state_dtype, read and written.
  *  out          [T, H, dv] in_dtype.  o_t, or the norm-gated y_t when gate
  *               is non-NULL.
@@ -110,7 +120,7 @@ KDA_API size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int 
  *               prefix sum of floor(len_i / checkpoint_every).
  *  gate, norm_w gate [T, H, dv] in_dtype and norm_w [dv] in_dtype, or both
  *               NULL.  When given, out = o / sqrt(mean(o^2) + eps) * norm_w *
- *               sigmoid(gate) per (token, head) row.
+ *               act(gate) per (token, head) row, act chosen by gate_act.
  *  scale        read-out scale; <= 0 selects 1/sqrt(dk).
  *  workspace    caller scratch of at least kda_prefill_workspace_bytes().
  *  dev_status   see the conventions above (may be NULL).
@@ -120,13 +130,15 @@ KDA_API size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int 
  */
 KDA_API kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, const void* g,
                                const void* beta, kda_dtype in_dtype, const int32_t* cu_seqlens,
-                               int N, int64_t T, const int32_t* state_indices, void* state_pool,
+                               int N, int64_t T, const int32_t* state_indices,
+                               const int32_t* has_initial_state, void* state_pool,
                                int64_t num_slots, kda_dtype state_dtype, void* out,
                                void* checkpoints, int32_t checkpoint_every,
                                int64_t checkpoint_capacity, int32_t* ckpt_offsets,
-                               const void* gate, const void* norm_w, float eps, int H, int dk,
-                               int dv, int chunk, float scale, void* workspace,
-                               size_t workspace_bytes, int32_t* dev_status, void* stream);
+                               const void* gate, const void* norm_w, float eps,
+                               kda_gate_act gate_act, int H, int dk, int dv, int chunk,
+                               float scale, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream);
 
 /*
  * One recurrent decode step for N sequences of one token each ("[Feature][KDA]
@@ -139,18 +151,20 @@ KDA_API kda_status kda_prefill_chunked(const void* q, const void* k, const void*
 KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, const void* g,
                            const void* beta, kda_dtype in_dtype, const int32_t* state_indices,
                            int N, void* state_pool, int64_t num_slots, kda_dtype state_dtype,
-                           void* out, const void* gate, const void* norm_w, float eps, int H,
-                           int dk, int dv, float scale, int32_t* dev_status, void* stream);
+                           void* out, const void* gate, const void* norm_w, float eps,
+                           kda_gate_act gate_act, int H, int dk, int dv, float scale,
+                           int32_t* dev_status, void* stream);
 
 /*
  * Standalone output RMSNorm-gate ("[Feature][KDA] ...", first section:
  * FusedRMSNormGated output normalisation and gating):
- *     y = o / sqrt(mean_dv(o^2) + eps) * w * sigmoid(gate)
+ *     y = o / sqrt(mean_dv(o^2) + eps) * w * act(gate),  act = sigmoid or SiLU
  * o, gate, y are [rows, H, dv] in `dtype`; w is [dv] in `dtype`.  y may alias o
  * (in place); otherwise o is preserved.
  */
-KDA_API kda_status kda_norm_gate(const void* o, const void* gate, const void* w, float eps, void* y,
-                         int64_t rows, int H, int dv, kda_dtype dtype, void* stream);
+KDA_API kda_status kda_norm_gate(const void* o, const void* gate, const void* w, float eps,
+                         kda_gate_act gate_act, void* y, int64_t rows, int H, int dv,
+                         kda_dtype dtype, void* stream);
 
 /*
  * Chunked prefill without caller scratch.  The pages have no counterpart of
@@ -171,9 +185,10 @@ KDA_API kda_status kda_norm_gate(const void* o, const void* gate, const void* w,
 #define KDA_STATIC_SCRATCH_BYTES ((size_t)128 << 20)
 KDA_API kda_status kda_prefill_chunked_static_scratch(
     const void* q, const void* k, const void* v, const void* g, const void* beta, kda_dtype in_dtype,
-    const int32_t* cu_seqlens, int N, int64_t T, const int32_t* state_indices, void* state_pool,
-    int64_t num_slots, kda_dtype state_dtype, void* out, void* checkpoints, int32_t checkpoint_every,
-    int64_t checkpoint_capacity, int32_t* ckpt_offsets, const void* gate, const void* norm_w, float eps,
+    const int32_t* cu_seqlens, int N, int64_t T, const int32_t* state_indices,
+    const int32_t* has_initial_state, void* state_pool, int64_t num_slots, kda_dtype state_dtype,
+    void* out, void* checkpoints, int32_t checkpoint_every, int64_t checkpoint_capacity,
+    int32_t* ckpt_offsets, const void* gate, const void* norm_w, float eps, kda_gate_act gate_act,
     int H, int dk, int dv, int chunk, float scale, int32_t* dev_status, void* stream);
 
 /* A static, human-readable name for a kda_status value. */

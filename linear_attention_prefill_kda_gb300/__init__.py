@@ -26,6 +26,7 @@ _LIB_PATH = os.path.join(_HERE, "libkda.so")
 _lib = None
 
 KDA_OK, KDA_F32, KDA_BF16 = 0, 0, 1
+GATE_ACT = {"sigmoid": 0, "silu": 1}  # kda_gate_act
 STATIC_SCRATCH_BYTES = 128 << 20  # KDA_STATIC_SCRATCH_BYTES in include/kda.h
 DEV_STATUS = {0: "ok", 1: "bad state index", 2: "bad cu_seqlens", 3: "on-chip wait timeout",
               4: "checkpoint capacity exceeded"}
@@ -37,18 +38,18 @@ _SIGNATURES = {
     "kda_prefill_workspace_bytes": (_SZ, [ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_int]),
     "kda_prefill_chunked": (ctypes.c_int, [
-        _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _I64, _P, _P, _I64, ctypes.c_int, _P,
-        _P, _I32, _I64, _P, _P, _P, _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-        _F32, _P, _SZ, _P, _P]),
+        _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _I64, _P, _P, _P, _I64, ctypes.c_int,
+        _P, _P, _I32, _I64, _P, _P, _P, _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, _F32, _P, _SZ, _P, _P]),
     "kda_decode_step": (ctypes.c_int, [
         _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _P, _I64, ctypes.c_int, _P, _P, _P,
-        _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int, _F32, _P, _P]),
-    "kda_norm_gate": (ctypes.c_int, [_P, _P, _P, _F32, _P, _I64, ctypes.c_int, ctypes.c_int,
-                                     ctypes.c_int, _P]),
+        _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _F32, _P, _P]),
+    "kda_norm_gate": (ctypes.c_int, [_P, _P, _P, _F32, ctypes.c_int, _P, _I64, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, _P]),
     "kda_prefill_chunked_static_scratch": (ctypes.c_int, [
-        _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _I64, _P, _P, _I64, ctypes.c_int, _P,
-        _P, _I32, _I64, _P, _P, _P, _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-        _F32, _P, _P]),
+        _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _I64, _P, _P, _P, _I64, ctypes.c_int,
+        _P, _P, _I32, _I64, _P, _P, _P, _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, _F32, _P, _P]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kda_version": (ctypes.c_int, []),
 }
@@ -129,7 +130,8 @@ def prefill_launches(dk: int, dv: int, chunk: int, in_dtype, gate: bool) -> int:
 def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, *,
                         chunk: int = 64, checkpoints=None, checkpoint_every: int = 0,
                         ckpt_offsets=None, gate=None, norm_w=None, eps: float = 1e-6,
-                        scale: float = 0.0, workspace=None, dev_status=None, stream=None):
+                        gate_act: str = "sigmoid", has_initial_state=None, scale: float = 0.0,
+                        workspace=None, dev_status=None, stream=None):
     """Chunked varlen prefill (see ``include/kda.h``).  All tensors on one
     CUDA device; ``state_pool`` is updated in place, ``out`` (and
     ``checkpoints``/``ckpt_offsets`` when given) are written."""
@@ -140,17 +142,18 @@ def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_indices, state_pool,
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = load().kda_prefill_chunked(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(cu_seqlens), N, T,
-        _ptr(state_indices), _ptr(state_pool), state_pool.shape[0], _dtype(state_pool), _ptr(out),
-        _ptr(checkpoints), int(checkpoint_every), cap, _ptr(ckpt_offsets), _ptr(gate),
-        _ptr(norm_w), float(eps), H, dk, dv, int(chunk), float(scale), _ptr(workspace), ws_bytes,
-        _ptr(dev_status), _stream(stream))
+        _ptr(state_indices), _ptr(has_initial_state), _ptr(state_pool), state_pool.shape[0],
+        _dtype(state_pool), _ptr(out), _ptr(checkpoints), int(checkpoint_every), cap,
+        _ptr(ckpt_offsets), _ptr(gate), _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk, dv,
+        int(chunk), float(scale), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
     _check(st, "kda_prefill_chunked")
 
 
 def kda_prefill_chunked_static_scratch(q, k, v, g, beta, cu_seqlens, state_indices, state_pool,
                                        out, *, chunk: int = 64, checkpoints=None,
                                        checkpoint_every: int = 0, ckpt_offsets=None, gate=None,
-                                       norm_w=None, eps: float = 1e-6, scale: float = 0.0,
+                                       norm_w=None, eps: float = 1e-6, gate_act: str = "sigmoid",
+                                       has_initial_state=None, scale: float = 0.0,
                                        dev_status=None, stream=None):
     """kda_prefill_chunked for callers that cannot allocate: the library's own
     device array (STATIC_SCRATCH_BYTES) replaces the workspace.  Calls share
@@ -161,28 +164,30 @@ def kda_prefill_chunked_static_scratch(q, k, v, g, beta, cu_seqlens, state_indic
     cap = checkpoints.shape[0] if checkpoints is not None else 0
     st = load().kda_prefill_chunked_static_scratch(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(cu_seqlens), N, T,
-        _ptr(state_indices), _ptr(state_pool), state_pool.shape[0], _dtype(state_pool), _ptr(out),
-        _ptr(checkpoints), int(checkpoint_every), cap, _ptr(ckpt_offsets), _ptr(gate),
-        _ptr(norm_w), float(eps), H, dk, dv, int(chunk), float(scale), _ptr(dev_status),
-        _stream(stream))
+        _ptr(state_indices), _ptr(has_initial_state), _ptr(state_pool), state_pool.shape[0],
+        _dtype(state_pool), _ptr(out), _ptr(checkpoints), int(checkpoint_every), cap,
+        _ptr(ckpt_offsets), _ptr(gate), _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk, dv,
+        int(chunk), float(scale), _ptr(dev_status), _stream(stream))
     _check(st, "kda_prefill_chunked_static_scratch")
 
 
 def kda_decode_step(q, k, v, g, beta, state_indices, state_pool, out, *, gate=None, norm_w=None,
-                    eps: float = 1e-6, scale: float = 0.0, dev_status=None, stream=None):
+                    eps: float = 1e-6, gate_act: str = "sigmoid", scale: float = 0.0,
+                    dev_status=None, stream=None):
     """One recurrent decode step for N one-token sequences (see ``include/kda.h``)."""
     N, H, dk = q.shape
     dv = v.shape[-1]
     st = load().kda_decode_step(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(state_indices), N,
         _ptr(state_pool), state_pool.shape[0], _dtype(state_pool), _ptr(out), _ptr(gate),
-        _ptr(norm_w), float(eps), H, dk, dv, float(scale), _ptr(dev_status), _stream(stream))
+        _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk, dv, float(scale), _ptr(dev_status),
+        _stream(stream))
     _check(st, "kda_decode_step")
 
 
-def kda_norm_gate(o, gate, w, y, *, eps: float = 1e-6, stream=None):
-    """y = o / sqrt(mean(o^2)+eps) * w * sigmoid(gate) over the last dim of [rows, H, dv]."""
+def kda_norm_gate(o, gate, w, y, *, eps: float = 1e-6, gate_act: str = "sigmoid", stream=None):
+    """y = o / sqrt(mean(o^2)+eps) * w * act(gate) over the last dim of [rows, H, dv]."""
     rows, H, dv = o.shape
-    st = load().kda_norm_gate(_ptr(o), _ptr(gate), _ptr(w), float(eps), _ptr(y), rows, H, dv,
-                              _dtype(o), _stream(stream))
+    st = load().kda_norm_gate(_ptr(o), _ptr(gate), _ptr(w), float(eps), GATE_ACT[gate_act],
+                              _ptr(y), rows, H, dv, _dtype(o), _stream(stream))
     _check(st, "kda_norm_gate")

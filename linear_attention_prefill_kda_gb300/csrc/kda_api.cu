@@ -11,6 +11,7 @@ namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool dtype_ok(kda_dtype d) { return d == KDA_F32 || d == KDA_BF16; }
 bool dim_ok(int d) { return d == 16 || d == 64 || d == 128; }
+bool act_ok(kda_gate_act a) { return a == KDA_GATE_SIGMOID || a == KDA_GATE_SILU; }
 
 // Every non-NULL pointer must be 16-byte aligned; required ones must be non-NULL.
 bool ptr_ok(const void* p, bool required) {
@@ -24,7 +25,7 @@ kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR
 
 extern "C" {
 
-int kda_version(void) { return 100; }
+int kda_version(void) { return 101; }
 
 const char* kda_status_string(kda_status s) {
   switch (s) {
@@ -44,13 +45,15 @@ size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int 
 
 kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, const void* g,
                                const void* beta, kda_dtype in_dtype, const int32_t* cu_seqlens,
-                               int N, int64_t T, const int32_t* state_indices, void* state_pool,
+                               int N, int64_t T, const int32_t* state_indices,
+                               const int32_t* has_initial_state, void* state_pool,
                                int64_t num_slots, kda_dtype state_dtype, void* out,
                                void* checkpoints, int32_t checkpoint_every,
                                int64_t checkpoint_capacity, int32_t* ckpt_offsets,
-                               const void* gate, const void* norm_w, float eps, int H, int dk,
-                               int dv, int chunk, float scale, void* workspace,
-                               size_t workspace_bytes, int32_t* dev_status, void* stream) {
+                               const void* gate, const void* norm_w, float eps,
+                               kda_gate_act gate_act, int H, int dk, int dv, int chunk,
+                               float scale, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream) {
   if (N < 0 || T < 0 || T > INT32_MAX || H <= 0 || H > 65535 || num_slots <= 0) return KDA_ERR_INVALID_ARG;
   if ((int64_t)N * H > INT32_MAX || (T / 16 + N) * (int64_t)H > INT32_MAX) return KDA_ERR_INVALID_ARG;
   if (!dtype_ok(in_dtype) || !dtype_ok(state_dtype)) return KDA_ERR_UNSUPPORTED;
@@ -63,7 +66,9 @@ kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, cons
     return KDA_ERR_INVALID_ARG;
   if (!ptr_ok(cu_seqlens, true) || !ptr_ok(state_indices, N > 0) || !ptr_ok(state_pool, true))
     return KDA_ERR_INVALID_ARG;
-  if (!ptr_ok(ckpt_offsets, false) || !ptr_ok(dev_status, false)) return KDA_ERR_INVALID_ARG;
+  if (!ptr_ok(ckpt_offsets, false) || !ptr_ok(dev_status, false) || !ptr_ok(has_initial_state, false))
+    return KDA_ERR_INVALID_ARG;
+  if (!act_ok(gate_act)) return KDA_ERR_INVALID_ARG;
   if ((gate == nullptr) != (norm_w == nullptr)) return KDA_ERR_INVALID_ARG;
   if (!ptr_ok(gate, false) || !ptr_ok(norm_w, false)) return KDA_ERR_INVALID_ARG;
   if (gate && !(eps >= 0.f)) return KDA_ERR_INVALID_ARG;
@@ -82,6 +87,7 @@ kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, cons
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
   p.cu_seqlens = cu_seqlens;
   p.state_indices = state_indices;
+  p.has_initial_state = has_initial_state;
   p.state_pool = state_pool;
   p.out = out;
   p.checkpoints = checkpoints;
@@ -95,14 +101,16 @@ kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, cons
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)dk);
   p.eps = eps;
   p.in_dtype = in_dtype; p.state_dtype = state_dtype;
+  p.gate_act = gate_act;
   return from_cuda(kda::launch_prefill(p, st));
 }
 
 kda_status kda_decode_step(const void* q, const void* k, const void* v, const void* g,
                            const void* beta, kda_dtype in_dtype, const int32_t* state_indices,
                            int N, void* state_pool, int64_t num_slots, kda_dtype state_dtype,
-                           void* out, const void* gate, const void* norm_w, float eps, int H,
-                           int dk, int dv, float scale, int32_t* dev_status, void* stream) {
+                           void* out, const void* gate, const void* norm_w, float eps,
+                           kda_gate_act gate_act, int H, int dk, int dv, float scale,
+                           int32_t* dev_status, void* stream) {
   if (N < 0 || H <= 0 || num_slots <= 0) return KDA_ERR_INVALID_ARG;
   if ((int64_t)N * H > INT32_MAX) return KDA_ERR_INVALID_ARG;
   if (!dtype_ok(in_dtype) || !dtype_ok(state_dtype)) return KDA_ERR_UNSUPPORTED;
@@ -115,6 +123,7 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const vo
   if ((gate == nullptr) != (norm_w == nullptr)) return KDA_ERR_INVALID_ARG;
   if (!ptr_ok(gate, false) || !ptr_ok(norm_w, false)) return KDA_ERR_INVALID_ARG;
   if (gate && !(eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+  if (!act_ok(gate_act)) return KDA_ERR_INVALID_ARG;
   kda::DecodeParams p{};
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
   p.state_indices = state_indices;
@@ -127,12 +136,14 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const vo
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)dk);
   p.eps = eps;
   p.in_dtype = in_dtype; p.state_dtype = state_dtype;
+  p.gate_act = gate_act;
   return from_cuda(kda::launch_decode(p, static_cast<cudaStream_t>(stream)));
 }
 
-kda_status kda_norm_gate(const void* o, const void* gate, const void* w, float eps, void* y,
-                         int64_t rows, int H, int dv, kda_dtype dtype, void* stream) {
-  if (rows < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+kda_status kda_norm_gate(const void* o, const void* gate, const void* w, float eps,
+                         kda_gate_act gate_act, void* y, int64_t rows, int H, int dv,
+                         kda_dtype dtype, void* stream) {
+  if (rows < 0 || H <= 0 || !act_ok(gate_act)) return KDA_ERR_INVALID_ARG;
   if (!dtype_ok(dtype)) return KDA_ERR_UNSUPPORTED;
   if (!dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
   if (!(eps >= 0.f)) return KDA_ERR_INVALID_ARG;
@@ -142,7 +153,7 @@ kda_status kda_norm_gate(const void* o, const void* gate, const void* w, float e
     return KDA_ERR_INVALID_ARG;
   kda::NormGateParams p{};
   p.o = o; p.gate = gate; p.w = w; p.y = y;
-  p.rows = rows; p.H = H; p.dv = dv; p.eps = eps; p.dtype = dtype;
+  p.rows = rows; p.H = H; p.dv = dv; p.eps = eps; p.dtype = dtype; p.gate_act = gate_act;
   return from_cuda(kda::launch_norm_gate(p, static_cast<cudaStream_t>(stream)));
 }
 

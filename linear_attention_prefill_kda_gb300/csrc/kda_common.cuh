@@ -69,7 +69,13 @@ __device__ __forceinline__ void latch_status(int32_t* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+// Gate activation of the RMSNorm-gate: sigmoid (act 0) or SiLU x*sigmoid(x) (act 1).
+__device__ __forceinline__ float gate_actf(float x, int act) {
+  const float s = sigmoidf_(x);
+  return act == KDA_GATE_SILU ? x * s : s;
+}
 
 // Floor applied to the per-token log-decay g by the chunked prefill kernels.
 // exp(-30) = 9.4e-14, so a token below the floor still erases the history to

@@ -9,7 +9,8 @@
 //     u_j = beta (v_j - p_j)
 //     S_ij <- alpha_i S_ij + k_i u_j
 //     o_j = scale (r_j + (q . k) u_j)        (= scale * (S_new^T q)_j)
-// then the optional RMSNorm-gate over the dv outputs of the row.
+// then the optional RMSNorm-gate (sigmoid or SiLU gate) over the dv outputs of
+// the row.
 //
 // The step is a pure HBM stream over the state (dk*dv elements read and
 // written once): one CTA per (sequence, head); a warp reads whole rows of the
@@ -132,10 +133,10 @@ decode_kernel(DecodeParams p) {
     const float inv = rsqrtf(ss / (float)DV + p.eps);
     const float4 gt = load4(reinterpret_cast<const TI*>(p.gate) + row * DV + cg * 4);
     const float4 w = load4(reinterpret_cast<const TI*>(p.norm_w) + cg * 4);
-    o[0] *= inv * w.x * sigmoidf_(gt.x);
-    o[1] *= inv * w.y * sigmoidf_(gt.y);
-    o[2] *= inv * w.z * sigmoidf_(gt.z);
-    o[3] *= inv * w.w * sigmoidf_(gt.w);
+    o[0] *= inv * w.x * gate_actf(gt.x, p.gate_act);
+    o[1] *= inv * w.y * gate_actf(gt.y, p.gate_act);
+    o[2] *= inv * w.z * gate_actf(gt.z, p.gate_act);
+    o[3] *= inv * w.w * gate_actf(gt.w, p.gate_act);
   }
   store4(out + cg * 4, make_float4(o[0], o[1], o[2], o[3]));
 }

@@ -21,6 +21,7 @@ struct DecodeParams {
   int N, H, dk, dv;
   float scale, eps;
   kda_dtype in_dtype, state_dtype;
+  int gate_act;  // kda_gate_act
 };
 
 struct NormGateParams {
@@ -31,12 +32,14 @@ struct NormGateParams {
   float eps;
   kda_dtype dtype;  // of gate, w and y (and of o unless o_f32)
   bool o_f32;       // o is fp32 scratch regardless of dtype
+  int gate_act;     // kda_gate_act
 };
 
 struct PrefillParams {
   const void *q, *k, *v, *g, *beta;
   const int32_t* cu_seqlens;
   const int32_t* state_indices;
+  const int32_t* has_initial_state;  // NULL: every sequence starts from its slot
   void* state_pool;
   void* out;
   void* checkpoints;
@@ -50,6 +53,7 @@ struct PrefillParams {
   int N, H, dk, dv, chunk, checkpoint_every;
   float scale, eps;
   kda_dtype in_dtype, state_dtype;
+  int gate_act;  // kda_gate_act
 };
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device), so

@@ -55,9 +55,10 @@ cudaError_t static_scratch_address(void** out) {
 
 extern "C" KDA_API kda_status kda_prefill_chunked_static_scratch(
     const void* q, const void* k, const void* v, const void* g, const void* beta, kda_dtype in_dtype,
-    const int32_t* cu_seqlens, int N, int64_t T, const int32_t* state_indices, void* state_pool,
-    int64_t num_slots, kda_dtype state_dtype, void* out, void* checkpoints, int32_t checkpoint_every,
-    int64_t checkpoint_capacity, int32_t* ckpt_offsets, const void* gate, const void* norm_w, float eps,
+    const int32_t* cu_seqlens, int N, int64_t T, const int32_t* state_indices,
+    const int32_t* has_initial_state, void* state_pool, int64_t num_slots, kda_dtype state_dtype,
+    void* out, void* checkpoints, int32_t checkpoint_every, int64_t checkpoint_capacity,
+    int32_t* ckpt_offsets, const void* gate, const void* norm_w, float eps, kda_gate_act gate_act,
     int H, int dk, int dv, int chunk, float scale, int32_t* dev_status, void* stream) {
   // Sizes beyond the array are rejected before any device work.
   if (N < 0 || T < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
@@ -68,8 +69,9 @@ extern "C" KDA_API kda_status kda_prefill_chunked_static_scratch(
   if (need > (size_t)KDA_STATIC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (need > 0 && static_scratch_address(&scratch) != cudaSuccess) return KDA_ERR_CUDA;
-  return kda_prefill_chunked(q, k, v, g, beta, in_dtype, cu_seqlens, N, T, state_indices, state_pool,
-                             num_slots, state_dtype, out, checkpoints, checkpoint_every, checkpoint_capacity,
-                             ckpt_offsets, gate, norm_w, eps, H, dk, dv, chunk, scale, scratch,
-                             need > 0 ? (size_t)KDA_STATIC_SCRATCH_BYTES : 0, dev_status, stream);
+  return kda_prefill_chunked(q, k, v, g, beta, in_dtype, cu_seqlens, N, T, state_indices, has_initial_state,
+                             state_pool, num_slots, state_dtype, out, checkpoints, checkpoint_every,
+                             checkpoint_capacity, ckpt_offsets, gate, norm_w, eps, gate_act, H, dk, dv, chunk,
+                             scale, scratch, need > 0 ? (size_t)KDA_STATIC_SCRATCH_BYTES : 0, dev_status,
+                             stream);
 }

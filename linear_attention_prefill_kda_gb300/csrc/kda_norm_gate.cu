@@ -1,6 +1,6 @@
 // Standalone output RMSNorm-gate ("[Feature][KDA] Add Kimi K3 KDA execution",
 // first section: FusedRMSNormGated output normalisation and gating):
-//     y = o / sqrt(mean_dv(o^2) + eps) * w * sigmoid(gate)
+//     y = o / sqrt(mean_dv(o^2) + eps) * w * act(gate),  act = sigmoid or SiLU
 // One warp per (token, head) row; each lane holds dv/32 elements (dv/4 lanes
 // with 4 elements each when dv < 128), loaded as one vector.  Memory bound:
 // reads o and gate, writes y once.  y may alias o.
@@ -32,10 +32,10 @@ __global__ void __launch_bounds__(256) norm_gate_kernel(NormGateParams p) {
   const float inv = rsqrtf(ss / (float)DV + p.eps);
   const float4 g = load4(gt + lane * 4);
   const float4 w = load4(reinterpret_cast<const T*>(p.w) + lane * 4);
-  x.x *= inv * w.x * sigmoidf_(g.x);
-  x.y *= inv * w.y * sigmoidf_(g.y);
-  x.z *= inv * w.z * sigmoidf_(g.z);
-  x.w *= inv * w.w * sigmoidf_(g.w);
+  x.x *= inv * w.x * gate_actf(g.x, p.gate_act);
+  x.y *= inv * w.y * gate_actf(g.y, p.gate_act);
+  x.z *= inv * w.z * gate_actf(g.z, p.gate_act);
+  x.w *= inv * w.w * gate_actf(g.w, p.gate_act);
   store4(y + lane * 4, x);
 }
 

@@ -76,6 +76,7 @@ cudaError_t launch_prefill(const PrefillParams& p_in, cudaStream_t stream) {
     ng.o_f32 = scratch;
     ng.gate = p.gate; ng.w = p.norm_w; ng.y = p.out;
     ng.rows = p.T; ng.H = p.H; ng.dv = p.dv; ng.eps = p.eps; ng.dtype = p.in_dtype;
+    ng.gate_act = p.gate_act;
     e = launch_norm_gate(ng, stream);
   }
   return e;

@@ -5,6 +5,8 @@
 //    zeroed ("[Feature][KDA] Add Kimi K3 KDA execution", section "KDA
 //    execution", step 5);
 //  - a zero-length sequence is a no-op;
+//  - a sequence whose has_initial_state flag is 0 starts from a zero state
+//    (a new prompt: "[Feature][KDA] ...", section "Metadata construction");
 //  - sequence i owns checkpoint entries [off_i, off_i + floor(len_i / I)),
 //    off_i the exclusive prefix sum, written to ckpt_offsets.
 #pragma once
@@ -20,6 +22,7 @@ struct SeqInfo {
   int32_t slot;
   bool zero_rows;
   bool ckpt_ok;
+  bool init;  // start from the slot's state (false: from zero, a new prompt)
 };
 
 // Must be called by every thread of the block (it contains __syncthreads).
@@ -46,6 +49,7 @@ __device__ __forceinline__ bool seq_prologue(const PrefillParams& p, int seq, in
   si.zero_rows = false;
   si.ckpt_ok = false;
   si.slot = -1;
+  si.init = p.has_initial_state == nullptr || p.has_initial_state[seq] != 0;
   const int64_t len = si.t1 - si.t0;
   if (first_slab && head == 0 && threadIdx.x == 0 && p.ckpt_offsets) {
     p.ckpt_offsets[seq] = (int32_t)si.ckpt_off;

@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(PrefillParams p)
 
   for (int i = tid; i < DK * BV; i += kThreads) {
     const int c = i / BV, v = i % BV;
-    sS[c * L::LDV + v] = to_f32(slot_state[c * DV + v0 + v]);
+    sS[c * L::LDV + v] = si.init ? to_f32(slot_state[c * DV + v0 + v]) : 0.f;
   }
 
   for (int c0 = 0; c0 < len; c0 += C) {

@@ -49,7 +49,7 @@ constexpr uint32_t WS_KLT = 32768;    // fp16 MN-major [M=c 128 x K=j 64] (K str
 constexpr uint32_t WS_U0 = 49152;     // fp16 [v/8][64 rows][8]: byte (v/8)*1024 + r*16 + (v%8)*2
 constexpr uint32_t WS_AQK = 65536;    // fp16 K-major [64 x 64] (SBO 1024)
 constexpr uint32_t WS_DECAY = 73728;  // fp32 [128]
-constexpr uint32_t WS_GW = 74240;     // fp16 [v/8][64 rows][8]: w * sigmoid(gate) (when gated)
+constexpr uint32_t WS_GW = 74240;     // fp16 [v/8][64 rows][8]: w * act(gate) (when gated)
 constexpr uint32_t WS_BYTES = 90624;
 constexpr uint32_t WS_COPY0 = 65536;  // PA | KLT | U0
 constexpr uint32_t WS_COPY1 = 8704;   // AQK | DECAY
@@ -174,7 +174,7 @@ __device__ void intra_exact_A(const bf16* fk, const bf16* fq, const float* fg, i
   }
 }
 
-// w * sigmoid(gate) for row r, channels [c0, c0 + 32) of a chunk -> fp16 in the
+// w * act(gate) for row r, channels [c0, c0 + 32) of a chunk -> fp16 in the
 // workspace (the output epilogue of the state kernel then needs two multiplies).
 __device__ __forceinline__ void gated_weight_rows(const PrefillParams& p, uint8_t* ws, int64_t tb, int head,
                                                   int n, int r, int c0) {
@@ -191,7 +191,7 @@ __device__ __forceinline__ void gated_weight_rows(const PrefillParams& p, uint8_
     }
     unpack_bf8(__ldg(reinterpret_cast<const uint4*>(gw) + i), w8);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) x[u] = __fdividef(w8[u], 1.f + __expf(-x[u]));
+    for (int u = 0; u < 8; ++u) x[u] = w8[u] * gate_actf(x[u], p.gate_act);
     *reinterpret_cast<uint4*>(ws + WS_GW + ((c0 + 8 * i) >> 3) * 1024 + r * 16) = pack_half8(x);
   }
 }
@@ -731,7 +731,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   // state row lrow, columns [64 hh, 64 hh + 64), fp32 in registers for the whole call
   TS* slot_state = reinterpret_cast<TS*>(p.state_pool) + ((int64_t)si.slot * H + head) * (D * D);
   float S[64];
-  load_state_row(slot_state + lrow * D + hh * 64, S);
+  if (si.init) {
+    load_state_row(slot_state + lrow * D + hh * 64, S);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) S[i] = 0.f;
+  }
   tc::fence_proxy_async();
   tc::fence_before_sync();
   __syncthreads();
@@ -768,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   write_sop();
 
   bf16* gout = reinterpret_cast<bf16*>(p.out);
-  uint4 graw[8];  // w * sigmoid(gate) (fp16) of the output row whose epilogue is pending
+  uint4 graw[8];  // w * act(gate) (fp16) of the output row whose epilogue is pending
 
   // Output epilogue of chunk kp (query-side warps only; they synchronise among
   // themselves with named barrier 1): read scale * O from TMEM, RMSNorm-gate,

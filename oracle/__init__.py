@@ -52,16 +52,17 @@ def _load():
             P = ctypes.c_void_p
             lib.kda_oracle_prefill.restype = ctypes.c_int
             lib.kda_oracle_prefill.argtypes = [
-                P, P, P, P, P, P, ctypes.c_int, P, P, ctypes.c_int64, P, P, ctypes.c_int,
+                P, P, P, P, P, P, ctypes.c_int, P, P, P, ctypes.c_int64, P, P, ctypes.c_int,
                 ctypes.c_int64, P, P, P, ctypes.c_double, ctypes.c_int, ctypes.c_int,
-                ctypes.c_int, ctypes.c_double, ctypes.c_int]
+                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int]
             lib.kda_oracle_decode.restype = ctypes.c_int
             lib.kda_oracle_decode.argtypes = [
                 P, P, P, P, P, P, ctypes.c_int, P, ctypes.c_int64, P, P, P, ctypes.c_double,
-                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int]
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                ctypes.c_int]
             lib.kda_oracle_norm_gate.restype = ctypes.c_int
             lib.kda_oracle_norm_gate.argtypes = [P, P, P, ctypes.c_double, P, ctypes.c_int64,
-                                                 ctypes.c_int]
+                                                 ctypes.c_int, ctypes.c_int]
             lib.kda_oracle_checkpoint_offsets.restype = ctypes.c_int64
             lib.kda_oracle_checkpoint_offsets.argtypes = [P, ctypes.c_int, ctypes.c_int, P]
             lib.kda_oracle_max_threads.restype = ctypes.c_int
@@ -108,8 +109,12 @@ def checkpoint_offsets(cu_seqlens, every: int) -> np.ndarray:
     return offs
 
 
+ACT = {"sigmoid": 0, "silu": 1}
+
+
 def prefill(q, k, v, g, beta, cu_seqlens, state_indices, pool, *, checkpoint_every=0,
-            gate=None, norm_w=None, eps=1e-6, scale=None, nthreads=0):
+            gate=None, norm_w=None, eps=1e-6, scale=None, nthreads=0, has_initial_state=None,
+            gate_act="sigmoid"):
     """Token-by-token KDA prefill in fp64.
 
     Shapes: q,k,g [T,H,dk]; v [T,H,dv]; beta [T,H]; cu_seqlens [N+1];
@@ -119,6 +124,7 @@ def prefill(q, k, v, g, beta, cu_seqlens, state_indices, pool, *, checkpoint_eve
     """
     q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
     cu, idx = _i32(cu_seqlens), _i32(state_indices)
+    his = None if has_initial_state is None else _i32(has_initial_state)
     pool = _f64(pool).copy()
     gate, norm_w = _f64(gate), _f64(norm_w)
     T, H, dk = q.shape
@@ -132,15 +138,16 @@ def prefill(q, k, v, g, beta, cu_seqlens, state_indices, pool, *, checkpoint_eve
     out = np.zeros((T, H, dv), np.float64)
     offs_out = np.zeros(N + 1, np.int32)
     rc = _load().kda_oracle_prefill(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu), N, _ptr(idx), _ptr(pool),
-        pool.shape[0], _ptr(out), _ptr(ck), int(checkpoint_every), ck.shape[0], _ptr(offs_out),
-        _ptr(gate), _ptr(norm_w), float(eps), H, dk, dv, float(scale), int(nthreads))
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu), N, _ptr(idx), _ptr(his),
+        _ptr(pool), pool.shape[0], _ptr(out), _ptr(ck), int(checkpoint_every), ck.shape[0],
+        _ptr(offs_out), _ptr(gate), _ptr(norm_w), float(eps), ACT[gate_act], H, dk, dv,
+        float(scale), int(nthreads))
     _check(rc)
     return out, pool, ck[:n_ck], offs_out
 
 
 def decode(q, k, v, g, beta, state_indices, pool, *, gate=None, norm_w=None, eps=1e-6,
-           scale=None, nthreads=0):
+           scale=None, nthreads=0, gate_act="sigmoid"):
     """One recurrent decode step in fp64.  q,k,g [N,H,dk]; v [N,H,dv]; beta [N,H].
 
     Returns ``(out [N,H,dv], pool_after)``; the input pool is not modified.
@@ -156,17 +163,18 @@ def decode(q, k, v, g, beta, state_indices, pool, *, gate=None, norm_w=None, eps
     out = np.zeros((N, H, dv), np.float64)
     rc = _load().kda_oracle_decode(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(idx), N, _ptr(pool), pool.shape[0],
-        _ptr(out), _ptr(gate), _ptr(norm_w), float(eps), H, dk, dv, float(scale), int(nthreads))
+        _ptr(out), _ptr(gate), _ptr(norm_w), float(eps), ACT[gate_act], H, dk, dv, float(scale),
+        int(nthreads))
     _check(rc)
     return out, pool
 
 
-def norm_gate(o, gate, w, eps=1e-6):
-    """y = o / sqrt(mean(o^2)+eps) * w * sigmoid(gate) over the last dimension."""
+def norm_gate(o, gate, w, eps=1e-6, gate_act="sigmoid"):
+    """y = o / sqrt(mean(o^2)+eps) * w * act(gate) over the last dimension."""
     o, gate, w = _f64(o), _f64(gate), _f64(w)
     dv = o.shape[-1]
     rows = o.size // dv
     y = np.zeros_like(o)
     _check(_load().kda_oracle_norm_gate(_ptr(o), _ptr(gate), _ptr(w), float(eps), _ptr(y),
-                                        rows, dv))
+                                        rows, dv, ACT[gate_act]))
     return y

@@ -37,9 +37,14 @@
  * ckpt_offsets[i] is the exclusive prefix sum of floor(len_i/I).
  *
  * Output norm-gate ("[Feature][KDA] ...", first section: FusedRMSNormGated,
- * output normalisation and gating):
- *     y = o / sqrt(mean_dv(o^2) + eps) * w * sigmoid(gate)
+ * output normalisation and gating; its test coverage names sigmoid and SiLU):
+ *     y = o / sqrt(mean_dv(o^2) + eps) * w * act(gate),  act = sigmoid or SiLU
  * per (token, head) row, weight w[dv] shared by the heads.
+ *
+ * Sequences without initial state ("[Feature][KDA] ...", section "Metadata
+ * construction": a one-token prompt without state is still prefill): when a
+ * has_initial_state flag is 0 the sequence starts from S = 0 instead of its
+ * slot's content.
  *
  * Everything is fp64.  Layouts are row-major, last dimension contiguous:
  *   q,k,g [T,H,dk]   v [T,H,dv]   beta [T,H]   out/gate [T,H,dv]
@@ -86,23 +91,26 @@ static void token_step(double* S, int dk, int dv, const double* q, const double*
   for (int j = 0; j < dv; ++j) o[j] *= scale;
 }
 
-/* y = o / sqrt(mean(o^2) + eps) * w * sigmoid(gate) over one row of dv. */
+/* y = o / sqrt(mean(o^2) + eps) * w * act(gate) over one row of dv, where
+ * act is the sigmoid (act == 0) or SiLU, x * sigmoid(x) (act == 1): the two
+ * gate activations the pages' norm-gate coverage lists. */
 static void norm_gate_row(const double* o, const double* gate, const double* w, double eps,
-                          int dv, double* y) {
+                          int dv, int act, double* y) {
   double ss = 0.0;
   for (int j = 0; j < dv; ++j) ss += o[j] * o[j];
   const double inv = 1.0 / sqrt(ss / (double)dv + eps);
   for (int j = 0; j < dv; ++j) {
     const double sig = 1.0 / (1.0 + exp(-gate[j]));
-    y[j] = o[j] * inv * w[j] * sig;
+    const double a = act == 1 ? gate[j] * sig : sig;
+    y[j] = o[j] * inv * w[j] * a;
   }
 }
 
 int kda_oracle_norm_gate(const double* o, const double* gate, const double* w, double eps,
-                         double* y, int64_t rows, int dv) {
-  if (!o || !gate || !w || !y || rows < 0 || dv <= 0) return ORACLE_ERR_ARG;
+                         double* y, int64_t rows, int dv, int act) {
+  if (!o || !gate || !w || !y || rows < 0 || dv <= 0 || act < 0 || act > 1) return ORACLE_ERR_ARG;
   for (int64_t r = 0; r < rows; ++r)
-    norm_gate_row(o + r * dv, gate + r * dv, w, eps, dv, y + r * dv);
+    norm_gate_row(o + r * dv, gate + r * dv, w, eps, dv, act, y + r * dv);
   return ORACLE_OK;
 }
 
@@ -129,12 +137,14 @@ int64_t kda_oracle_checkpoint_offsets(const int32_t* cu_seqlens, int N, int ever
  */
 int kda_oracle_prefill(const double* q, const double* k, const double* v, const double* g,
                        const double* beta, const int32_t* cu_seqlens, int N,
-                       const int32_t* state_indices, double* pool, int64_t num_slots,
+                       const int32_t* state_indices, const int32_t* has_initial_state,
+                       double* pool, int64_t num_slots,
                        double* out, double* checkpoints, int checkpoint_every,
                        int64_t checkpoint_capacity, int32_t* ckpt_offsets,
-                       const double* gate, const double* norm_w, double eps, int H, int dk,
-                       int dv, double scale, int nthreads) {
+                       const double* gate, const double* norm_w, double eps, int act, int H,
+                       int dk, int dv, double scale, int nthreads) {
   if (N < 0 || H <= 0 || dk <= 0 || dv <= 0 || checkpoint_every < 0) return ORACLE_ERR_ARG;
+  if (act < 0 || act > 1) return ORACLE_ERR_ARG;
   if (N == 0) return ORACLE_OK;
   if (!cu_seqlens || !state_indices || !pool || !out) return ORACLE_ERR_ARG;
   if (gate && !norm_w) return ORACLE_ERR_ARG;
@@ -182,12 +192,15 @@ int kda_oracle_prefill(const double* q, const double* k, const double* v, const 
       }
       if (t1 == t0) continue;
       double* slot_state = pool + ((size_t)slot * H + h) * sd;
-      memcpy(S, slot_state, sizeof(double) * sd);
+      /* a sequence without initial state (a new prompt) starts from zero; its
+       * final state is still written to the slot */
+      if (has_initial_state && has_initial_state[i] == 0) memset(S, 0, sizeof(double) * sd);
+      else memcpy(S, slot_state, sizeof(double) * sd);
       int64_t m = 0;
       for (int64_t t = t0; t < t1; ++t) {
         const size_t qk = ((size_t)t * H + h) * dk, vo = ((size_t)t * H + h) * dv;
         token_step(S, dk, dv, q + qk, k + qk, v + vo, g + qk, beta[(size_t)t * H + h], scale, u, o);
-        if (gate) norm_gate_row(o, gate + vo, norm_w, eps, dv, out + vo);
+        if (gate) norm_gate_row(o, gate + vo, norm_w, eps, dv, act, out + vo);
         else memcpy(out + vo, o, sizeof(double) * dv);
         if (checkpoint_every > 0 && (t - t0 + 1) % checkpoint_every == 0) {
           memcpy(checkpoints + (((size_t)offs[i] + m) * H + h) * sd, S, sizeof(double) * sd);
@@ -212,14 +225,15 @@ int kda_oracle_prefill(const double* q, const double* k, const double* v, const 
 int kda_oracle_decode(const double* q, const double* k, const double* v, const double* g,
                       const double* beta, const int32_t* state_indices, int N, double* pool,
                       int64_t num_slots, double* out, const double* gate, const double* norm_w,
-                      double eps, int H, int dk, int dv, double scale, int nthreads) {
+                      double eps, int act, int H, int dk, int dv, double scale, int nthreads) {
   if (N < 0) return ORACLE_ERR_ARG;
   if (N == 0) return ORACLE_OK;
   int32_t* cu = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N + 1));
   if (!cu) return ORACLE_ERR_NOMEM;
   for (int i = 0; i <= N; ++i) cu[i] = i;
-  const int rc = kda_oracle_prefill(q, k, v, g, beta, cu, N, state_indices, pool, num_slots, out,
-                                    NULL, 0, 0, NULL, gate, norm_w, eps, H, dk, dv, scale, nthreads);
+  const int rc = kda_oracle_prefill(q, k, v, g, beta, cu, N, state_indices, NULL, pool, num_slots,
+                                    out, NULL, 0, 0, NULL, gate, norm_w, eps, act, H, dk, dv, scale,
+                                    nthreads);
   free(cu);
   return rc;
 }

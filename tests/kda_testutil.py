@@ -61,7 +61,9 @@ def run_prefill(kda, d, w, dev, *, lengths=None, ckpt=True, out_dtype=None):
                             t["state_indices"], t["pool"], out, chunk=w.chunk, checkpoints=ck,
                             checkpoint_every=I, ckpt_offsets=offs, gate=t.get("gate"),
                             norm_w=t.get("norm_w"), eps=d.get("eps", 1e-6), scale=d["scale"],
-                            workspace=ws, dev_status=status)
+                            gate_act=d.get("gate_act", "sigmoid"),
+                            has_initial_state=t.get("has_initial_state"), workspace=ws,
+                            dev_status=status)
     torch.cuda.synchronize()
     return out, t["pool"], ck, offs, status
 
@@ -75,4 +77,6 @@ def oracle_prefill(oracle, d, w, *, ckpt=True, heads=None):
                           d["cu_seqlens"], d["state_indices"], psel(d["pool"]),
                           checkpoint_every=w.checkpoint_every if ckpt else 0,
                           gate=None if gate is None else sel(gate), norm_w=d.get("norm_w"),
-                          eps=d.get("eps", 1e-6), scale=d["scale"])
+                          eps=d.get("eps", 1e-6), scale=d["scale"],
+                          gate_act=d.get("gate_act", "sigmoid"),
+                          has_initial_state=d.get("has_initial_state"))

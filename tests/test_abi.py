@@ -48,14 +48,15 @@ def test_status_strings(lib):
 
 def _prefill(lib, **over):
     a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, in_dtype=1, cu=FAKE, N=2, T=100, idx=FAKE,
-             pool=FAKE, slots=4, sdt=0, out=FAKE, ck=None, every=0, cap=0, offs=None, gate=None,
-             w=None, eps=1e-6, H=2, dk=64, dv=64, chunk=64, scale=0.0, ws=None, wsb=0, st=None)
+             his=None, pool=FAKE, slots=4, sdt=0, out=FAKE, ck=None, every=0, cap=0, offs=None,
+             gate=None, w=None, eps=1e-6, act=0, H=2, dk=64, dv=64, chunk=64, scale=0.0, ws=None,
+             wsb=0, st=None)
     a.update(over)
     return lib.kda_prefill_chunked(
         a["q"], a["k"], a["v"], a["g"], a["beta"], a["in_dtype"], a["cu"], a["N"], a["T"],
-        a["idx"], a["pool"], a["slots"], a["sdt"], a["out"], a["ck"], a["every"], a["cap"],
-        a["offs"], a["gate"], a["w"], a["eps"], a["H"], a["dk"], a["dv"], a["chunk"], a["scale"],
-        a["ws"], a["wsb"], a["st"], None)
+        a["idx"], a["his"], a["pool"], a["slots"], a["sdt"], a["out"], a["ck"], a["every"],
+        a["cap"], a["offs"], a["gate"], a["w"], a["eps"], a["act"], a["H"], a["dk"], a["dv"],
+        a["chunk"], a["scale"], a["ws"], a["wsb"], a["st"], None)
 
 
 @pytest.mark.parametrize("over,expect", [
@@ -64,7 +65,8 @@ def _prefill(lib, **over):
     (dict(q=None), -1), (dict(pool=None), -1), (dict(cu=None), -1), (dict(k=MIS), -1),
     (dict(out=MIS), -1), (dict(every=32), -1), (dict(every=128, ck=None, cap=10), -1),
     (dict(every=64, ck=FAKE, cap=0), -1), (dict(gate=FAKE), -1), (dict(w=FAKE), -1),
-    (dict(gate=FAKE, w=FAKE, eps=-1.0), -1), (dict(st=MIS), -1),
+    (dict(gate=FAKE, w=FAKE, eps=-1.0), -1), (dict(st=MIS), -1), (dict(his=MIS), -1),
+    (dict(act=2), -1), (dict(H=70000), -1),
 ])
 def test_prefill_rejects(lib, over, expect):
     assert _prefill(lib, **over) == expect
@@ -72,19 +74,19 @@ def test_prefill_rejects(lib, over, expect):
 
 def _decode(lib, **over):
     a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, in_dtype=1, idx=FAKE, N=4, pool=FAKE,
-             slots=8, sdt=0, out=FAKE, gate=None, w=None, eps=1e-6, H=2, dk=128, dv=128,
+             slots=8, sdt=0, out=FAKE, gate=None, w=None, eps=1e-6, act=0, H=2, dk=128, dv=128,
              scale=0.0, st=None)
     a.update(over)
     return lib.kda_decode_step(a["q"], a["k"], a["v"], a["g"], a["beta"], a["in_dtype"], a["idx"],
                                a["N"], a["pool"], a["slots"], a["sdt"], a["out"], a["gate"],
-                               a["w"], a["eps"], a["H"], a["dk"], a["dv"], a["scale"], a["st"],
-                               None)
+                               a["w"], a["eps"], a["act"], a["H"], a["dk"], a["dv"], a["scale"],
+                               a["st"], None)
 
 
 @pytest.mark.parametrize("over,expect", [
     (dict(dk=64), -2), (dict(dk=96, dv=96), -2), (dict(in_dtype=3), -2), (dict(N=-2), -1),
     (dict(H=-1), -1), (dict(slots=0), -1), (dict(idx=None), -1), (dict(v=MIS), -1),
-    (dict(gate=FAKE), -1), (dict(w=FAKE), -1),
+    (dict(gate=FAKE), -1), (dict(w=FAKE), -1), (dict(act=-1), -1),
 ])
 def test_decode_rejects(lib, over, expect):
     assert _decode(lib, **over) == expect
@@ -92,16 +94,17 @@ def test_decode_rejects(lib, over, expect):
 
 def test_empty_calls_are_noops(lib):
     assert _decode(lib, N=0, q=None, k=None, v=None, g=None, beta=None, idx=None, out=None) == 0
-    assert lib.kda_norm_gate(FAKE, FAKE, FAKE, 1e-6, FAKE, 0, 4, 128, 1, None) == 0
+    assert lib.kda_norm_gate(FAKE, FAKE, FAKE, 1e-6, 0, FAKE, 0, 4, 128, 1, None) == 0
 
 
 @pytest.mark.parametrize("args,expect", [
-    ((FAKE, FAKE, FAKE, 1e-6, FAKE, 10, 4, 48, 1), -2),
-    ((FAKE, FAKE, FAKE, 1e-6, FAKE, 10, 4, 128, 9), -2),
-    ((None, FAKE, FAKE, 1e-6, FAKE, 10, 4, 128, 1), -1),
-    ((FAKE, FAKE, MIS, 1e-6, FAKE, 10, 4, 128, 1), -1),
-    ((FAKE, FAKE, FAKE, -1.0, FAKE, 10, 4, 128, 1), -1),
-    ((FAKE, FAKE, FAKE, 1e-6, FAKE, -1, 4, 128, 1), -1),
+    ((FAKE, FAKE, FAKE, 1e-6, 0, FAKE, 10, 4, 48, 1), -2),
+    ((FAKE, FAKE, FAKE, 1e-6, 0, FAKE, 10, 4, 128, 9), -2),
+    ((None, FAKE, FAKE, 1e-6, 0, FAKE, 10, 4, 128, 1), -1),
+    ((FAKE, FAKE, MIS, 1e-6, 0, FAKE, 10, 4, 128, 1), -1),
+    ((FAKE, FAKE, FAKE, -1.0, 0, FAKE, 10, 4, 128, 1), -1),
+    ((FAKE, FAKE, FAKE, 1e-6, 0, FAKE, -1, 4, 128, 1), -1),
+    ((FAKE, FAKE, FAKE, 1e-6, 5, FAKE, 10, 4, 128, 1), -1),
 ])
 def test_norm_gate_rejects(lib, args, expect):
     assert lib.kda_norm_gate(*args, None) == expect
@@ -124,9 +127,9 @@ def test_static_scratch_entry_rejects_oversize_on_host(lib):
     """The no-allocation prefill refuses a problem whose scratch exceeds its
     fixed array before touching the device."""
     rc = lib.kda_prefill_chunked_static_scratch(
-        FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, 65536, FAKE, FAKE, 4, 0, FAKE, None, 0, 0, None,
-        None, None, 1e-6, 32, 128, 128, 64, 0.0, None, None)
+        FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, 65536, FAKE, None, FAKE, 4, 0, FAKE, None, 0, 0,
+        None, None, None, 1e-6, 0, 32, 128, 128, 64, 0.0, None, None)
     assert rc == -3
     assert lib.kda_prefill_chunked_static_scratch(
-        FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, 100, FAKE, FAKE, 4, 0, FAKE, None, 0, 0, None,
-        None, None, 1e-6, 2, 96, 96, 64, 0.0, None, None) == -2
+        FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, 100, FAKE, None, FAKE, 4, 0, FAKE, None, 0, 0,
+        None, None, None, 1e-6, 0, 2, 96, 96, 64, 0.0, None, None) == -2

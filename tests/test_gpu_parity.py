@@ -84,6 +84,22 @@ def test_prefill_tc_shape_mixed(kda_gpu):
     _check_prefill(kda_gpu, w, W.make_prefill(w))
 
 
+@pytest.mark.parametrize("d,in_dtype,state_dtype", [(128, torch.bfloat16, torch.float32),
+                                                    (128, torch.bfloat16, torch.bfloat16),
+                                                    (64, torch.bfloat16, torch.float32),
+                                                    (16, torch.float32, torch.float32)])
+def test_prefill_new_prompts_and_silu_gate(kda_gpu, d, in_dtype, state_dtype):
+    """Sequences flagged without initial state start from zero whatever their
+    slot holds (the slots hold random states here); the SiLU gate activation."""
+    w = W.SCHED.replace(seqlens=(70, 1, 130, 33), H=3, dk=d, dv=d, in_dtype=in_dtype,
+                        state_dtype=state_dtype, num_slots=9, slot_range=None,
+                        checkpoint_every=64, seed=600 + d)
+    dd = W.make_prefill(w)
+    dd["has_initial_state"] = torch.tensor([0, 0, 1, 0], dtype=torch.int32)
+    dd["gate_act"] = "silu"
+    _check_prefill(kda_gpu, w, dd)
+
+
 def test_prefill_gate_fp32_and_chunk16(kda_gpu):
     w = W.SCHED.replace(seqlens=(100, 37, 256), H=4, dk=64, dv=64, chunk=16, checkpoint_every=32,
                         in_dtype=torch.float32, num_slots=8, slot_range=None, seed=77)
@@ -207,6 +223,25 @@ def test_decode_full_64_steps(kda_gpu):
     assert torch.equal(dev_pool[mask.to(DEV)].cpu(), pool0[mask])
 
 
+@pytest.mark.parametrize("act", ["sigmoid", "silu"])
+def test_decode_gate_activations(kda_gpu, act):
+    w = W.DECODE.replace(N=6, H=2, num_slots=8, seed=710)
+    pd = W.make_decode_pool(w)
+    sd = W.make_decode_step(w, 0)
+    pool = pd["pool"].to(DEV)
+    t = to_dev(sd, DEV)
+    out = torch.empty(w.N, w.H, w.dv, device=DEV, dtype=w.in_dtype)
+    kda_gpu.kda_decode_step(t["q"], t["k"], t["v"], t["g"], t["beta"], pd["state_indices"].to(DEV),
+                            pool, out, gate=t["gate"], norm_w=pd["norm_w"].to(DEV), eps=pd["eps"],
+                            gate_act=act)
+    torch.cuda.synchronize()
+    y_ref, p_ref = oracle.decode(sd["q"], sd["k"], sd["v"], sd["g"], sd["beta"], pd["state_indices"],
+                                 pd["pool"], gate=sd["gate"], norm_w=pd["norm_w"], eps=pd["eps"],
+                                 gate_act=act)
+    assert excess_error(out, y_ref) <= 0.01
+    assert excess_error(pool, p_ref) <= 0.01
+
+
 @pytest.mark.parametrize("d", [16, 64, 128])
 @pytest.mark.parametrize("in_dtype,state_dtype", [(torch.float32, torch.float32),
                                                   (torch.bfloat16, torch.bfloat16),
@@ -241,15 +276,16 @@ def test_decode_small(kda_gpu, d, in_dtype, state_dtype):
 @pytest.mark.parametrize("dv", [16, 64, 128])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("inplace", [False, True])
-def test_norm_gate(kda_gpu, dv, dtype, inplace):
+@pytest.mark.parametrize("act", ["sigmoid", "silu"])
+def test_norm_gate(kda_gpu, dv, dtype, inplace, act):
     gen = torch.Generator().manual_seed(dv)
     o = torch.randn(37, 5, dv, generator=gen).to(dtype)
     gate = torch.randn(37, 5, dv, generator=gen).to(dtype)
     w = (1 + 0.02 * torch.randn(dv, generator=gen)).to(dtype)
-    ref = oracle.norm_gate(o, gate, w, eps=1e-6)
+    ref = oracle.norm_gate(o, gate, w, eps=1e-6, gate_act=act)
     od, gd, wd = o.to(DEV), gate.to(DEV), w.to(DEV)
     y = od if inplace else torch.empty_like(od)
-    kda_gpu.kda_norm_gate(od, gd, wd, y, eps=1e-6)
+    kda_gpu.kda_norm_gate(od, gd, wd, y, eps=1e-6, gate_act=act)
     torch.cuda.synchronize()
     assert excess_error(y, ref) <= 1e-5 if dtype == torch.float32 else excess_error(y, ref) <= 1e-2
     if not inplace:

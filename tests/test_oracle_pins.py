@@ -357,3 +357,33 @@ def test_pins_catch_planted_mistakes():
     np.testing.assert_allclose(out[:, 0], o_ref, atol=1e-12)
     for mode in ("read_before_write", "decay_after_residual", "no_beta_write"):
         assert np.max(np.abs(variant(mode) - o_ref)) > 1e-3, mode
+
+
+def test_hand_worked_norm_gate_silu():
+    gd = _read_golden("norm_gate_silu_example.txt")
+    y = oracle.norm_gate(gd["o"][None], gd["gate"][None], gd["w"], eps=gd["eps"][0],
+                         gate_act="silu")
+    np.testing.assert_allclose(y[0], gd["y"], atol=1e-12)
+
+
+def test_no_initial_state_starts_from_zero():
+    """A sequence flagged without initial state computes exactly what the same
+    sequence computes from a zeroed slot, whatever the slot held; flagged-with
+    sequences are unaffected, and the final state still lands in the slot."""
+    rng = np.random.default_rng(13)
+    lens = [9, 14, 5]
+    T, H, dk, dv = sum(lens), 2, 4, 3
+    q, k, v, g, beta = _rand_inputs(rng, T, H, dk, dv)
+    pool = rng.standard_normal((5, H, dk, dv))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    idx = np.array([4, 0, 2], np.int32)
+    flags = np.array([1, 0, 1], np.int32)
+    out, pool_a, _, _ = oracle.prefill(q, k, v, g, beta, cu, idx, pool, has_initial_state=flags)
+    zeroed = pool.copy()
+    zeroed[0] = 0.0
+    out_z, pool_z, _, _ = oracle.prefill(q, k, v, g, beta, cu, idx, zeroed)
+    np.testing.assert_allclose(out, out_z, atol=1e-14)
+    np.testing.assert_allclose(pool_a, pool_z, atol=1e-14)
+    out_all, _, _, _ = oracle.prefill(q, k, v, g, beta, cu, idx, pool)
+    np.testing.assert_allclose(out[:9], out_all[:9], atol=1e-14)
+    assert np.max(np.abs(out[9:23] - out_all[9:23])) > 1e-6  # the flag did change seq 1

@@ -62,6 +62,6 @@ def test_static_scratch_rejects_oversize(kda_gpu):
     fake = 1 << 20  # never dereferenced: the size check comes first
     # 65536 tokens x 32 heads needs ~2.4 GB of scratch, far above the array
     rc = lib.kda_prefill_chunked_static_scratch(
-        fake, fake, fake, fake, fake, 1, fake, 1, 65536, fake, fake, 4, 0, fake, None, 0, 0, None,
-        None, None, 1e-6, 32, 128, 128, 64, 0.0, None, None)
+        fake, fake, fake, fake, fake, 1, fake, 1, 65536, fake, None, fake, 4, 0, fake, None, 0, 0,
+        None, None, None, 1e-6, 0, 32, 128, 128, 64, 0.0, None, None)
     assert rc == -3  # KDA_ERR_WORKSPACE
