@@ -6,11 +6,13 @@ Workloads (seeded synthetic inputs, no dataset):
            chunk 64, checkpoints every 256 tokens, fused RMSNorm-gate.
   decode   256 sequences x 1 token, H=32, dk=dv=128, bf16 inputs, fp32
            1024-slot pool, fused RMSNorm-gate.
-A step is one prefill call followed by one decode step; each is timed in its
-own loop with CUDA events on the launching stream, the L2 flushed (a 256 MiB
+  spec     the decode batch verifying 4 draft tokens per sequence (per-token
+           states kept) followed by the commit of the accepted prefixes.
+A step is one prefill call, one decode step and one verify + commit; each is
+timed in its own loop with CUDA events on the launching stream, the L2 flushed (a 256 MiB
 write) before every timed prefill call (the decode step streams 1.07 GB, far
-above L2).  ``value`` is prefill tokens/s; the decode figures sit under
-``decode``.  ``--impl reference`` times the fp64 CPU oracle on the same
+above L2).  ``value`` is prefill tokens/s; the decode and verification
+figures sit under ``decode`` and ``spec_decode``.  ``--impl reference`` times the fp64 CPU oracle on the same
 workload instead.  Under torchrun each rank runs an independent replica (the
 path has no exchange step) and rank 0 reports the aggregate.
 """
@@ -196,6 +198,22 @@ def decode_algorithmic(w):
     return int(b), float(fl)
 
 
+def spec_algorithmic(w, K, num_accepted):
+    """Bytes of one verification call (K tokens per sequence, per-token states
+    stored) plus the commit of the accepted states."""
+    ib = 2 if w.in_dtype == torch.bfloat16 else 4
+    sb = 2 if w.state_dtype == torch.bfloat16 else 4
+    st = w.H * w.dk * w.dv * sb
+    b = w.N * st                                         # pool state read
+    b += w.N * K * st                                    # per-token states written
+    b += w.N * K * w.H * (3 * w.dk + w.dv + 1 + w.dv) * ib  # q k g v beta out
+    if w.gate:
+        b += w.N * K * w.H * w.dv * ib + w.dv * ib
+    b += 2 * int((num_accepted > 0).sum()) * st          # commit: read + write
+    b += w.N * 8
+    return int(b)
+
+
 # ----------------------------------------------------------------- GPU arm
 def run_gpu(args):
     import linear_attention_prefill_kda_gb300 as kda
@@ -235,6 +253,27 @@ def run_gpu(args):
     dw = W.DECODE
     with_decode = args.workload in ("both", "decode")
     with_prefill = args.workload in ("both", "prefill")
+    with_spec = args.workload in ("both", "spec")
+    SPEC_K = 4
+    if with_spec:
+        sp = W.make_decode_pool(dw)
+        spool = sp["pool"].to(dev)
+        sidx = sp["state_indices"].to(dev)
+        snw = sp["norm_w"].to(dev)
+        sdraft = W.make_decode_draft(dw, SPEC_K)
+        sacc_host = sdraft.pop("num_accepted")
+        sdr = {k: v.to(dev) for k, v in sdraft.items()}
+        sacc = sacc_host.to(dev)
+        sout = torch.empty(dw.N, SPEC_K, dw.H, dw.dv, device=dev, dtype=dw.in_dtype)
+        sts = torch.empty(dw.N, SPEC_K, dw.H, dw.dk, dw.dv, device=dev, dtype=dw.state_dtype)
+
+    def spec_call():
+        if not with_spec:
+            return
+        kda.kda_decode_multi(sdr["q"], sdr["k"], sdr["v"], sdr["g"], sdr["beta"], sidx, spool,
+                             sout, sts, gate=sdr["gate"], norm_w=snw, eps=sp["eps"],
+                             dev_status=status, stream=stream)
+        kda.kda_commit_accepted(sts, sacc, sidx, spool, dev_status=status, stream=stream)
     if with_decode:
         pd = W.make_decode_pool(dw)
         dpool = pd["pool"].to(dev)
@@ -261,6 +300,7 @@ def run_gpu(args):
         if with_prefill:
             prefill_call()
         decode_call(0)
+        spec_call()
     barrier()
 
     with ClockSampler(local) as clk:
@@ -284,6 +324,15 @@ def run_gpu(args):
         e1.record(stream)
         barrier()
         dec_ms_total = e0.elapsed_time(e1)
+        # speculative verification: K=4 draft tokens per sequence + commit
+        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        e2.record(stream)
+        for i in range(args.steps if with_spec else 0):
+            spec_call()
+        e3.record(stream)
+        barrier()
+        spec_ms_total = e2.elapsed_time(e3)
     clocks = clk.summary()
     st = int(status.item())
     if st != 0:
@@ -291,7 +340,8 @@ def run_gpu(args):
 
     pre_ms_mean = sum(pre_ms) / len(pre_ms)
     dec_ms = dec_ms_total / args.steps
-    pre_ms_mean, dec_ms = max_over_ranks([pre_ms_mean, dec_ms], dev)
+    spec_ms = spec_ms_total / args.steps if with_spec else float("nan")
+    pre_ms_mean, dec_ms, spec_ms = max_over_ranks([pre_ms_mean, dec_ms, spec_ms], dev)
 
     # ---------------- e2e through the public API with host buffers
     names = ["q", "k", "v", "g", "beta", "gate"]
@@ -330,6 +380,8 @@ def run_gpu(args):
     pre_gbs = rate(pre_bytes, pre_ms_mean) / 1e9
     dec_gbs = rate(dec_bytes, dec_ms) / 1e9
     pre_tflops = rate(pre_flops, pre_ms_mean) / 1e12
+    spec_bytes = spec_algorithmic(dw, SPEC_K, sacc_host) if with_spec else 0
+    spec_gbs = rate(spec_bytes, spec_ms) / 1e9
     tokens_s = replica_rate(T, ws, pre_ms_mean)
     seqsteps_s = replica_rate(dw.N, ws, dec_ms)
     result = {
@@ -366,9 +418,18 @@ def run_gpu(args):
                                 "unit": "GB/s", "frac": round(dec_gbs / pk["hbm"], 4),
                                 "traffic": recorded_traffic("decode_step_dram_bytes"),
                                 "algorithmic_bytes": dec_bytes}},
+        "spec_decode": {"value": round(replica_rate(dw.N * SPEC_K, ws, spec_ms), 1),
+                        "unit": "draft tokens verified/s", "draft_tokens": SPEC_K,
+                        "ms_per_step": round(spec_ms, 4),
+                        "roofline": {"bound": "hbm", "achieved": round(spec_gbs, 1),
+                                     "peak": pk["hbm"], "unit": "GB/s",
+                                     "frac": round(spec_gbs / pk["hbm"], 4),
+                                     "traffic": recorded_traffic("spec_step_dram_bytes"),
+                                     "algorithmic_bytes": spec_bytes}},
         "e2e": {"value": round(replica_rate(T, ws, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (prefill_launches(kda, w) * with_prefill + with_decode),
+        "gpu_launches": args.steps * (prefill_launches(kda, w) * with_prefill + with_decode
+                                      + 2 * with_spec),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -472,8 +533,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["libkda", "reference"], default="libkda")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["both", "prefill", "decode"], default="both",
-                    help="time both parts (default) or one of them (for profiling runs)")
+    ap.add_argument("--workload", choices=["both", "prefill", "decode", "spec"], default="both",
+                    help="time every part (default) or one of them (for profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -156,6 +156,47 @@ KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, 
                            int32_t* dev_status, void* stream);
 
 /*
+ * K recurrent decode steps per sequence, for verifying K speculative tokens
+ * ("[Feature][KDA] Add Kimi K3 KDA execution", section "Metadata
+ * construction": speculative decode is its own batch kind; the FlashKDA page,
+ * risk section: state recovery inside speculative decoding).  Sequence i runs
+ * tokens t = 0..K-1 through the decode step of kda_decode_step, starting from
+ * state_pool[state_indices[i]], and the state after token t is stored to
+ * token_states[i, t] so that the state after any accepted prefix can be
+ * committed afterwards (kda_commit_accepted).
+ *  q, k, g      [N, K, H, dk] in_dtype (token t of sequence i at row i*K + t).
+ *  v, out, gate [N, K, H, dv]; beta [N, K, H].
+ *  state_indices int32 [N] (device); -1 = padding (its K output rows are zeroed,
+ *               its token_states left untouched); out of range -> KDA_DEV_BAD_INDEX.
+ *  token_states [N, K, H, dk, dv] state_dtype (device, 16-byte aligned), or
+ *               NULL to keep no per-token states.
+ *  write_back   nonzero: the state after token K-1 is also written to the slot
+ *               (every token accepted); zero: the pool is only read.
+ * Other arguments as for kda_decode_step.  The state is carried in fp32 across
+ * the K tokens and rounded to state_dtype only at the stores.
+ */
+KDA_API kda_status kda_decode_multi(const void* q, const void* k, const void* v, const void* g,
+                            const void* beta, kda_dtype in_dtype, const int32_t* state_indices,
+                            int N, int K, void* state_pool, int64_t num_slots,
+                            kda_dtype state_dtype, void* out, void* token_states, int write_back,
+                            const void* gate, const void* norm_w, float eps,
+                            kda_gate_act gate_act, int H, int dk, int dv, float scale,
+                            int32_t* dev_status, void* stream);
+
+/*
+ * Commit the verified prefix of a kda_decode_multi call: for each sequence i
+ * with a_i = num_accepted[i] >= 1, state_pool[state_indices[i]] =
+ * token_states[i, a_i - 1]; a_i == 0 or a padding index (-1) leaves the slot
+ * unchanged.  num_accepted int32 [N] (device); a_i outside [0, K] or an index
+ * out of range latches KDA_DEV_BAD_INDEX and skips the sequence.  token_states
+ * as written by kda_decode_multi with the same N, K, H, dk, dv, state_dtype.
+ */
+KDA_API kda_status kda_commit_accepted(const void* token_states, const int32_t* num_accepted,
+                               const int32_t* state_indices, int N, int K, void* state_pool,
+                               int64_t num_slots, kda_dtype state_dtype, int H, int dk, int dv,
+                               int32_t* dev_status, void* stream);
+
+/*
  * Standalone output RMSNorm-gate ("[Feature][KDA] ...", first section:
  * FusedRMSNormGated output normalisation and gating):
  *     y = o / sqrt(mean_dv(o^2) + eps) * w * act(gate),  act = sigmoid or SiLU

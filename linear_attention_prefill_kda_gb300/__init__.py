@@ -18,7 +18,8 @@ __all__ = [
     "load", "lib_path", "KdaError", "KDA_OK", "KDA_F32", "KDA_BF16",
     "kda_prefill_chunked", "kda_prefill_workspace_bytes", "kda_decode_step", "kda_norm_gate",
     "kda_status_string", "kda_version", "DEV_STATUS", "prefill_launches",
-    "kda_prefill_chunked_static_scratch", "STATIC_SCRATCH_BYTES",
+    "kda_prefill_chunked_static_scratch", "STATIC_SCRATCH_BYTES", "kda_decode_multi",
+    "kda_commit_accepted",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -44,6 +45,13 @@ _SIGNATURES = {
     "kda_decode_step": (ctypes.c_int, [
         _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _P, _I64, ctypes.c_int, _P, _P, _P,
         _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _F32, _P, _P]),
+    "kda_decode_multi": (ctypes.c_int, [
+        _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, ctypes.c_int, _P, _I64, ctypes.c_int,
+        _P, _P, ctypes.c_int, _P, _P, _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        _F32, _P, _P]),
+    "kda_commit_accepted": (ctypes.c_int, [
+        _P, _P, _P, ctypes.c_int, ctypes.c_int, _P, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, _P, _P]),
     "kda_norm_gate": (ctypes.c_int, [_P, _P, _P, _F32, ctypes.c_int, _P, _I64, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int, _P]),
     "kda_prefill_chunked_static_scratch": (ctypes.c_int, [
@@ -183,6 +191,34 @@ def kda_decode_step(q, k, v, g, beta, state_indices, state_pool, out, *, gate=No
         _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk, dv, float(scale), _ptr(dev_status),
         _stream(stream))
     _check(st, "kda_decode_step")
+
+
+def kda_decode_multi(q, k, v, g, beta, state_indices, state_pool, out, token_states=None, *,
+                     write_back: bool = False, gate=None, norm_w=None, eps: float = 1e-6,
+                     gate_act: str = "sigmoid", scale: float = 0.0, dev_status=None, stream=None):
+    """K decode steps per sequence with per-token states (see ``include/kda.h``).
+
+    q, k, g are [N, K, H, dk]; v, out, gate [N, K, H, dv]; beta [N, K, H];
+    token_states [N, K, H, dk, dv] or None.
+    """
+    N, K, H, dk = q.shape
+    dv = v.shape[-1]
+    st = load().kda_decode_multi(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(state_indices), N, K,
+        _ptr(state_pool), state_pool.shape[0], _dtype(state_pool), _ptr(out), _ptr(token_states),
+        int(bool(write_back)), _ptr(gate), _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk,
+        dv, float(scale), _ptr(dev_status), _stream(stream))
+    _check(st, "kda_decode_multi")
+
+
+def kda_commit_accepted(token_states, num_accepted, state_indices, state_pool, *,
+                        dev_status=None, stream=None):
+    """state_pool[idx_i] = token_states[i, a_i - 1] where a_i >= 1 (see ``include/kda.h``)."""
+    N, K, H, dk, dv = token_states.shape
+    st = load().kda_commit_accepted(
+        _ptr(token_states), _ptr(num_accepted), _ptr(state_indices), N, K, _ptr(state_pool),
+        state_pool.shape[0], _dtype(state_pool), H, dk, dv, _ptr(dev_status), _stream(stream))
+    _check(st, "kda_commit_accepted")
 
 
 def kda_norm_gate(o, gate, w, y, *, eps: float = 1e-6, gate_act: str = "sigmoid", stream=None):

@@ -25,7 +25,7 @@ kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR
 
 extern "C" {
 
-int kda_version(void) { return 101; }
+int kda_version(void) { return 102; }
 
 const char* kda_status_string(kda_status s) {
   switch (s) {
@@ -138,6 +138,68 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const vo
   p.in_dtype = in_dtype; p.state_dtype = state_dtype;
   p.gate_act = gate_act;
   return from_cuda(kda::launch_decode(p, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_decode_multi(const void* q, const void* k, const void* v, const void* g,
+                            const void* beta, kda_dtype in_dtype, const int32_t* state_indices,
+                            int N, int K, void* state_pool, int64_t num_slots,
+                            kda_dtype state_dtype, void* out, void* token_states, int write_back,
+                            const void* gate, const void* norm_w, float eps,
+                            kda_gate_act gate_act, int H, int dk, int dv, float scale,
+                            int32_t* dev_status, void* stream) {
+  if (N < 0 || K < 0 || H <= 0 || num_slots <= 0) return KDA_ERR_INVALID_ARG;
+  if ((int64_t)N * H > INT32_MAX || (int64_t)N * K > INT32_MAX) return KDA_ERR_INVALID_ARG;
+  if (!dtype_ok(in_dtype) || !dtype_ok(state_dtype)) return KDA_ERR_UNSUPPORTED;
+  if (!dim_ok(dk) || dv != dk) return KDA_ERR_UNSUPPORTED;
+  if (N == 0 || K == 0) return KDA_OK;
+  if (!ptr_ok(q, true) || !ptr_ok(k, true) || !ptr_ok(v, true) || !ptr_ok(g, true) ||
+      !ptr_ok(beta, true) || !ptr_ok(out, true) || !ptr_ok(state_indices, true) ||
+      !ptr_ok(state_pool, true) || !ptr_ok(token_states, false) || !ptr_ok(dev_status, false))
+    return KDA_ERR_INVALID_ARG;
+  if ((gate == nullptr) != (norm_w == nullptr)) return KDA_ERR_INVALID_ARG;
+  if (!ptr_ok(gate, false) || !ptr_ok(norm_w, false)) return KDA_ERR_INVALID_ARG;
+  if (gate && !(eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+  if (!act_ok(gate_act)) return KDA_ERR_INVALID_ARG;
+  kda::DecodeMultiParams p{};
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+  p.state_indices = state_indices;
+  p.state_pool = state_pool;
+  p.out = out;
+  p.token_states = token_states;
+  p.gate = gate; p.norm_w = norm_w;
+  p.dev_status = dev_status;
+  p.num_slots = num_slots;
+  p.N = N; p.K = K; p.H = H; p.dk = dk; p.dv = dv;
+  p.write_back = write_back != 0;
+  p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)dk);
+  p.eps = eps;
+  p.in_dtype = in_dtype; p.state_dtype = state_dtype;
+  p.gate_act = gate_act;
+  return from_cuda(kda::launch_decode_multi(p, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_commit_accepted(const void* token_states, const int32_t* num_accepted,
+                               const int32_t* state_indices, int N, int K, void* state_pool,
+                               int64_t num_slots, kda_dtype state_dtype, int H, int dk, int dv,
+                               int32_t* dev_status, void* stream) {
+  if (N < 0 || K < 0 || H <= 0 || num_slots <= 0) return KDA_ERR_INVALID_ARG;
+  if ((int64_t)N * H > INT32_MAX || (int64_t)N * K > INT32_MAX) return KDA_ERR_INVALID_ARG;
+  if (!dtype_ok(state_dtype)) return KDA_ERR_UNSUPPORTED;
+  if (!dim_ok(dk) || dv != dk) return KDA_ERR_UNSUPPORTED;
+  if (N == 0 || K == 0) return KDA_OK;
+  if (!ptr_ok(token_states, true) || !ptr_ok(num_accepted, true) || !ptr_ok(state_indices, true) ||
+      !ptr_ok(state_pool, true) || !ptr_ok(dev_status, false))
+    return KDA_ERR_INVALID_ARG;
+  kda::CommitParams p{};
+  p.token_states = token_states;
+  p.num_accepted = num_accepted;
+  p.state_indices = state_indices;
+  p.state_pool = state_pool;
+  p.dev_status = dev_status;
+  p.num_slots = num_slots;
+  p.N = N; p.K = K; p.H = H; p.dk = dk; p.dv = dv;
+  p.state_dtype = state_dtype;
+  return from_cuda(kda::launch_commit(p, static_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_norm_gate(const void* o, const void* gate, const void* w, float eps,

@@ -24,6 +24,33 @@ struct DecodeParams {
   int gate_act;  // kda_gate_act
 };
 
+struct DecodeMultiParams {
+  const void *q, *k, *v, *g, *beta;  // [N*K, H, *] token-major
+  const int32_t* state_indices;
+  void* state_pool;
+  void* out;            // [N*K, H, dv]
+  void* token_states;   // [N*K, H, dk, dv] state dtype
+  const void *gate, *norm_w;
+  int32_t* dev_status;
+  int64_t num_slots;
+  int N, K, H, dk, dv;
+  int write_back;
+  float scale, eps;
+  kda_dtype in_dtype, state_dtype;
+  int gate_act;
+};
+
+struct CommitParams {
+  const void* token_states;
+  const int32_t* num_accepted;
+  const int32_t* state_indices;
+  void* state_pool;
+  int32_t* dev_status;
+  int64_t num_slots;
+  int N, K, H, dk, dv;
+  kda_dtype state_dtype;
+};
+
 struct NormGateParams {
   const void *o, *gate, *w;
   void* y;
@@ -62,6 +89,8 @@ struct PrefillParams {
 cudaError_t set_smem_once(const void* kernel, int bytes);
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_multi(const DecodeMultiParams& p, cudaStream_t stream);
+cudaError_t launch_commit(const CommitParams& p, cudaStream_t stream);
 cudaError_t launch_norm_gate(const NormGateParams& p, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
 // Upper bound over every option (what kda_prefill_workspace_bytes reports).

@@ -169,6 +169,45 @@ def decode(q, k, v, g, beta, state_indices, pool, *, gate=None, norm_w=None, eps
     return out, pool
 
 
+def decode_multi(q, k, v, g, beta, state_indices, pool, *, gate=None, norm_w=None, eps=1e-6,
+                 scale=None, nthreads=0, gate_act="sigmoid"):
+    """K recurrent decode steps per sequence, keeping the state after each token
+    (speculative-decoding verification: "[Feature][KDA] Add Kimi K3 KDA
+    execution", section "Metadata construction", and the FlashKDA summary's
+    risk section).  Each step is :func:`decode` on the pool left by the previous
+    one.  q,k,g [N,K,H,dk]; v, gate [N,K,H,dv]; beta [N,K,H].
+
+    Returns ``(out [N,K,H,dv], token_states [N,K,H,dk,dv], pool_after_K)``;
+    token_states rows of padding sequences (index -1) are NaN.
+    """
+    q, k, v, g, beta, gate = (_f64(x) for x in (q, k, v, g, beta, gate))
+    N, K, H, dk = q.shape
+    dv = v.shape[-1]
+    idx = _i32(state_indices)
+    cur = _f64(pool).copy()
+    out = np.zeros((N, K, H, dv), np.float64)
+    states = np.full((N, K, H, dk, dv), np.nan)
+    live = idx >= 0
+    for t in range(K):
+        out[:, t], cur = decode(q[:, t], k[:, t], v[:, t], g[:, t], beta[:, t], idx, cur,
+                                gate=None if gate is None else gate[:, t],
+                                norm_w=norm_w, eps=eps, scale=scale, nthreads=nthreads,
+                                gate_act=gate_act)
+        states[live, t] = cur[idx[live]]
+    return out, states, cur
+
+
+def commit_accepted(token_states, num_accepted, state_indices, pool):
+    """pool[idx_i] = token_states[i, a_i - 1] for a_i = num_accepted[i] >= 1;
+    a_i == 0 or idx_i == -1 leaves the slot unchanged."""
+    pool = _f64(pool).copy()
+    token_states = _f64(token_states)
+    for i, (slot, a) in enumerate(zip(_i32(state_indices), _i32(num_accepted))):
+        if slot >= 0 and a >= 1:
+            pool[slot] = token_states[i, a - 1]
+    return pool
+
+
 def norm_gate(o, gate, w, eps=1e-6, gate_act="sigmoid"):
     """y = o / sqrt(mean(o^2)+eps) * w * act(gate) over the last dimension."""
     o, gate, w = _f64(o), _f64(gate), _f64(w)

@@ -92,9 +92,49 @@ def test_decode_rejects(lib, over, expect):
     assert _decode(lib, **over) == expect
 
 
+def _decode_multi(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, in_dtype=1, idx=FAKE, N=4, K=3, pool=FAKE,
+             slots=8, sdt=0, out=FAKE, ts=FAKE, wb=0, gate=None, w=None, eps=1e-6, act=0, H=2,
+             dk=128, dv=128, scale=0.0, st=None)
+    a.update(over)
+    return lib.kda_decode_multi(a["q"], a["k"], a["v"], a["g"], a["beta"], a["in_dtype"],
+                                a["idx"], a["N"], a["K"], a["pool"], a["slots"], a["sdt"],
+                                a["out"], a["ts"], a["wb"], a["gate"], a["w"], a["eps"], a["act"],
+                                a["H"], a["dk"], a["dv"], a["scale"], a["st"], None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dk=64), -2), (dict(in_dtype=3), -2), (dict(sdt=4), -2), (dict(N=-1), -1),
+    (dict(K=-1), -1), (dict(H=0), -1), (dict(slots=0), -1), (dict(idx=None), -1),
+    (dict(ts=MIS), -1), (dict(q=MIS), -1), (dict(gate=FAKE), -1), (dict(act=3), -1),
+    (dict(N=1 << 20, K=1 << 12), -1),
+])
+def test_decode_multi_rejects(lib, over, expect):
+    assert _decode_multi(lib, **over) == expect
+
+
+def _commit(lib, **over):
+    a = dict(ts=FAKE, acc=FAKE, idx=FAKE, N=4, K=3, pool=FAKE, slots=8, sdt=0, H=2, dk=64, dv=64,
+             st=None)
+    a.update(over)
+    return lib.kda_commit_accepted(a["ts"], a["acc"], a["idx"], a["N"], a["K"], a["pool"],
+                                   a["slots"], a["sdt"], a["H"], a["dk"], a["dv"], a["st"], None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dv=128), -2), (dict(sdt=2), -2), (dict(N=-1), -1), (dict(slots=0), -1),
+    (dict(ts=None), -1), (dict(acc=None), -1), (dict(pool=MIS), -1), (dict(st=MIS), -1),
+])
+def test_commit_rejects(lib, over, expect):
+    assert _commit(lib, **over) == expect
+
+
 def test_empty_calls_are_noops(lib):
     assert _decode(lib, N=0, q=None, k=None, v=None, g=None, beta=None, idx=None, out=None) == 0
     assert lib.kda_norm_gate(FAKE, FAKE, FAKE, 1e-6, 0, FAKE, 0, 4, 128, 1, None) == 0
+    assert _decode_multi(lib, K=0, q=None, ts=None) == 0
+    assert _decode_multi(lib, N=0, idx=None, out=None) == 0
+    assert _commit(lib, N=0, ts=None, acc=None) == 0
 
 
 @pytest.mark.parametrize("args,expect", [

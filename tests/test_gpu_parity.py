@@ -273,6 +273,95 @@ def test_decode_small(kda_gpu, d, in_dtype, state_dtype):
         assert excess_error(pool, p_ref) <= tol
 
 
+@pytest.mark.parametrize("d", [16, 64, 128])
+@pytest.mark.parametrize("K", [1, 5])
+@pytest.mark.parametrize("in_dtype,state_dtype", [(torch.float32, torch.float32),
+                                                  (torch.bfloat16, torch.bfloat16),
+                                                  (torch.bfloat16, torch.float32)])
+def test_decode_multi_and_commit(kda_gpu, d, K, in_dtype, state_dtype):
+    """K draft tokens per sequence: outputs and every per-token state against
+    the oracle, the pool untouched by the verification call, then the commit
+    of the accepted prefixes; a second call with write_back leaves the
+    K-token state in the slots."""
+    w = W.DECODE.replace(N=7, H=3, dk=d, dv=d, in_dtype=in_dtype,
+                         state_dtype=state_dtype, num_slots=12, seed=900 + d + K)
+    pd = W.make_decode_pool(w)
+    dd = W.make_decode_draft(w, K)
+    idx = torch.tensor([3, -1, 11, 0, 7, 5, 9], dtype=torch.int32)
+    acc = dd["num_accepted"]
+    t = to_dev(dd, DEV)
+    nw = pd["norm_w"].to(DEV)
+    pool = pd["pool"].to(DEV)
+    out = torch.full((w.N, K, w.H, w.dv), float("nan"), device=DEV, dtype=in_dtype)
+    ts = torch.full((w.N, K, w.H, w.dk, w.dv), float("nan"), device=DEV, dtype=state_dtype)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda_gpu.kda_decode_multi(t["q"], t["k"], t["v"], t["g"], t["beta"], idx.to(DEV), pool, out, ts,
+                             gate=t["gate"], norm_w=nw, eps=pd["eps"], gate_act="silu",
+                             dev_status=status)
+    torch.cuda.synchronize()
+    y_ref, ts_ref, pool_k = oracle.decode_multi(
+        dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], idx, pd["pool"], gate=dd["gate"],
+        norm_w=pd["norm_w"], eps=pd["eps"], gate_act="silu")
+    tol = tol_for(state_dtype)
+    live = (idx >= 0).numpy()
+    assert int(status.item()) == 0
+    assert excess_error(out, y_ref) <= tol
+    assert torch.count_nonzero(out[1].float()).item() == 0
+    assert excess_error(ts[torch.from_numpy(live).to(DEV)], ts_ref[live]) <= tol
+    assert torch.isnan(ts[1].float()).all()  # padding rows keep no states
+    assert torch.equal(pool.cpu(), pd["pool"])  # verification only reads the pool
+    kda_gpu.kda_commit_accepted(ts, acc.to(DEV), idx.to(DEV), pool, dev_status=status)
+    torch.cuda.synchronize()
+    ref_commit = oracle.commit_accepted(ts_ref, acc.numpy(), idx.numpy(), pd["pool"])
+    assert int(status.item()) == 0
+    assert excess_error(pool, ref_commit) <= tol
+    for i in range(w.N):  # slots with nothing accepted stay bit-identical
+        if idx[i] >= 0 and acc[i] == 0:
+            assert torch.equal(pool[idx[i]].cpu(), pd["pool"][idx[i]])
+    pool2 = pd["pool"].to(DEV)
+    kda_gpu.kda_decode_multi(t["q"], t["k"], t["v"], t["g"], t["beta"], idx.to(DEV), pool2, out,
+                             None, write_back=True, gate=t["gate"], norm_w=nw, eps=pd["eps"],
+                             gate_act="silu", dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert excess_error(pool2, pool_k) <= tol
+    assert excess_error(out, y_ref) <= tol
+
+
+def test_decode_multi_full_width(kda_gpu):
+    """256 sequences x 4 draft tokens at 32 heads, d = 128 (the decode batch);
+    the oracle follows 16 sampled sequences."""
+    w, K = W.DECODE, 4
+    pd = W.make_decode_pool(w)
+    dd = W.make_decode_draft(w, K)
+    idx = pd["state_indices"]
+    t = to_dev(dd, DEV)
+    pool = pd["pool"].to(DEV)
+    out = torch.empty(w.N, K, w.H, w.dv, device=DEV, dtype=w.in_dtype)
+    ts = torch.empty(w.N, K, w.H, w.dk, w.dv, device=DEV, dtype=w.state_dtype)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda_gpu.kda_decode_multi(t["q"], t["k"], t["v"], t["g"], t["beta"], idx.to(DEV), pool, out, ts,
+                             gate=t["gate"], norm_w=pd["norm_w"].to(DEV), eps=pd["eps"],
+                             dev_status=status)
+    kda_gpu.kda_commit_accepted(ts, dd["num_accepted"].to(DEV), idx.to(DEV), pool,
+                                dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sample = list(range(0, w.N, w.N // 16))
+    sidx = idx[sample]
+    sub_pool = pd["pool"][sidx.long()]
+    ref_idx = np.arange(len(sample), dtype=np.int32)
+    y_ref, ts_ref, _ = oracle.decode_multi(
+        *(dd[n][sample] for n in ("q", "k", "v", "g", "beta")), ref_idx, sub_pool,
+        gate=dd["gate"][sample], norm_w=pd["norm_w"], eps=pd["eps"])
+    tol = tol_for(w.state_dtype)
+    assert excess_error(out[sample], y_ref) <= tol
+    assert excess_error(ts[sample], ts_ref) <= tol
+    ref_commit = oracle.commit_accepted(ts_ref, dd["num_accepted"][sample].numpy(), ref_idx,
+                                        sub_pool)
+    assert excess_error(pool[sidx.long().to(DEV)], ref_commit) <= tol
+
+
 @pytest.mark.parametrize("dv", [16, 64, 128])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("inplace", [False, True])

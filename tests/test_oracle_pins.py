@@ -387,3 +387,43 @@ def test_no_initial_state_starts_from_zero():
     out_all, _, _, _ = oracle.prefill(q, k, v, g, beta, cu, idx, pool)
     np.testing.assert_allclose(out[:9], out_all[:9], atol=1e-14)
     assert np.max(np.abs(out[9:23] - out_all[9:23])) > 1e-6  # the flag did change seq 1
+
+
+def test_multi_token_decode_equals_prefill_with_per_token_checkpoints():
+    """K decode steps per sequence are the prefill of those K tokens: the
+    outputs agree, and the state after token t is the prefill's checkpoint
+    t when a checkpoint is taken after every token.  Committing a_i accepted
+    tokens leaves the slot at checkpoint a_i - 1 (unchanged for a_i = 0)."""
+    rng = np.random.default_rng(21)
+    N, K, H, dk, dv = 4, 5, 2, 6, 4
+    q, k, v, g, beta = _rand_inputs(rng, N * K, H, dk, dv)
+    gate = rng.standard_normal((N * K, H, dv))
+    w = 1 + 0.1 * rng.standard_normal(dv)
+    pool = rng.standard_normal((7, H, dk, dv))
+    idx = np.array([3, -1, 0, 6], np.int32)
+    sh = lambda x: x.reshape((N, K) + x.shape[1:])
+    out, ts, pool_k = oracle.decode_multi(sh(q), sh(k), sh(v), sh(g), sh(beta), idx, pool,
+                                          gate=sh(gate), norm_w=w, gate_act="silu")
+    live = [i for i in range(N) if idx[i] >= 0]
+    cu = np.arange(len(live) + 1, dtype=np.int32) * K
+    rows = np.concatenate([np.arange(i * K, (i + 1) * K) for i in live])
+    o_p, pool_p, ck, _ = oracle.prefill(q[rows], k[rows], v[rows], g[rows], beta[rows], cu,
+                                        idx[live], pool, checkpoint_every=1, gate=gate[rows],
+                                        norm_w=w, gate_act="silu")
+    np.testing.assert_allclose(out[live].reshape(-1, H, dv), o_p, atol=1e-12)
+    np.testing.assert_allclose(ts[live].reshape(-1, H, dk, dv), ck, atol=1e-12)
+    np.testing.assert_allclose(pool_k, pool_p, atol=1e-12)
+    assert np.all(out[1] == 0) and np.all(np.isnan(ts[1]))
+    acc = np.array([2, 3, 0, K], np.int32)
+    committed = oracle.commit_accepted(ts, acc, idx, pool)
+    np.testing.assert_allclose(committed[3], ck[1], atol=1e-12)
+    np.testing.assert_array_equal(committed[0], pool[0])
+    np.testing.assert_allclose(committed[6], pool_p[6], atol=1e-12)
+    untouched = [s for s in range(7) if s not in (3, 0, 6)]
+    np.testing.assert_array_equal(committed[untouched], pool[untouched])
+    # one step of the expanded transition pins token 0 independently of both routines
+    S = pool[3, 1]
+    i0 = 0
+    Sn = (np.eye(dk) - beta[i0, 1] * np.outer(k[i0, 1], k[i0, 1])) @ (
+        np.exp(g[i0, 1])[:, None] * S) + beta[i0, 1] * np.outer(k[i0, 1], v[i0, 1])
+    np.testing.assert_allclose(ts[0, 0, 1], Sn, atol=1e-12)

@@ -191,3 +191,16 @@ def make_decode_step(w: DecodeWorkload, step: int, seed=None):
     base = w.seed if seed is None else seed
     gen = torch.Generator().manual_seed(int(base) * 1_000_003 + 7919 * (step + 1))
     return _token_inputs(gen, w.N, w.H, w.dk, w.dv, w.in_dtype, w.gate)
+
+
+
+def make_decode_draft(w: DecodeWorkload, K: int, seed=None):
+    """Inputs of K draft tokens per sequence for speculative-decoding
+    verification: q,k,g [N,K,H,dk]; v, gate [N,K,H,dv]; beta [N,K,H]; the
+    accepted-prefix lengths a_i, uniform in [0, K]."""
+    base = w.seed if seed is None else seed
+    gen = torch.Generator().manual_seed(int(base) * 1_000_003 + 104729 * K)
+    t = _token_inputs(gen, w.N * K, w.H, w.dk, w.dv, w.in_dtype, w.gate)
+    out = {name: x.reshape((w.N, K) + tuple(x.shape[1:])) for name, x in t.items()}
+    out["num_accepted"] = torch.randint(0, K + 1, (w.N,), generator=gen, dtype=torch.int32)
+    return out
