@@ -129,6 +129,11 @@ namespace intra {
 //  phase 1 (cumulative gate as L G):
 constexpr uint32_t S_GOP = 0;           // bf16 MN-major [K=j 64 x N=c 128] raw g (K stride 2048)
 constexpr uint32_t S_LOP = 16384;       // bf16 K-major [128 x 64] (SBO 1024): L[m][j] = (j <= m % 64)
+//  phase 1 also: raw k, q, g rows of the chunk (rows padded to 272 bytes so
+//  that row-per-lane reads spread over the banks; rows past the end zero)
+constexpr uint32_t RAW_STRIDE = 272;
+constexpr uint32_t RAW_BYTES = 64 * RAW_STRIDE;
+constexpr uint32_t S_RAWK = 32768;      // k rows; q at + RAW_BYTES, g at + 2 RAW_BYTES
 //  phase 2 (decay-weighted K K^T and Q K^T):
 constexpr uint32_t S_AROW_HI = 0;       // bf16 K-major [128 x 128] (SBO 2048): K e^(G-Gm) ; Q e^(G-Gm)
 constexpr uint32_t S_AROW_LO = 32768;
@@ -145,6 +150,7 @@ constexpr uint32_t S_TP = 81920;        // bf16 K-major [128 x 64] (SBO 1024): T
 //  exact path (extreme decay) instead of phase 2:
 constexpr uint32_t S_FK = 0, S_FQ = 16384, S_FG = 32768, S_FAKK = 65536, S_FAQK = 81920;
 static_assert(S_MB + 3 * 16 * 17 * 4 <= S_KW, "solve scratch overlaps the W operand");
+static_assert(S_RAWK >= S_LOP + 16384 && S_RAWK + 3 * RAW_BYTES <= S_REGION, "raw rows overlap phase-1 operands");
 // per-chunk scalars after the region
 constexpr uint32_t S_BETA = S_REGION;          // fp32 [64]
 constexpr uint32_t S_GM = S_BETA + 256;        // fp32 [128] G at the middle row m
@@ -227,11 +233,19 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   __shared__ __align__(8) uint64_t bar, bar_l;
   __shared__ uint32_t s_tmem;
 
+  // Thread roles.  A warp may only touch the TMEM lane quarter of its SM
+  // sub-partition (warp % 4), so the TMEM-bound steps are split by quarter:
+  // quarters 0-1 hold the key rows of the products (lanes 0-63), quarters 2-3
+  // the query rows (lanes 64-127).  Everything else is split evenly: each
+  // thread owns chunk row r and the 32 channels [cb, cb + 32) of both k and q,
+  // so all four sub-partitions carry the same element-wise load.
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int side = (warp >> 1) & 1;  // 0: key rows (TMEM lanes 0-63), 1: query rows (64-127)
-  const int hh = warp >> 2;          // channel half
-  const int r = 32 * (warp & 1) + lane;
-  const int lane_base = 64 * side + 32 * (warp & 1);
+  const int qd = warp & 3;
+  const int side = qd >> 1;          // 0: TMEM lanes 0-63, 1: lanes 64-127
+  const int hh = warp >> 2;
+  const int r = 32 * (qd & 1) + lane;
+  const int lane_base = 32 * qd;
+  const int cb = 64 * hh + 32 * side;
   // 1D grid over (slot, head), head fastest, slots in reverse: the chunks of
   // the first sequences are produced last, so their workspace blocks are still
   // in L2 when the state kernel, which starts with those sequences, reads them.
@@ -276,6 +290,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   const int64_t tb = (int64_t)p.cu_seqlens[seq] + (int64_t)s_misc[1] * C;
   uint8_t* ws = reinterpret_cast<uint8_t*>(p.workspace) + (slot * H + head) * (int64_t)WS_BYTES;
 
+  // k, q, g rows of the chunk arrive by coalesced 16-byte asynchronous copies
+  // (a warp moves two whole rows per instruction); v and gate rows, read
+  // later, are prefetched into L2 meanwhile.
   if (warp == 0) {
     tc::tmem_alloc(&s_tmem, 256);
     tc::fence_before_sync();
@@ -287,34 +304,56 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     tc::mbar_arrive_expect_tx(&bar_l, sizeof(LTable));
     tc::bulk_g2s(sm + S_LOP, &g_ltable, sizeof(LTable), &bar_l);
   }
-  const bool valid = r < n;
-  const int64_t rowoff = ((tb + r) * H + head) * (int64_t)D + hh * 64;
-  const bf16* gsrc = reinterpret_cast<const bf16*>(side == 0 ? p.k : p.q);
-  uint4 xr[8];  // k (side 0) or q (side 1) for this row's 64 channels
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    xr[i] = valid ? __ldg(reinterpret_cast<const uint4*>(gsrc + rowoff) + i) : make_uint4(0, 0, 0, 0);
-
-  if (side == 0) {
+  for (int s = 0; s < 3 * C * 16 / kThreads; ++s) {
+    const int idx = tid + kThreads * s;
+    const int t = idx >> 10, j = (idx >> 4) & (C - 1), piece = idx & 15;
+    const bf16* base = reinterpret_cast<const bf16*>(t == 0 ? p.k : t == 1 ? p.q : p.g);
+    const bool has = j < n;
+    tc::cp_async16(sm + S_RAWK + t * RAW_BYTES + j * RAW_STRIDE + piece * 16,
+                   base + ((tb + (has ? j : 0)) * H + head) * (int64_t)D + piece * 8, has);
+  }
+  tc::cp_async_commit();
+  if (warp >= 1 && warp <= 4) {
+    const int s = tid - 32, t = s / C, j = s % C;  // t = 0: v, 1: gate
+    if (j < n && (t == 0 || p.gate)) {
+      const bf16* base = reinterpret_cast<const bf16*>(t == 0 ? p.v : p.gate);
+      tc::prefetch_l2(base + ((tb + j) * H + head) * (int64_t)D, 256);
+    }
+  }
+  tc::cp_async_wait_all();
+  __syncthreads();
+  const bool valid = r < n;
+  const int64_t rowoff = ((tb + r) * H + head) * (int64_t)D + cb;
+  const int64_t row0off = (tb * H + head) * (int64_t)D + cb;  // a row that exists (for zero-filled copies)
+  uint4 kr[4], qr[4];  // k and q of row r, channels [cb, cb + 32) (zero rows past the chunk's end)
+  {
+    const uint8_t* rk = sm + S_RAWK + r * RAW_STRIDE + cb * 2;
+    uint4 gr[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      kr[i] = *reinterpret_cast<const uint4*>(rk + 16 * i);
+      qr[i] = *reinterpret_cast<const uint4*>(rk + RAW_BYTES + 16 * i);
+      gr[i] = *reinterpret_cast<const uint4*>(rk + 2 * RAW_BYTES + 16 * i);
+    }
     // raw g (floored) -> B operand of the cumulative-sum product
-    const bf16* gg = reinterpret_cast<const bf16*>(p.g);
     const __nv_bfloat162 floor2 = __float2bfloat162_rn(kLogDecayFloor);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint4 gr = valid ? __ldg(reinterpret_cast<const uint4*>(gg + rowoff) + i) : make_uint4(0, 0, 0, 0);
-      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&gr);
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&gr[i]);
 #pragma unroll
       for (int u = 0; u < 4; ++u) h[u] = __hmax2(h[u], floor2);
-      *reinterpret_cast<uint4*>(sm + S_GOP + mnmaj(hh * 64 + 8 * i, r, 2048)) = gr;
+      *reinterpret_cast<uint4*>(sm + S_GOP + mnmaj(cb + 8 * i, r, 2048)) = gr[i];
     }
-    if (hh == 0) s_beta[r] = valid ? __bfloat162float(reinterpret_cast<const bf16*>(p.beta)[(tb + r) * H + head]) : 0.f;
   }
+  if (hh == 0 && side == 0)
+    s_beta[r] = valid ? __bfloat162float(reinterpret_cast<const bf16*>(p.beta)[(tb + r) * H + head]) : 0.f;
   tc::fence_proxy_async();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
-  // ---- G = L g : inclusive in-chunk cumulative sum, rows duplicated for both sides ----
+  // ---- G = L g : inclusive in-chunk cumulative sum, rows duplicated in both lane halves ----
   bool ok_l = true;
   if (tid == 0) ok_l = tc::mbar_wait(&bar_l, 0);  // the L operand has landed
   if (tid == 0 && ok_l) {
@@ -330,21 +369,18 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   phase ^= 1;
   tc::fence_after_sync();
   const int m = min(C / 2 - 1, n - 1);
-  // tcgen05.ld is warp-collective (.sync.aligned): whole key-side warps load,
-  // and only the lanes of rows m and n-1 store.
-  if (ok && side == 0) {
+  // tcgen05.ld is warp-collective (.sync.aligned): whole warps load, and only
+  // the lanes of rows m and n-1 store.
+  if (ok) {
     float g32[32];
+    tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, cb), g32);
+    if (r == m) {
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, hh * 64 + 32 * part), g32);
-      if (r == m) {
+      for (int u = 0; u < 32; ++u) s_gm[cb + u] = g32[u];
+    }
+    if (r == n - 1) {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) s_gm[hh * 64 + 32 * part + u] = g32[u];
-      }
-      if (r == n - 1) {
-#pragma unroll
-        for (int u = 0; u < 32; ++u) s_gl[hh * 64 + 32 * part + u] = g32[u];
-      }
+      for (int u = 0; u < 32; ++u) s_gl[cb + u] = g32[u];
     }
   }
   __syncthreads();
@@ -363,49 +399,50 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   __syncthreads();
 
   // ---- operands of the decay-weighted products (and the global-only ones) ----
-  // e_m = e^(G - G_m), e_i = e^(G_m - G).  A chunk where some |G - G_m| > 60
+  // e1 = e^(G - G_m), e2 = e^(G_m - G).  A chunk where some |G - G_m| > 60
   // is redone on the exact path below (these values are then discarded).
   {
     bool big = false;
+    float g32[32];
+    tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, cb), g32);
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      float g32[32];
-      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, hh * 64 + 32 * part), g32);
+    for (int i = 0; i < 4; ++i) {
+      const int c0 = cb + 8 * i;
+      float kx[8], qx[8], e1[8], e2[8], v[8];
+      unpack_bf8(kr[i], kx);
+      unpack_bf8(qr[i], qx);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int i = part * 4 + q4;
-        const int c0 = hh * 64 + 8 * i;
-        float x[8], v1[8], v2[8], dg[8];
-        unpack_bf8(xr[i], x);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          dg[u] = g32[8 * q4 + u] - s_gm[c0 + u];
-          big |= fabsf(dg[u]) > 60.f;
-        }
-        uint4 hi, lo;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v1[u] = x[u] * __expf(dg[u]);
-        split_bf8(v1, hi, lo);
-        const int arow = side == 0 ? r : 64 + r;
-        *reinterpret_cast<uint4*>(sm + S_AROW_HI + kmaj(arow, c0, 2048)) = hi;
-        *reinterpret_cast<uint4*>(sm + S_AROW_LO + kmaj(arow, c0, 2048)) = lo;
-        if (side == 0) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) v2[u] = x[u] * __expf(-dg[u]);
-          split_bf8(v2, hi, lo);
-          *reinterpret_cast<uint4*>(sm + S_BCOL_HI + kmaj(r, c0, 2048)) = hi;
-          *reinterpret_cast<uint4*>(sm + S_BCOL_LO + kmaj(r, c0, 2048)) = lo;
-          // (K e^(G_last - G))^T, fp16 MN-major, straight to the workspace
-#pragma unroll
-          for (int u = 0; u < 8; ++u) v2[u] *= s_eglm[c0 + u];
-          *reinterpret_cast<uint4*>(ws + WS_KLT + mnmaj(c0, r, 2048)) = pack_half8(v2);
-        } else {
-          // Q e^G -> rows 64-127 of [W; Q e^G] in the workspace
-#pragma unroll
-          for (int u = 0; u < 8; ++u) v1[u] *= s_egm[c0 + u];
-          *reinterpret_cast<uint4*>(ws + WS_PA + kmaj(64 + r, c0, 2048)) = pack_half8(v1);
-        }
+      for (int u = 0; u < 8; ++u) {
+        const float dg = g32[8 * i + u] - s_gm[c0 + u];
+        big |= fabsf(dg) > 60.f;
+        e1[u] = __expf(dg);
+        e2[u] = __expf(-dg);
       }
+      uint4 hi, lo;
+      // key row r of the left operand: K e^(G - G_m)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = kx[u] * e1[u];
+      split_bf8(v, hi, lo);
+      *reinterpret_cast<uint4*>(sm + S_AROW_HI + kmaj(r, c0, 2048)) = hi;
+      *reinterpret_cast<uint4*>(sm + S_AROW_LO + kmaj(r, c0, 2048)) = lo;
+      // query row 64 + r: Q e^(G - G_m); Q e^G -> rows 64-127 of [W; Q e^G] in the workspace
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = qx[u] * e1[u];
+      split_bf8(v, hi, lo);
+      *reinterpret_cast<uint4*>(sm + S_AROW_HI + kmaj(64 + r, c0, 2048)) = hi;
+      *reinterpret_cast<uint4*>(sm + S_AROW_LO + kmaj(64 + r, c0, 2048)) = lo;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] *= s_egm[c0 + u];
+      *reinterpret_cast<uint4*>(ws + WS_PA + kmaj(64 + r, c0, 2048)) = pack_half8(v);
+      // right operand row r: K e^(G_m - G); (K e^(G_last - G))^T to the workspace
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = kx[u] * e2[u];
+      split_bf8(v, hi, lo);
+      *reinterpret_cast<uint4*>(sm + S_BCOL_HI + kmaj(r, c0, 2048)) = hi;
+      *reinterpret_cast<uint4*>(sm + S_BCOL_LO + kmaj(r, c0, 2048)) = lo;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] *= s_eglm[c0 + u];
+      *reinterpret_cast<uint4*>(ws + WS_KLT + mnmaj(c0, r, 2048)) = pack_half8(v);
     }
     if (big) atomicOr(&s_misc[3], 1);
   }
@@ -429,62 +466,62 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
       }
       tc::mma_commit(&bar);
     }
-    if (p.gate) gated_weight_rows(p, ws, tb, head, n, r, 64 * hh + 32 * side);
+    if (p.gate) gated_weight_rows(p, ws, tb, head, n, r, cb);
   } else {
-    if (p.gate) gated_weight_rows(p, ws, tb, head, n, r, 64 * hh + 32 * side);
+    if (p.gate) gated_weight_rows(p, ws, tb, head, n, r, cb);
     // exact element-wise path: stage k, q, G for every row, write the
     // global-only operands with direct exponentials
     bf16* fk = reinterpret_cast<bf16*>(sm + S_FK);
     bf16* fq = reinterpret_cast<bf16*>(sm + S_FQ);
     float* fg = reinterpret_cast<float*>(sm + S_FG);
+    float g32[32];
+    tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, cb), g32);
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      float g32[32];
-      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, hh * 64 + 32 * part), g32);
+    for (int i = 0; i < 4; ++i) {
+      const int c0 = cb + 8 * i;
+      float kx[8], qx[8], v[8];
+      unpack_bf8(kr[i], kx);
+      unpack_bf8(qr[i], qx);
+      *reinterpret_cast<uint4*>(fk + r * D + c0) = kr[i];
+      *reinterpret_cast<uint4*>(fq + r * D + c0) = qr[i];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int i = part * 4 + q4;
-        const int c0 = hh * 64 + 8 * i;
-        float x[8], v1[8];
-        unpack_bf8(xr[i], x);
-        *reinterpret_cast<uint4*>((side == 0 ? fk : fq) + r * D + c0) = xr[i];
-        if (side == 0) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            fg[r * D + c0 + u] = g32[8 * q4 + u];
-            v1[u] = x[u] * expf(s_gl[c0 + u] - g32[8 * q4 + u]);
-          }
-          *reinterpret_cast<uint4*>(ws + WS_KLT + mnmaj(c0, r, 2048)) = pack_half8(v1);
-        } else {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) v1[u] = x[u] * expf(g32[8 * q4 + u]);
-          *reinterpret_cast<uint4*>(ws + WS_PA + kmaj(64 + r, c0, 2048)) = pack_half8(v1);
-        }
+      for (int u = 0; u < 8; ++u) {
+        fg[r * D + c0 + u] = g32[8 * i + u];
+        v[u] = kx[u] * expf(s_gl[c0 + u] - g32[8 * i + u]);
       }
+      *reinterpret_cast<uint4*>(ws + WS_KLT + mnmaj(c0, r, 2048)) = pack_half8(v);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = qx[u] * expf(g32[8 * i + u]);
+      *reinterpret_cast<uint4*>(ws + WS_PA + kmaj(64 + r, c0, 2048)) = pack_half8(v);
     }
     __syncthreads();
     intra_exact_A(fk, fq, fg, n, reinterpret_cast<float*>(sm + S_FAKK), reinterpret_cast<float*>(sm + S_FAQK));
   }
+  // V -> U0 operand (bf16 MN-major [K=j 64 x N=v 128]) by asynchronous 16-byte
+  // copies, once the operand buffer it lands in is no longer read
+  const bf16* gv = reinterpret_cast<const bf16*>(p.v) + (valid ? rowoff : row0off);
   float a32[32];
-  float kwv[64];  // K e^G for this row's 64 channels (key side)
+  uint4 kw[4];  // K e^G for row r, channels [cb, cb + 32) (bf16)
   if (!exact) {
     ok = cta_wait(&bar, phase);
     phase ^= 1;
     tc::fence_after_sync();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      tc::cp_async16(sm + S_VB + mnmaj(cb + 8 * i, r, 2048), reinterpret_cast<const uint4*>(gv) + i, valid);
+    tc::cp_async_commit();
     if (ok) {
       tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, 128 + hh * 32), a32);
-      if (side == 1) {
-        // K e^G = (K e^(G-Gm)) e^(G_m) for key row r, from the hi+lo operand
-        // still in place (the query-side threads have the lighter load)
+      // K e^G = (K e^(G - G_m)) e^(G_m), from the hi + lo operand still in place
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c0 = hh * 64 + 8 * i;
-          float h8[8], l8[8];
-          unpack_bf8(*reinterpret_cast<const uint4*>(sm + S_AROW_HI + kmaj(r, c0, 2048)), h8);
-          unpack_bf8(*reinterpret_cast<const uint4*>(sm + S_AROW_LO + kmaj(r, c0, 2048)), l8);
+      for (int i = 0; i < 4; ++i) {
+        const int c0 = cb + 8 * i;
+        float h8[8], l8[8];
+        unpack_bf8(*reinterpret_cast<const uint4*>(sm + S_AROW_HI + kmaj(r, c0, 2048)), h8);
+        unpack_bf8(*reinterpret_cast<const uint4*>(sm + S_AROW_LO + kmaj(r, c0, 2048)), l8);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) kwv[8 * i + u] = (h8[u] + l8[u]) * s_egm[c0 + u];
-        }
+        for (int u = 0; u < 8; ++u) h8[u] = (h8[u] + l8[u]) * s_egm[c0 + u];
+        kw[i] = pack_bf8(h8);
       }
     }
   } else {
@@ -496,108 +533,45 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
       const int j = hh * 32 + u;
       a32[u] = side == 0 ? fakk[r * C + j] : faqk[r * C + j];
     }
-    if (side == 1) {
-      const bf16* fk = reinterpret_cast<const bf16*>(sm + S_FK);
-      const float* fg = reinterpret_cast<const float*>(sm + S_FG);
+    const bf16* fk = reinterpret_cast<const bf16*>(sm + S_FK);
+    const float* fg = reinterpret_cast<const float*>(sm + S_FG);
 #pragma unroll
-      for (int u = 0; u < 64; ++u)
-        kwv[u] = __bfloat162float(fk[r * D + hh * 64 + u]) * expf(fg[r * D + hh * 64 + u]);
+    for (int i = 0; i < 4; ++i) {
+      float x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = cb + 8 * i + u;
+        x[u] = __bfloat162float(fk[r * D + c]) * expf(fg[r * D + c]);
+      }
+      kw[i] = pack_bf8(x);
     }
   }
   tc::fence_before_sync();
   __syncthreads();  // region reads done; phase-3 buffers may be written
   if (!ok) {
+    tc::cp_async_wait_all();
     if (tid == 0) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
     return;
   }
+  if (exact) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      tc::cp_async16(sm + S_VB + mnmaj(cb + 8 * i, r, 2048), reinterpret_cast<const uint4*>(gv) + i, valid);
+    tc::cp_async_commit();
+  }
   float* s_akk = reinterpret_cast<float*>(sm + S_AKK);
   float* s_tf = reinterpret_cast<float*>(sm + S_TF);
   if (side == 0) {
-    // ---- key-side warps (0, 1, 4, 5; named barrier 2): T = (I + A)^-1 ----
-    const int kt = (warp >> 2) * 64 + (warp & 1) * 32 + lane;  // 0..127
+    // beta-scaled strictly lower A_kk (TMEM lanes 0-63)
     const float br = s_beta[r];
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
       const int j = hh * 32 + u;
       s_akk[r * 65 + j] = (j < r) ? br * a32[u] : 0.f;
     }
-    asm volatile("bar.sync 2, 128;" ::: "memory");
-    if (kt < 64) {
-      // column jj of the inverse of the unit lower-triangular 16x16 block b:
-      // x_rr = [rr == jj] - sum_{ii < rr} A[rr][ii] x_ii  (x_ii = 0 for ii < jj)
-      const int b = kt >> 4, jj = kt & 15;
-      const float* ab = s_akk + (16 * b) * 65 + 16 * b;
-      float x[16];
-#pragma unroll
-      for (int rr = 0; rr < 16; ++rr) {
-        float sacc = rr == jj ? 1.f : 0.f;
-#pragma unroll
-        for (int ii = 0; ii < rr; ++ii) sacc -= ab[rr * 65 + ii] * x[ii];
-        x[rr] = rr >= jj ? sacc : 0.f;
-      }
-#pragma unroll
-      for (int rr = 0; rr < 16; ++rr) s_tf[(16 * b + rr) * 65 + 16 * b + jj] = x[rr];
-    }
-    asm volatile("bar.sync 2, 128;" ::: "memory");
-    // off-diagonal 16x16 blocks, nearest the diagonal first:
-    //   M = sum_{bk=bj}^{bi-1} A[bi][bk] T[bk][bj],  T[bi][bj] = -T[bi][bi] M
-    // each thread owns 2x2 output tiles (rows rr, rr+8; columns cc, cc+8)
-    float* s_mb = reinterpret_cast<float*>(sm + S_MB);
-    for (int dist = 1; dist < 4; ++dist) {
-      const int ntiles = (4 - dist) * 64;
-      for (int t = kt; t < ntiles; t += 128) {
-        const int pi = t >> 6, rr = (t >> 3) & 7, cc = t & 7;
-        const int bj = pi, bi = pi + dist;
-        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-        for (int bk = bj; bk < bi; ++bk) {
-          const float* ar0 = s_akk + (16 * bi + rr) * 65 + 16 * bk;
-          const float* ar1 = ar0 + 8 * 65;
-          const float* tcol = s_tf + (16 * bk) * 65 + 16 * bj + cc;
-#pragma unroll
-          for (int l = 0; l < 16; ++l) {
-            const float x0 = ar0[l], x1 = ar1[l], y0 = tcol[l * 65], y1 = tcol[l * 65 + 8];
-            a00 += x0 * y0; a01 += x0 * y1; a10 += x1 * y0; a11 += x1 * y1;
-          }
-        }
-        float* mb = s_mb + pi * 272;
-        mb[rr * 17 + cc] = a00; mb[rr * 17 + cc + 8] = a01;
-        mb[(rr + 8) * 17 + cc] = a10; mb[(rr + 8) * 17 + cc + 8] = a11;
-      }
-      asm volatile("bar.sync 2, 128;" ::: "memory");
-      for (int t = kt; t < ntiles; t += 128) {
-        const int pi = t >> 6, rr = (t >> 3) & 7, cc = t & 7;
-        const int bj = pi, bi = pi + dist;
-        const float* tr0 = s_tf + (16 * bi + rr) * 65 + 16 * bi;
-        const float* tr1 = tr0 + 8 * 65;
-        const float* mb = s_mb + pi * 272 + cc;
-        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-#pragma unroll
-        for (int l = 0; l < 16; ++l) {
-          const float x0 = tr0[l], x1 = tr1[l], y0 = mb[l * 17], y1 = mb[l * 17 + 8];
-          a00 += x0 * y0; a01 += x0 * y1; a10 += x1 * y0; a11 += x1 * y1;
-        }
-        float* dst = s_tf + (16 * bi + rr) * 65 + 16 * bj + cc;
-        dst[0] = -a00; dst[8] = -a01; dst[8 * 65] = -a10; dst[8 * 65 + 8] = -a11;
-      }
-      asm volatile("bar.sync 2, 128;" ::: "memory");
-    }
-    // T' = T Diag(beta) -> bf16 K-major [128 x 64] rows 0-63
-#pragma unroll
-    for (int g8 = 0; g8 < 4; ++g8) {
-      float x[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = hh * 32 + 8 * g8 + u;
-        x[u] = j <= r ? s_tf[r * 65 + j] * s_beta[j] : 0.f;  // blocks above the diagonal are never written
-      }
-      *reinterpret_cast<uint4*>(sm + S_TP + kmaj(r, hh * 32 + 8 * g8, 1024)) = pack_bf8(x);
-    }
   } else {
-    // ---- query-side warps, concurrently: K e^G -> W operand, A_qk -> workspace, V -> U0 operand
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      *reinterpret_cast<uint4*>(sm + S_KW + mnmaj(hh * 64 + 8 * i, r, 2048)) = pack_bf8(kwv + 8 * i);
+    // A_qk (lanes 64-127), lower triangle with the diagonal, to the workspace
 #pragma unroll
     for (int g8 = 0; g8 < 4; ++g8) {
       float x[8];
@@ -608,16 +582,91 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
       }
       *reinterpret_cast<uint4*>(ws + WS_AQK + kmaj(r, hh * 32 + 8 * g8, 1024)) = pack_half8(x);
     }
-    const bf16* gv = reinterpret_cast<const bf16*>(p.v);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint4 vr = valid ? __ldg(reinterpret_cast<const uint4*>(gv + rowoff) + i) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(sm + S_VB + mnmaj(hh * 64 + 8 * i, r, 2048)) = vr;
-    }
-    const int qt = hh * 64 + r;  // 0..127
-    for (int i = qt; i < 8192 / 16; i += 128)
-      reinterpret_cast<uint4*>(sm + S_TP + 8192)[i] = make_uint4(0, 0, 0, 0);
   }
+  // K e^G -> W operand (bf16 MN-major [K=j 64 x N=c 128])
+#pragma unroll
+  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(sm + S_KW + mnmaj(cb + 8 * i, r, 2048)) = kw[i];
+  __syncthreads();
+  // ---- T = (I + A)^-1 on all eight warps ----
+  if (warp < 4 && lane < 16) {
+    // column jj of the inverse of the unit lower-triangular 16x16 block b:
+    // x_rr = [rr == jj] - sum_{ii < rr} A[rr][ii] x_ii  (x_ii = 0 for ii < jj)
+    const int b = warp, jj = lane;
+    const float* ab = s_akk + (16 * b) * 65 + 16 * b;
+    float x[16];
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+      float sacc = rr == jj ? 1.f : 0.f;
+#pragma unroll
+      for (int ii = 0; ii < rr; ++ii) sacc -= ab[rr * 65 + ii] * x[ii];
+      x[rr] = rr >= jj ? sacc : 0.f;
+    }
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) s_tf[(16 * b + rr) * 65 + 16 * b + jj] = x[rr];
+  }
+  __syncthreads();
+  // off-diagonal 16x16 blocks, nearest the diagonal first:
+  //   M = sum_{bk=bj}^{bi-1} A[bi][bk] T[bk][bj],  T[bi][bj] = -T[bi][bi] M
+  // each thread owns 2x2 output tiles (rows rr, rr+8; columns cc, cc+8)
+  float* s_mb = reinterpret_cast<float*>(sm + S_MB);
+  for (int dist = 1; dist < 4; ++dist) {
+    const int ntiles = (4 - dist) * 64;
+    if (tid < ntiles) {
+      const int t = tid;
+      const int pi = t >> 6, rr = (t >> 3) & 7, cc = t & 7;
+      const int bj = pi, bi = pi + dist;
+      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+      for (int bk = bj; bk < bi; ++bk) {
+        const float* ar0 = s_akk + (16 * bi + rr) * 65 + 16 * bk;
+        const float* ar1 = ar0 + 8 * 65;
+        const float* tcol = s_tf + (16 * bk) * 65 + 16 * bj + cc;
+#pragma unroll
+        for (int l = 0; l < 16; ++l) {
+          const float x0 = ar0[l], x1 = ar1[l], y0 = tcol[l * 65], y1 = tcol[l * 65 + 8];
+          a00 += x0 * y0; a01 += x0 * y1; a10 += x1 * y0; a11 += x1 * y1;
+        }
+      }
+      float* mb = s_mb + pi * 272;
+      mb[rr * 17 + cc] = a00; mb[rr * 17 + cc + 8] = a01;
+      mb[(rr + 8) * 17 + cc] = a10; mb[(rr + 8) * 17 + cc + 8] = a11;
+    }
+    __syncthreads();
+    if (tid < ntiles) {
+      const int t = tid;
+      const int pi = t >> 6, rr = (t >> 3) & 7, cc = t & 7;
+      const int bj = pi, bi = pi + dist;
+      const float* tr0 = s_tf + (16 * bi + rr) * 65 + 16 * bi;
+      const float* tr1 = tr0 + 8 * 65;
+      const float* mb = s_mb + pi * 272 + cc;
+      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+#pragma unroll
+      for (int l = 0; l < 16; ++l) {
+        const float x0 = tr0[l], x1 = tr1[l], y0 = mb[l * 17], y1 = mb[l * 17 + 8];
+        a00 += x0 * y0; a01 += x0 * y1; a10 += x1 * y0; a11 += x1 * y1;
+      }
+      float* dst = s_tf + (16 * bi + rr) * 65 + 16 * bj + cc;
+      dst[0] = -a00; dst[8] = -a01; dst[8 * 65] = -a10; dst[8 * 65 + 8] = -a11;
+    }
+    __syncthreads();
+  }
+  // T' = T Diag(beta) -> bf16 K-major [128 x 64], rows 64-127 a copy of rows
+  // 0-63 (so the product's lanes 64-127 repeat it for the query-side warps)
+  {
+    const int j0 = 32 * hh + 16 * side;
+#pragma unroll
+    for (int g8 = 0; g8 < 2; ++g8) {
+      float x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + 8 * g8 + u;
+        x[u] = j <= r ? s_tf[r * 65 + j] * s_beta[j] : 0.f;  // blocks above the diagonal are never written
+      }
+      const uint4 t8 = pack_bf8(x);
+      *reinterpret_cast<uint4*>(sm + S_TP + kmaj(r, j0 + 8 * g8, 1024)) = t8;
+      *reinterpret_cast<uint4*>(sm + S_TP + kmaj(64 + r, j0 + 8 * g8, 1024)) = t8;
+    }
+  }
+  tc::cp_async_wait_all();
   tc::fence_proxy_async();
   tc::fence_before_sync();
   __syncthreads();
@@ -625,31 +674,34 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   // ---- W = T' (K e^G) -> TMEM cols 0-127 ; U0 = T' V -> cols 128-255 ----
   if (tid == 0) {
     constexpr uint32_t idW = tc::idesc_f16(128, 128, true, false, true);
-    const uint32_t ta = tc::smem_u32(sm + S_TP), kw = tc::smem_u32(sm + S_KW), vb = tc::smem_u32(sm + S_VB);
+    const uint32_t ta = tc::smem_u32(sm + S_TP), kwb = tc::smem_u32(sm + S_KW), vb = tc::smem_u32(sm + S_VB);
 #pragma unroll
     for (int kk = 0; kk < C / 16; ++kk) {
       const uint64_t a = tc::sdesc(ta + kk * 256, 128, 1024);
-      tc::mma_f16(tmem, a, tc::sdesc(kw + kk * 4096, 2048, 128), idW, kk > 0);
+      tc::mma_f16(tmem, a, tc::sdesc(kwb + kk * 4096, 2048, 128), idW, kk > 0);
       tc::mma_f16(tmem + 128, a, tc::sdesc(vb + kk * 4096, 2048, 128), idW, kk > 0);
     }
     tc::mma_commit(&bar);
   }
   ok = cta_wait(&bar, phase);
   tc::fence_after_sync();
-  if (ok && side == 0) {
-    // W rows 0-63 of [W; Q e^G] (fp16 K-major) and U0 (fp16, [v/8][row][8])
+  if (ok) {
+    // lanes 0-63: W rows -> rows 0-63 of [W; Q e^G] (fp16 K-major);
+    // lanes 64-127: U0 rows -> fp16 [v/8][row][8]
     float w32[32];
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
       const int cbase = hh * 64 + part * 32;
-      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, cbase), w32);
+      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, 128 * side + cbase), w32);
+      if (side == 0) {
 #pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8)
-        *reinterpret_cast<uint4*>(ws + WS_PA + kmaj(r, cbase + 8 * g8, 2048)) = pack_half8(w32 + 8 * g8);
-      tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, 128 + cbase), w32);
+        for (int g8 = 0; g8 < 4; ++g8)
+          *reinterpret_cast<uint4*>(ws + WS_PA + kmaj(r, cbase + 8 * g8, 2048)) = pack_half8(w32 + 8 * g8);
+      } else {
 #pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8)
-        *reinterpret_cast<uint4*>(ws + WS_U0 + ((cbase + 8 * g8) >> 3) * 1024 + r * 16) = pack_half8(w32 + 8 * g8);
+        for (int g8 = 0; g8 < 4; ++g8)
+          *reinterpret_cast<uint4*>(ws + WS_U0 + ((cbase + 8 * g8) >> 3) * 1024 + r * 16) = pack_half8(w32 + 8 * g8);
+      }
     }
   }
   if (!ok && tid == 0) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
