@@ -252,6 +252,11 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   const int H = p.H;
   const int head = (int)(blockIdx.x % (unsigned)H);
   const int64_t slot = num_slots_bound(p.T, p.N) - 1 - (int64_t)(blockIdx.x / (unsigned)H);
+  // The state kernel is launched as a programmatic dependent of this grid:
+  // once every CTA of this grid has started, its CTAs may take SMs freed by
+  // this grid's last wave and run their prologue; they wait for this grid's
+  // completion (griddepcontrol.wait) before reading the workspace.
+  asm volatile("griddepcontrol.launch_dependents;");
 
   // ---- locate (sequence, chunk) of this slot: sequence i owns the slots
   //      [first(i), first(i+1)) with first(i) = cu[i]/C + i (strictly
@@ -724,18 +729,62 @@ constexpr uint32_t S_SS = S_NW + 512;      // fp32 [2][64]
 constexpr uint32_t SMEM_BYTES = S_SS + 512;
 }  // namespace state
 
-template <typename TS>
-__device__ __forceinline__ void load_state_row(const TS* src, float* s) {
+// 8x8 transpose of 16-byte chunks within each group of 8 lanes: before, lane
+// j of a group holds v[c] = X[j][c]; after, v[c] = X[c][j] (xor butterfly,
+// constant register indices).
+template <typename V4>  // float4 or uint4
+__device__ __forceinline__ void transpose8x8(V4 (&v)[8], int lane) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float4 v = load4(src + 4 * i);
-    s[4 * i] = v.x; s[4 * i + 1] = v.y; s[4 * i + 2] = v.z; s[4 * i + 3] = v.w;
+  for (int b = 4; b >= 1; b >>= 1) {
+    const bool upper = (lane & b) != 0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      if (c & b) continue;
+      const V4 send = upper ? v[c] : v[c | b];
+      V4 recv;
+      recv.x = __shfl_xor_sync(0xffffffffu, send.x, b);
+      recv.y = __shfl_xor_sync(0xffffffffu, send.y, b);
+      recv.z = __shfl_xor_sync(0xffffffffu, send.z, b);
+      recv.w = __shfl_xor_sync(0xffffffffu, send.w, b);
+      if (upper) v[c] = recv; else v[c | b] = recv;
+    }
+  }
+}
+
+// A (dk x dv) row-major state block is held one row per thread: row
+// 32 quad + lane, columns [64 hh, 64 hh + 64) in s[64].  Loads and stores go
+// through transpose8x8 so that each memory instruction of a warp covers four
+// whole 128-byte (fp32) row segments instead of 32 scattered 16-byte pieces.
+// Warp-collective: every lane must take part.
+template <typename TS>
+__device__ __forceinline__ void load_state_block(const TS* blk, float* s, int quad, int lane, int hh) {
+  const int rbase = 32 * quad + 8 * (lane >> 3), j = lane & 7;
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    float4 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) v[c] = load4(blk + (rbase + c) * D + hh * 64 + 32 * h2 + 4 * j);
+    transpose8x8(v, lane);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      s[32 * h2 + 4 * c] = v[c].x; s[32 * h2 + 4 * c + 1] = v[c].y;
+      s[32 * h2 + 4 * c + 2] = v[c].z; s[32 * h2 + 4 * c + 3] = v[c].w;
+    }
   }
 }
 template <typename TS>
-__device__ __forceinline__ void store_state_row(TS* dst, const float* s) {
+__device__ __forceinline__ void store_state_block(TS* blk, const float* s, int quad, int lane, int hh) {
+  const int rbase = 32 * quad + 8 * (lane >> 3), j = lane & 7;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) store4(dst + 4 * i, make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]));
+  for (int h2 = 0; h2 < 2; ++h2) {
+    float4 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      v[c] = make_float4(s[32 * h2 + 4 * c], s[32 * h2 + 4 * c + 1], s[32 * h2 + 4 * c + 2], s[32 * h2 + 4 * c + 3]);
+    transpose8x8(v, lane);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) store4(blk + (rbase + c) * D + hh * 64 + 32 * h2 + 4 * j, v[c]);
+  }
 }
 
 template <typename TS>
@@ -784,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   TS* slot_state = reinterpret_cast<TS*>(p.state_pool) + ((int64_t)si.slot * H + head) * (D * D);
   float S[64];
   if (si.init) {
-    load_state_row(slot_state + lrow * D + hh * 64, S);
+    load_state_block(slot_state, S, quad, lane, hh);
   } else {
 #pragma unroll
     for (int i = 0; i < 64; ++i) S[i] = 0.f;
@@ -811,6 +860,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     uint8_t* st = sm + (k & 1) * STAGE;
     tc::bulk_g2s(st + ST_AQK, ws_block(k) + WS_AQK, WS_COPY1, &bar_ld[k & 1]);
   };
+  // the workspace is written by the intra-chunk grid that precedes this one
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0) {
     issue_load_main(0);
     issue_load_tail(0);
@@ -843,6 +894,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
       tc::tmem_ld32(tc::tmem_addr(tP, 32 * quad, hh * 64 + 32), t32);
 #pragma unroll
       for (int u = 0; u < 32; ++u) o[32 + u] = p.scale * t32[u];
+    } else {
+#pragma unroll
+      for (int u = 0; u < 64; ++u) o[u] = 0.f;
     }
     if (p.gate) {
       float ss = 0.f;
@@ -876,8 +930,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   int64_t pending_ck = -1;  // checkpoint entry whose store is still to be issued
   auto store_pending_ck = [&]() {
     if (pending_ck >= 0) {
-      TS* dst = reinterpret_cast<TS*>(p.checkpoints) + (pending_ck * H + head) * (int64_t)(D * D) + lrow * D + hh * 64;
-      store_state_row(dst, S);
+      store_state_block(reinterpret_cast<TS*>(p.checkpoints) + (pending_ck * H + head) * (int64_t)(D * D), S, quad,
+                        lane, hh);
       pending_ck = -1;
     }
   };
@@ -1001,7 +1055,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     }
   } else {
     store_pending_ck();
-    store_state_row(slot_state + lrow * D + hh * 64, S);
+    store_state_block(slot_state, S, quad, lane, hh);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1026,18 +1080,28 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
   e = set_smem_once(sk, (int)tcp::state::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int64_t slots = tcp::num_slots_bound(p.T, p.N);
-  if (p.T > 0 && slots > 0) {
+  const bool intra = p.T > 0 && slots > 0;
+  if (intra) {
     dim3 g1((unsigned)(slots * p.H));
     tcp::kda_intra_kernel<<<g1, tcp::kThreads, tcp::intra::SMEM_BYTES, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  dim3 g2((unsigned)((int64_t)p.N * p.H));
-  if (p.state_dtype == KDA_F32)
-    tcp::kda_state_kernel<float><<<g2, tcp::kThreads, tcp::state::SMEM_BYTES, stream>>>(p);
-  else
-    tcp::kda_state_kernel<bf16><<<g2, tcp::kThreads, tcp::state::SMEM_BYTES, stream>>>(p);
-  return cudaGetLastError();
+  // The state kernel depends on the intra grid programmatically (it may start
+  // its prologue while the intra grid's last CTAs run); without an intra grid
+  // it is an ordinary stream-ordered launch.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((int64_t)p.N * p.H));
+  cfg.blockDim = dim3(tcp::kThreads);
+  cfg.dynamicSmemBytes = tcp::state::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = intra ? 1 : 0;
+  if (p.state_dtype == KDA_F32) return cudaLaunchKernelEx(&cfg, tcp::kda_state_kernel<float>, p);
+  return cudaLaunchKernelEx(&cfg, tcp::kda_state_kernel<bf16>, p);
 }
 
 }  // namespace kda
