@@ -94,7 +94,11 @@ KDA_API size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int 
  *               [cu_seqlens[i], cu_seqlens[i+1]); cu_seqlens[0] == 0 and
  *               cu_seqlens[N] == T.  Chunks restart at every sequence start;
  *               the last chunk of a sequence may be partial.  A zero-length
- *               sequence is a no-op (its slot is not rewritten).
+ *               sequence is a no-op (its slot is not rewritten).  The entries
+ *               must be non-decreasing: a negative length latches
+ *               KDA_DEV_BAD_SEQLENS; ranges that overlap an earlier sequence
+ *               give undefined values for the sequences involved (every
+ *               access still stays inside the buffers).
  *  state_indices int32 [N], device.  Sequence i starts from
  *               state_pool[state_indices[i]] and its final state is written
  *               back to that slot in place.  -1 marks a padding sequence: its
