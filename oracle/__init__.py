@@ -63,6 +63,10 @@ def _load():
             lib.kda_oracle_norm_gate.restype = ctypes.c_int
             lib.kda_oracle_norm_gate.argtypes = [P, P, P, ctypes.c_double, P, ctypes.c_int64,
                                                  ctypes.c_int, ctypes.c_int]
+            lib.kda_oracle_norm_gate_ex.restype = ctypes.c_int
+            lib.kda_oracle_norm_gate_ex.argtypes = [P, P, P, ctypes.c_int64, P, P, ctypes.c_double,
+                                                    ctypes.c_int, P, P, ctypes.c_int64, ctypes.c_int,
+                                                    ctypes.c_int]
             lib.kda_oracle_checkpoint_offsets.restype = ctypes.c_int64
             lib.kda_oracle_checkpoint_offsets.argtypes = [P, ctypes.c_int, ctypes.c_int, P]
             lib.kda_oracle_max_threads.restype = ctypes.c_int
@@ -217,3 +221,22 @@ def norm_gate(o, gate, w, eps=1e-6, gate_act="sigmoid"):
     _check(_load().kda_oracle_norm_gate(_ptr(o), _ptr(gate), _ptr(w), float(eps), _ptr(y),
                                         rows, dv, ACT[gate_act]))
     return y
+
+
+def norm_gate_ex(o, gate, *, residual=None, w=None, b=None, eps=1e-6, gate_act="sigmoid",
+                 gate_row_stride=0):
+    """Norm-gate variants: x = o + residual; z = x / sqrt(mean(x^2)+eps) * w + b;
+    y = z * act(gate).  o, residual: [rows, H, dv]; gate: flat buffer whose row r
+    (all heads) starts at r * gate_row_stride (0: H*dv, i.e. [rows, H, dv]).
+    Returns ``(y, residual_out)``, residual_out = x."""
+    o = _f64(o)
+    rows, H, dv = o.shape
+    residual, w, b = _f64(residual), _f64(w), _f64(b)
+    gate = _f64(gate).reshape(-1)
+    stride = gate_row_stride or H * dv
+    y = np.zeros_like(o)
+    res_out = np.zeros_like(o)
+    _check(_load().kda_oracle_norm_gate_ex(_ptr(o), _ptr(residual), _ptr(gate), int(stride), _ptr(w),
+                                           _ptr(b), float(eps), ACT[gate_act], _ptr(y), _ptr(res_out),
+                                           rows, H, dv))
+    return y, res_out

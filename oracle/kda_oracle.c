@@ -114,6 +114,44 @@ int kda_oracle_norm_gate(const double* o, const double* gate, const double* w, d
   return ORACLE_OK;
 }
 
+/*
+ * Norm-gate variants covered by the norm-gate tests of "[Feature][KDA] Add
+ * Kimi K3 KDA execution" (testing section: fp16/bf16, sigmoid/SiLU, packed
+ * gate strides, affine and residual/prenorm paths).  Per (row r, head h):
+ *   x = o + residual                      (residual optional)
+ *   residual_out = x                      (the prenorm output, optional)
+ *   z = x / sqrt(mean(x^2) + eps) * w + b (w optional: 1; b optional: 0)
+ *   y = z * act(gate)                     act = sigmoid or SiLU
+ * o, residual, y, residual_out are [rows, H, dv]; w, b are [dv]; the gate of
+ * (r, h) starts at gate[r * gate_row_stride + h * dv].
+ */
+int kda_oracle_norm_gate_ex(const double* o, const double* residual, const double* gate,
+                            int64_t gate_row_stride, const double* w, const double* b, double eps,
+                            int act, double* y, double* residual_out, int64_t rows, int H, int dv) {
+  if (!o || !gate || !y || rows < 0 || H <= 0 || dv <= 0 || act < 0 || act > 1) return ORACLE_ERR_ARG;
+  if (gate_row_stride < (int64_t)H * dv) return ORACLE_ERR_ARG;
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int h = 0; h < H; ++h) {
+      const int64_t off = (r * H + h) * (int64_t)dv;
+      const double* gt = gate + r * gate_row_stride + (int64_t)h * dv;
+      double ss = 0.0;
+      for (int j = 0; j < dv; ++j) {
+        const double x = o[off + j] + (residual ? residual[off + j] : 0.0);
+        if (residual_out) residual_out[off + j] = x;
+        ss += x * x;
+      }
+      const double inv = 1.0 / sqrt(ss / (double)dv + eps);
+      for (int j = 0; j < dv; ++j) {
+        const double x = o[off + j] + (residual ? residual[off + j] : 0.0);
+        const double z = x * inv * (w ? w[j] : 1.0) + (b ? b[j] : 0.0);
+        const double sig = 1.0 / (1.0 + exp(-gt[j]));
+        y[off + j] = z * (act == 1 ? gt[j] * sig : sig);
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
 /* Exclusive prefix sum of floor(len_i / every); returns the total, or -1 on
  * a malformed cu_seqlens.  every == 0 means no checkpoints. */
 int64_t kda_oracle_checkpoint_offsets(const int32_t* cu_seqlens, int N, int every,

@@ -427,3 +427,51 @@ def test_multi_token_decode_equals_prefill_with_per_token_checkpoints():
     Sn = (np.eye(dk) - beta[i0, 1] * np.outer(k[i0, 1], k[i0, 1])) @ (
         np.exp(g[i0, 1])[:, None] * S) + beta[i0, 1] * np.outer(k[i0, 1], v[i0, 1])
     np.testing.assert_allclose(ts[0, 0, 1], Sn, atol=1e-12)
+
+
+def test_hand_worked_norm_gate_ex():
+    """Residual + affine weight + bias, both activations, against the values
+    worked by hand in the fixture; the prenorm output is x = o + residual."""
+    gd = _read_golden("norm_gate_ex_example.txt")
+    sh = lambda a: a.reshape(1, 1, -1)
+    for act, key in (("sigmoid", "y_sigmoid"), ("silu", "y_silu")):
+        y, x = oracle.norm_gate_ex(sh(gd["o"]), sh(gd["gate"]), residual=sh(gd["residual"]),
+                                   w=gd["w"], b=gd["b"], eps=gd["eps"][0], gate_act=act)
+        np.testing.assert_allclose(y[0, 0], gd[key], atol=1e-12)
+        np.testing.assert_allclose(x[0, 0], gd["x"], atol=0)
+
+
+def test_norm_gate_ex_reductions():
+    """Special cases that pin each option of the variant entry: no residual,
+    unit weight and zero bias reduce to the plain norm-gate; no weight equals
+    unit weight; the bias enters as b * act(gate); a packed gate row (stride
+    > H*dv, heads at their offsets) equals the contiguous gate; the residual
+    path equals the plain norm-gate of o + residual."""
+    rng = np.random.default_rng(31)
+    rows, H, dv = 5, 3, 8
+    o = rng.standard_normal((rows, H, dv))
+    res = rng.standard_normal((rows, H, dv))
+    gate = rng.standard_normal((rows, H, dv))
+    w = 1 + 0.1 * rng.standard_normal(dv)
+    b = 0.3 * rng.standard_normal(dv)
+    for act in ("sigmoid", "silu"):
+        ref = oracle.norm_gate(o, gate, w, eps=1e-6, gate_act=act)
+        y, x = oracle.norm_gate_ex(o, gate, w=w, gate_act=act)
+        np.testing.assert_allclose(y, ref, atol=1e-14)
+        np.testing.assert_array_equal(x, o)
+        y1, _ = oracle.norm_gate_ex(o, gate, w=np.ones(dv), gate_act=act)
+        y0, _ = oracle.norm_gate_ex(o, gate, gate_act=act)
+        np.testing.assert_allclose(y0, y1, atol=1e-14)
+        yb, _ = oracle.norm_gate_ex(o, gate, w=w, b=b, gate_act=act)
+        sig = 1 / (1 + np.exp(-gate))
+        a = sig if act == "sigmoid" else gate * sig
+        np.testing.assert_allclose(yb - ref, b * a, atol=1e-13)
+        packed = rng.standard_normal((rows, H * dv + 40))
+        packed[:, 16:16 + H * dv] = gate.reshape(rows, -1)
+        yp, _ = oracle.norm_gate_ex(o, packed[:, 16:].copy(), w=w, gate_act=act,
+                                    gate_row_stride=H * dv + 24)
+        np.testing.assert_allclose(yp, ref, atol=1e-14)
+        yr, xr = oracle.norm_gate_ex(o, gate, residual=res, w=w, gate_act=act)
+        np.testing.assert_allclose(xr, o + res, atol=1e-15)
+        np.testing.assert_allclose(yr, oracle.norm_gate(o + res, gate, w, eps=1e-6, gate_act=act),
+                                   atol=1e-14)
