@@ -60,7 +60,10 @@ typedef enum {
   KDA_ERR_CUDA = -4         /* a CUDA launch or attribute call failed */
 } kda_status;
 
-typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+/* Element types.  KDA_F16 is accepted by kda_norm_gate_ex only (the pages'
+ * norm-gate coverage names fp16 and bf16); the recurrence entry points take
+ * KDA_F32 and KDA_BF16. */
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1, KDA_F16 = 2 } kda_dtype;
 
 /* Activation of the output gate in the RMSNorm-gate: sigmoid(x) or SiLU,
  * x * sigmoid(x) (the two activations the pages' norm-gate coverage names). */
@@ -210,6 +213,28 @@ KDA_API kda_status kda_commit_accepted(const void* token_states, const int32_t* 
 KDA_API kda_status kda_norm_gate(const void* o, const void* gate, const void* w, float eps,
                          kda_gate_act gate_act, void* y, int64_t rows, int H, int dv,
                          kda_dtype dtype, void* stream);
+
+/*
+ * Norm-gate variants, the coverage list of "[Feature][KDA] ..." (testing
+ * section: fp16/bf16, sigmoid/SiLU, packed gate strides, affine and
+ * residual/prenorm paths).  Per token row t and head h, over the dv values:
+ *     x = o + residual                                  (residual may be NULL)
+ *     residual_out = x                                  (the prenorm output; may be NULL)
+ *     y = (x / sqrt(mean(x^2) + eps) * w + b) * act(gate)
+ * w and b are [dv] (NULL: w = 1, b = 0).  o, residual, residual_out and y are
+ * [rows, H, dv]; the gate of (t, h) is the dv values at
+ * gate + t * gate_row_stride + h * dv (gate_row_stride in elements, a
+ * multiple of 4 and >= H * dv; 0 means H * dv), so a gate that is a slice of
+ * a packed projection output can be used without a copy.  Every tensor is in
+ * `dtype` (f32, bf16 or f16); x is formed and normalised in fp32 and rounded
+ * to dtype at the stores.  y may alias o or residual, residual_out may alias
+ * o or residual; y and residual_out must differ.  Inputs not aliased by an
+ * output are preserved.
+ */
+KDA_API kda_status kda_norm_gate_ex(const void* o, const void* residual, void* residual_out,
+                            const void* gate, int64_t gate_row_stride, const void* w,
+                            const void* b, float eps, kda_gate_act gate_act, void* y, int64_t rows,
+                            int H, int dv, kda_dtype dtype, void* stream);
 
 /*
  * Chunked prefill without caller scratch.  The pages have no counterpart of

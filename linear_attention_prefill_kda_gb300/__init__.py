@@ -19,14 +19,14 @@ __all__ = [
     "kda_prefill_chunked", "kda_prefill_workspace_bytes", "kda_decode_step", "kda_norm_gate",
     "kda_status_string", "kda_version", "DEV_STATUS", "prefill_launches",
     "kda_prefill_chunked_static_scratch", "STATIC_SCRATCH_BYTES", "kda_decode_multi",
-    "kda_commit_accepted",
+    "kda_commit_accepted", "kda_norm_gate_ex", "KDA_F16",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libkda.so")
 _lib = None
 
-KDA_OK, KDA_F32, KDA_BF16 = 0, 0, 1
+KDA_OK, KDA_F32, KDA_BF16, KDA_F16 = 0, 0, 1, 2
 GATE_ACT = {"sigmoid": 0, "silu": 1}  # kda_gate_act
 STATIC_SCRATCH_BYTES = 128 << 20  # KDA_STATIC_SCRATCH_BYTES in include/kda.h
 DEV_STATUS = {0: "ok", 1: "bad state index", 2: "bad cu_seqlens", 3: "on-chip wait timeout",
@@ -52,6 +52,8 @@ _SIGNATURES = {
     "kda_commit_accepted": (ctypes.c_int, [
         _P, _P, _P, ctypes.c_int, ctypes.c_int, _P, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, _P, _P]),
+    "kda_norm_gate_ex": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _P, _F32, ctypes.c_int, _P, _I64,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]),
     "kda_norm_gate": (ctypes.c_int, [_P, _P, _P, _F32, ctypes.c_int, _P, _I64, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int, _P]),
     "kda_prefill_chunked_static_scratch": (ctypes.c_int, [
@@ -100,6 +102,8 @@ def _dtype(t: torch.Tensor) -> int:
         return KDA_F32
     if t.dtype == torch.bfloat16:
         return KDA_BF16
+    if t.dtype == torch.float16:
+        return KDA_F16
     raise ValueError(f"unsupported dtype {t.dtype}")
 
 
@@ -219,6 +223,24 @@ def kda_commit_accepted(token_states, num_accepted, state_indices, state_pool, *
         _ptr(token_states), _ptr(num_accepted), _ptr(state_indices), N, K, _ptr(state_pool),
         state_pool.shape[0], _dtype(state_pool), H, dk, dv, _ptr(dev_status), _stream(stream))
     _check(st, "kda_commit_accepted")
+
+
+def kda_norm_gate_ex(o, gate, y, *, residual=None, residual_out=None, w=None, b=None,
+                     eps: float = 1e-6, gate_act: str = "sigmoid", stream=None):
+    """Norm-gate variants (see ``include/kda.h``): o, residual, residual_out, y
+    are contiguous [rows, H, dv]; ``gate`` is a [rows, H, dv] tensor whose heads
+    and values are contiguous and whose token rows may be further apart (a
+    slice of a packed projection output): its row stride is passed as
+    gate_row_stride."""
+    rows, H, dv = o.shape
+    if tuple(gate.shape) != (rows, H, dv) or gate.stride(2) != 1 or gate.stride(1) != dv:
+        raise ValueError("gate must be [rows, H, dv] with contiguous heads and values")
+    gptr = ctypes.c_void_p(gate.data_ptr()) if gate.numel() > 0 else None
+    st = load().kda_norm_gate_ex(_ptr(o), _ptr(residual), _ptr(residual_out), gptr,
+                                 int(gate.stride(0)) if rows > 1 else 0, _ptr(w), _ptr(b),
+                                 float(eps), GATE_ACT[gate_act], _ptr(y), rows, H, dv, _dtype(o),
+                                 _stream(stream))
+    _check(st, "kda_norm_gate_ex")
 
 
 def kda_norm_gate(o, gate, w, y, *, eps: float = 1e-6, gate_act: str = "sigmoid", stream=None):

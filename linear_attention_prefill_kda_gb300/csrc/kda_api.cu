@@ -25,7 +25,7 @@ kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR
 
 extern "C" {
 
-int kda_version(void) { return 102; }
+int kda_version(void) { return 103; }
 
 const char* kda_status_string(kda_status s) {
   switch (s) {
@@ -200,6 +200,30 @@ kda_status kda_commit_accepted(const void* token_states, const int32_t* num_acce
   p.N = N; p.K = K; p.H = H; p.dk = dk; p.dv = dv;
   p.state_dtype = state_dtype;
   return from_cuda(kda::launch_commit(p, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_norm_gate_ex(const void* o, const void* residual, void* residual_out,
+                            const void* gate, int64_t gate_row_stride, const void* w,
+                            const void* b, float eps, kda_gate_act gate_act, void* y, int64_t rows,
+                            int H, int dv, kda_dtype dtype, void* stream) {
+  if (rows < 0 || H <= 0 || !act_ok(gate_act) || !(eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+  if (dtype != KDA_F32 && dtype != KDA_BF16 && dtype != KDA_F16) return KDA_ERR_UNSUPPORTED;
+  if (!dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+  const int64_t row_elems = (int64_t)H * dv;
+  if (gate_row_stride == 0) gate_row_stride = row_elems;
+  if (gate_row_stride < row_elems || gate_row_stride % 4 != 0) return KDA_ERR_INVALID_ARG;
+  if (rows == 0) return KDA_OK;
+  if ((rows * H + 7) / 8 > INT32_MAX) return KDA_ERR_INVALID_ARG;
+  if (!ptr_ok(o, true) || !ptr_ok(gate, true) || !ptr_ok(y, true) || !ptr_ok(residual, false) ||
+      !ptr_ok(residual_out, false) || !ptr_ok(w, false) || !ptr_ok(b, false))
+    return KDA_ERR_INVALID_ARG;
+  if (residual_out && residual_out == y) return KDA_ERR_INVALID_ARG;
+  kda::NormGateExParams p{};
+  p.o = o; p.residual = residual; p.gate = gate; p.w = w; p.b = b;
+  p.y = y; p.residual_out = residual_out;
+  p.rows = rows; p.gate_row_stride = gate_row_stride;
+  p.H = H; p.dv = dv; p.eps = eps; p.dtype = dtype; p.gate_act = gate_act;
+  return from_cuda(kda::launch_norm_gate_ex(p, static_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_norm_gate(const void* o, const void* gate, const void* w, float eps,

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -11,6 +12,7 @@
 namespace kda {
 
 using bf16 = __nv_bfloat16;
+using f16 = __half;
 
 template <typename T>
 __device__ __forceinline__ float to_f32(T x);
@@ -18,6 +20,8 @@ template <>
 __device__ __forceinline__ float to_f32<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_f32<bf16>(bf16 x) { return __bfloat162float(x); }
+template <>
+__device__ __forceinline__ float to_f32<f16>(f16 x) { return __half2float(x); }
 
 template <typename T>
 __device__ __forceinline__ T from_f32(float x);
@@ -34,6 +38,20 @@ __device__ __forceinline__ float4 load4(const bf16* p) {
   __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
   float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
   return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+__device__ __forceinline__ float4 load4(const f16* p) {
+  uint2 raw = *reinterpret_cast<const uint2*>(p);
+  const float2 fa = __half22float2(*reinterpret_cast<__half2*>(&raw.x));
+  const float2 fb = __half22float2(*reinterpret_cast<__half2*>(&raw.y));
+  return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+__device__ __forceinline__ void store4(f16* p, float4 v) {
+  __half2 a = __floats2half2_rn(v.x, v.y);
+  __half2 b = __floats2half2_rn(v.z, v.w);
+  uint2 raw;
+  raw.x = *reinterpret_cast<uint32_t*>(&a);
+  raw.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = raw;
 }
 __device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 __device__ __forceinline__ void store4(bf16* p, float4 v) {

@@ -62,6 +62,16 @@ struct NormGateParams {
   int gate_act;     // kda_gate_act
 };
 
+struct NormGateExParams {
+  const void *o, *residual, *gate, *w, *b;  // residual, w, b may be NULL
+  void *y, *residual_out;                   // residual_out may be NULL
+  int64_t rows, gate_row_stride;            // gate row stride in elements
+  int H, dv;
+  float eps;
+  kda_dtype dtype;
+  int gate_act;
+};
+
 struct PrefillParams {
   const void *q, *k, *v, *g, *beta;
   const int32_t* cu_seqlens;
@@ -92,6 +102,7 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_multi(const DecodeMultiParams& p, cudaStream_t stream);
 cudaError_t launch_commit(const CommitParams& p, cudaStream_t stream);
 cudaError_t launch_norm_gate(const NormGateParams& p, cudaStream_t stream);
+cudaError_t launch_norm_gate_ex(const NormGateExParams& p, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
 // Upper bound over every option (what kda_prefill_workspace_bytes reports).
 size_t prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk);

@@ -3,9 +3,9 @@ the same inputs, and the tolerance rule.
 
 Tolerance rule.  The bound is max-abs 0.01 when the state is fp32 and 0.03
 when it is bf16 (the FlashKDA checkpoint test's tolerances).  Values the ABI
-stores in bf16 (outputs with bf16 inputs, bf16 states) carry an unavoidable
-final rounding of half a bf16 ulp; that rounding is allowed on top of the
-bound: |gpu - oracle| <= tol + ulp_half(oracle).
+stores in bf16 or fp16 (outputs with 16-bit inputs, bf16 states) carry an
+unavoidable final rounding of half an ulp; that rounding is allowed on top of
+the bound: |gpu - oracle| <= tol + ulp_half(oracle).
 """
 from __future__ import annotations
 
@@ -18,11 +18,16 @@ def tol_for(state_dtype) -> float:
 
 
 def half_ulp(ref: np.ndarray, dtype) -> np.ndarray:
-    if dtype != torch.bfloat16:
+    """Half a unit in the last place of ref in the stored dtype (bf16: 8
+    significant bits, fp16: 11; fp32 results get no allowance)."""
+    bits = {torch.bfloat16: 8, torch.float16: 11}.get(dtype)
+    if bits is None:
         return np.zeros_like(ref)
     a = np.abs(ref)
     e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    return np.where(a > 0, 2.0 ** (e - 8), 0.0)
+    if dtype == torch.float16:
+        e = np.maximum(e, -14.0)  # subnormal spacing
+    return np.where(a > 0, 2.0 ** (e - bits), 0.0)
 
 
 def excess_error(gpu: torch.Tensor, ref: np.ndarray) -> float:

@@ -150,6 +150,28 @@ def test_norm_gate_rejects(lib, args, expect):
     assert lib.kda_norm_gate(*args, None) == expect
 
 
+def _ngx(lib, **over):
+    a = dict(o=FAKE, res=None, rout=None, gate=FAKE, gstride=0, w=None, b=None, eps=1e-6, act=0,
+             y=FAKE, rows=10, H=4, dv=128, dt=2)
+    a.update(over)
+    return lib.kda_norm_gate_ex(a["o"], a["res"], a["rout"], a["gate"], a["gstride"], a["w"], a["b"],
+                                a["eps"], a["act"], a["y"], a["rows"], a["H"], a["dv"], a["dt"], None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dv=48), -2), (dict(dt=3), -2), (dict(rows=-1), -1), (dict(H=0), -1), (dict(act=2), -1),
+    (dict(eps=-1.0), -1), (dict(gstride=4 * 128 - 4), -1), (dict(gstride=4 * 128 + 2), -1),
+    (dict(o=None), -1), (dict(gate=None), -1), (dict(y=MIS), -1), (dict(res=MIS), -1),
+    (dict(rout=FAKE, y=FAKE), -1),
+])
+def test_norm_gate_ex_rejects(lib, over, expect):
+    assert _ngx(lib, **over) == expect
+
+
+def test_norm_gate_ex_empty_is_noop(lib):
+    assert _ngx(lib, rows=0, o=None, gate=None, y=None) == 0
+
+
 def test_workspace_query(lib):
     assert kda.kda_prefill_workspace_bytes(8, 4096, 32, 128, 128, 64) >= 0
     assert lib.kda_prefill_workspace_bytes(-1, 10, 2, 64, 64, 64) == 0

@@ -363,6 +363,52 @@ def test_decode_multi_full_width(kda_gpu):
 
 
 @pytest.mark.parametrize("dv", [16, 64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("variant", ["residual_prenorm", "bias_no_weight", "packed_gate",
+                                     "in_place"])
+def test_norm_gate_variants(kda_gpu, dv, dtype, variant):
+    """The norm-gate variants against the oracle: residual with prenorm output,
+    bias without weight (SiLU), a gate read from a packed projection row, and
+    in-place outputs (y over o, prenorm over residual)."""
+    gen = torch.Generator().manual_seed(500 + dv)
+    rows, H = 29, 3
+    mk = lambda *sh: torch.randn(*sh, generator=gen).to(dtype)
+    o, res, gate = mk(rows, H, dv), mk(rows, H, dv), mk(rows, H, dv)
+    w = (1 + 0.05 * torch.randn(dv, generator=gen)).to(dtype)
+    b = (0.2 * torch.randn(dv, generator=gen)).to(dtype)
+    act = "silu" if variant == "bias_no_weight" else "sigmoid"
+    use_res = variant in ("residual_prenorm", "in_place")
+    use_w = variant != "bias_no_weight"
+    use_b = variant in ("bias_no_weight", "residual_prenorm")
+    if variant == "packed_gate":
+        packed = mk(rows, H * dv + 32)
+        packed[:, 16:16 + H * dv] = gate.reshape(rows, -1)
+        dpacked = packed.to(DEV)
+        dgate = dpacked[:, 16:16 + H * dv].view(rows, H, dv)
+    else:
+        dgate = gate.to(DEV)
+    y_ref, x_ref = oracle.norm_gate_ex(o, gate, residual=res if use_res else None,
+                                       w=w if use_w else None, b=b if use_b else None, eps=1e-6,
+                                       gate_act=act)
+    od, rd = o.to(DEV), res.to(DEV)
+    y = od if variant == "in_place" else torch.empty_like(od)
+    rout = rd if variant == "in_place" else (torch.empty_like(od) if use_res else None)
+    kda_gpu.kda_norm_gate_ex(od, dgate, y, residual=rd if use_res else None, residual_out=rout,
+                             w=w.to(DEV) if use_w else None, b=b.to(DEV) if use_b else None,
+                             eps=1e-6, gate_act=act)
+    torch.cuda.synchronize()
+    tol = 1e-5 if dtype == torch.float32 else 1e-3
+    assert excess_error(y, y_ref) <= tol
+    if rout is not None:
+        assert excess_error(rout, x_ref) <= tol
+    if variant != "in_place":
+        assert torch.equal(od.cpu(), o)  # inputs preserved
+        assert torch.equal(rd.cpu(), res)
+    if variant == "packed_gate":
+        assert torch.equal(dpacked.cpu(), packed)  # the rest of the packed row untouched
+
+
+@pytest.mark.parametrize("dv", [16, 64, 128])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("inplace", [False, True])
 @pytest.mark.parametrize("act", ["sigmoid", "silu"])
