@@ -67,6 +67,9 @@ def _load():
             lib.kda_oracle_norm_gate_ex.argtypes = [P, P, P, ctypes.c_int64, P, P, ctypes.c_double,
                                                     ctypes.c_int, P, P, ctypes.c_int64, ctypes.c_int,
                                                     ctypes.c_int]
+            lib.kda_oracle_conv_prefill.restype = ctypes.c_int
+            lib.kda_oracle_conv_prefill.argtypes = [P, P, P, P, ctypes.c_int, P, P, P, ctypes.c_int64,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
             lib.kda_oracle_checkpoint_offsets.restype = ctypes.c_int64
             lib.kda_oracle_checkpoint_offsets.argtypes = [P, ctypes.c_int, ctypes.c_int, P]
             lib.kda_oracle_max_threads.restype = ctypes.c_int
@@ -240,3 +243,34 @@ def norm_gate_ex(o, gate, *, residual=None, w=None, b=None, eps=1e-6, gate_act="
                                            _ptr(b), float(eps), ACT[gate_act], _ptr(y), _ptr(res_out),
                                            rows, H, dv))
     return y, res_out
+
+
+CONV_ACT = {"none": 0, "silu": 1}
+
+
+def conv_prefill(x, w, cu_seqlens, state_indices, pool, *, bias=None, has_initial_state=None,
+                 act="silu"):
+    """Short causal convolution over packed sequences ("[Feature][KDA] Add Kimi
+    K3 KDA execution", "KDA execution" step 2).  x [T, C]; w [C, W]; bias [C];
+    pool [slots, W-1, C].  Returns ``(y [T, C], pool_after)``; the input pool is
+    not modified."""
+    x, w, bias = _f64(x), _f64(w), _f64(bias)
+    pool = _f64(pool).copy()
+    cu, idx = _i32(cu_seqlens), _i32(state_indices)
+    his = None if has_initial_state is None else _i32(has_initial_state)
+    T, C = x.shape
+    W = w.shape[1]
+    y = np.zeros((T, C), np.float64)
+    _check(_load().kda_oracle_conv_prefill(_ptr(x), _ptr(w), _ptr(bias), _ptr(cu), len(idx), _ptr(idx),
+                                           _ptr(his), _ptr(pool), pool.shape[0], C, W,
+                                           CONV_ACT[act], _ptr(y)))
+    return y, pool
+
+
+def conv_decode(x, w, state_indices, pool, *, bias=None, act="silu"):
+    """One token per sequence: the prefill of a length-1 segment per sequence
+    (the cache supplies the W-1 earlier inputs).  x [N, C]."""
+    x = _f64(x)
+    N = x.shape[0]
+    cu = np.arange(N + 1, dtype=np.int32)
+    return conv_prefill(x, w, cu, state_indices, pool, bias=bias, act=act)

@@ -152,6 +152,59 @@ int kda_oracle_norm_gate_ex(const double* o, const double* residual, const doubl
   return ORACLE_OK;
 }
 
+/*
+ * Short causal convolution ahead of the recurrence ("[Feature][KDA] Add Kimi
+ * K3 KDA execution", section "KDA execution", step 2: run the causal
+ * convolution and update its cache).  Depthwise over `channels`, width W, on
+ * each sequence's tokens extended on the left by the W-1 cached inputs (zero
+ * when the sequence has no initial state):
+ *   y[t, c] = act(bias[c] + sum_{i<W} w[c, i] * xe[t - (W-1) + i, c])
+ * act = identity (0) or SiLU (1).  The cache of a sequence afterwards holds
+ * its last W-1 extended inputs, oldest first: cache[j, c] = xe[t1 - (W-1) + j, c].
+ * x, y: [T, channels]; w: [channels, W]; bias: [channels] or NULL; cache pool:
+ * [num_slots, W-1, channels], updated in place.  A padding sequence (index -1)
+ * gets zero outputs and leaves the pool alone.
+ */
+int kda_oracle_conv_prefill(const double* x, const double* w, const double* bias,
+                            const int32_t* cu_seqlens, int N, const int32_t* state_indices,
+                            const int32_t* has_initial_state, double* pool, int64_t num_slots,
+                            int channels, int W, int act, double* y) {
+  if (!x || !w || !cu_seqlens || !state_indices || !pool || !y || N < 0 || channels <= 0 || W < 1 ||
+      act < 0 || act > 1)
+    return ORACLE_ERR_ARG;
+  const int Wm = W - 1;
+  for (int i = 0; i < N; ++i) {
+    const int64_t t0 = cu_seqlens[i], t1 = cu_seqlens[i + 1];
+    if (t1 < t0) return ORACLE_ERR_ARG;
+    const int32_t slot = state_indices[i];
+    if (slot < 0) {
+      for (int64_t t = t0; t < t1; ++t)
+        for (int c = 0; c < channels; ++c) y[t * channels + c] = 0.0;
+      continue;
+    }
+    if (slot >= num_slots) return ORACLE_ERR_ARG;
+    if (t1 == t0) continue;
+    double* cache = pool + (int64_t)slot * Wm * channels;
+    const int init = has_initial_state ? has_initial_state[i] != 0 : 1;
+    const int64_t len = t1 - t0;
+    for (int c = 0; c < channels; ++c) {
+      /* the extended sequence xe[0 .. Wm + len) for this channel */
+      double* xe = (double*)malloc(sizeof(double) * (size_t)(Wm + len));
+      if (!xe) return ORACLE_ERR_ARG;
+      for (int j = 0; j < Wm; ++j) xe[j] = init ? cache[(int64_t)j * channels + c] : 0.0;
+      for (int64_t t = 0; t < len; ++t) xe[Wm + t] = x[(t0 + t) * channels + c];
+      for (int64_t t = 0; t < len; ++t) {
+        double acc = bias ? bias[c] : 0.0;
+        for (int k = 0; k < W; ++k) acc += w[(int64_t)c * W + k] * xe[t + k];
+        y[(t0 + t) * channels + c] = act == 1 ? acc / (1.0 + exp(-acc)) : acc;
+      }
+      for (int j = 0; j < Wm; ++j) cache[(int64_t)j * channels + c] = xe[len + j];
+      free(xe);
+    }
+  }
+  return ORACLE_OK;
+}
+
 /* Exclusive prefix sum of floor(len_i / every); returns the total, or -1 on
  * a malformed cu_seqlens.  every == 0 means no checkpoints. */
 int64_t kda_oracle_checkpoint_offsets(const int32_t* cu_seqlens, int N, int every,

@@ -475,3 +475,80 @@ def test_norm_gate_ex_reductions():
         np.testing.assert_allclose(xr, o + res, atol=1e-15)
         np.testing.assert_allclose(yr, oracle.norm_gate(o + res, gate, w, eps=1e-6, gate_act=act),
                                    atol=1e-14)
+
+
+# ------------------------------------------------------------ short causal conv
+def test_hand_worked_conv():
+    gd = _read_golden("conv_example.txt")
+    x = gd["x"].reshape(-1, 1)
+    pool = gd["cache"].reshape(1, 2, 1)
+    cu, idx = np.array([0, len(x)], np.int32), np.array([0], np.int32)
+    y, p = oracle.conv_prefill(x, gd["w"].reshape(1, 3), cu, idx, pool, act="none")
+    np.testing.assert_allclose(y[:, 0], gd["y"], atol=0)
+    np.testing.assert_allclose(p[0, :, 0], gd["cache_after"], atol=0)
+    ys, _ = oracle.conv_prefill(x, gd["w"].reshape(1, 3), cu, idx, pool, act="silu")
+    np.testing.assert_allclose(ys[2, 0], gd["silu_y2"][0], atol=1e-13)
+
+
+def _conv_inputs(rng, lens, C, W, slots=9):
+    T = sum(lens)
+    x = rng.standard_normal((T, C))
+    w = rng.standard_normal((C, W))
+    b = rng.standard_normal(C)
+    pool = rng.standard_normal((slots, W - 1, C))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    return x, w, b, pool, cu
+
+
+@pytest.mark.parametrize("W", [1, 2, 4])
+def test_conv_matches_numpy_convolve(W):
+    """Each channel of each sequence is numpy's full convolution of the
+    extended sequence (cache then inputs) with the reversed taps, shifted so
+    that only past and current inputs enter."""
+    rng = np.random.default_rng(40 + W)
+    lens, C = [7, 1, 0, 12], 5
+    x, w, b, pool, cu = _conv_inputs(rng, lens, C, W)
+    idx = np.array([3, 0, 5, 8], np.int32)
+    y, p = oracle.conv_prefill(x, w, cu, idx, pool, bias=b, act="none")
+    for i, L in enumerate(lens):
+        if L == 0:
+            continue
+        for c in range(C):
+            xe = np.concatenate([pool[idx[i], :, c], x[cu[i]:cu[i + 1], c]])
+            full = np.convolve(xe, w[c, ::-1])       # full[n] = sum_k w[c, W-1-k'] ...
+            ref = full[W - 1:W - 1 + L] + b[c]        # outputs aligned to the current input
+            np.testing.assert_allclose(y[cu[i]:cu[i + 1], c], ref, atol=1e-12)
+            if W > 1:
+                np.testing.assert_allclose(p[idx[i], :, c], xe[-(W - 1):], atol=0)
+    np.testing.assert_array_equal(p[5], pool[5])  # the empty sequence leaves its slot
+
+
+def test_conv_split_decode_and_flags():
+    """Two calls carrying the cache through the pool equal one call; K decode
+    steps equal the prefill of those K tokens; a sequence without initial
+    state equals one whose cache is zero; padding rows are zero and leave the
+    pool alone; SiLU is applied to the pre-activation."""
+    rng = np.random.default_rng(77)
+    C, W = 6, 4
+    x, w, b, pool, cu = _conv_inputs(rng, [11], C, W)
+    idx = np.array([2], np.int32)
+    y, p = oracle.conv_prefill(x, w, cu, idx, pool, bias=b)
+    y1, p1 = oracle.conv_prefill(x[:5], w, np.array([0, 5], np.int32), idx, pool, bias=b)
+    y2, p2 = oracle.conv_prefill(x[5:], w, np.array([0, 6], np.int32), idx, p1, bias=b)
+    np.testing.assert_allclose(np.concatenate([y1, y2]), y, atol=1e-13)
+    np.testing.assert_allclose(p2, p, atol=0)
+    pd, ys = pool, []
+    for t in range(11):
+        yt, pd = oracle.conv_decode(x[t:t + 1], w, idx, pd, bias=b)
+        ys.append(yt[0])
+    np.testing.assert_allclose(np.array(ys), y, atol=1e-13)
+    np.testing.assert_allclose(pd, p, atol=0)
+    zeroed = pool.copy()
+    zeroed[2] = 0
+    yz, _ = oracle.conv_prefill(x, w, cu, idx, zeroed, bias=b)
+    yf, _ = oracle.conv_prefill(x, w, cu, idx, pool, bias=b, has_initial_state=np.array([0], np.int32))
+    np.testing.assert_allclose(yf, yz, atol=0)
+    yp, pp = oracle.conv_prefill(x, w, cu, np.array([-1], np.int32), pool, bias=b)
+    assert np.all(yp == 0) and np.array_equal(pp, pool)
+    ya, _ = oracle.conv_prefill(x, w, cu, idx, pool, bias=b, act="none")
+    np.testing.assert_allclose(y, ya / (1 + np.exp(-ya)), atol=1e-14)
