@@ -8,11 +8,13 @@ Workloads (seeded synthetic inputs, no dataset):
            1024-slot pool, fused RMSNorm-gate.
   spec     the decode batch verifying 4 draft tokens per sequence (per-token
            states kept) followed by the commit of the accepted prefixes.
-A step is one prefill call, one decode step and one verify + commit; each is
-timed in its own loop with CUDA events on the launching stream, the L2 flushed (a 256 MiB
+  conv     the short causal convolution (width 4, SiLU) over the scheduler
+           step's q, k, v projections (12288 channels), with its cache pool.
+A step is one prefill call, one decode step, one verify + commit and one
+convolution call; each is timed in its own loop with CUDA events on the launching stream, the L2 flushed (a 256 MiB
 write) before every timed prefill call (the decode step streams 1.07 GB, far
 above L2).  ``value`` is prefill tokens/s; the decode and verification
-figures sit under ``decode`` and ``spec_decode``.  ``--impl reference`` times the fp64 CPU oracle on the same
+figures sit under ``decode``, ``spec_decode`` and ``conv_prefill``.  ``--impl reference`` times the fp64 CPU oracle on the same
 workload instead.  Under torchrun each rank runs an independent replica (the
 path has no exchange step) and rank 0 reports the aggregate.
 """
@@ -214,6 +216,13 @@ def spec_algorithmic(w, K, num_accepted):
     return int(b)
 
 
+def conv_algorithmic(w, C, Wd):
+    """Bytes of one short-convolution call: x read and y written once, taps and
+    bias, and each sequence's cache read and written."""
+    n_seq = sum(1 for L in w.seqlens if L > 0)
+    return int(2 * w.T * C * 2 + C * (Wd + 1) * 2 + 2 * n_seq * (Wd - 1) * C * 2)
+
+
 # ----------------------------------------------------------------- GPU arm
 def run_gpu(args):
     import linear_attention_prefill_kda_gb300 as kda
@@ -267,6 +276,21 @@ def run_gpu(args):
         sout = torch.empty(dw.N, SPEC_K, dw.H, dw.dv, device=dev, dtype=dw.in_dtype)
         sts = torch.empty(dw.N, SPEC_K, dw.H, dw.dk, dw.dv, device=dev, dtype=dw.state_dtype)
 
+    with_conv = args.workload in ("both", "conv")
+    CONV_C, CONV_W = 3 * w.H * w.dk, 4  # q, k, v projections of the scheduler step
+    if with_conv:
+        cdat = W.make_conv(w.seqlens, CONV_C, CONV_W, torch.bfloat16, num_slots=w.num_slots,
+                           seed=17)
+        cdev = {k: v.to(dev) for k, v in cdat.items()}
+        cy = torch.empty_like(cdev["x"])
+
+    def conv_call():
+        if not with_conv:
+            return
+        kda.kda_causal_conv1d_prefill(cdev["x"], cdev["w"], cdev["cu_seqlens"],
+                                      cdev["state_indices"], cdev["pool"], cy, bias=cdev["b"],
+                                      act="silu", dev_status=status, stream=stream)
+
     def spec_call():
         if not with_spec:
             return
@@ -301,6 +325,7 @@ def run_gpu(args):
             prefill_call()
         decode_call(0)
         spec_call()
+        conv_call()
     barrier()
 
     with ClockSampler(local) as clk:
@@ -333,6 +358,19 @@ def run_gpu(args):
         e3.record(stream)
         barrier()
         spec_ms_total = e2.elapsed_time(e3)
+        # short causal convolution over the scheduler step's q, k, v projections,
+        # L2 flushed before each call (the 100 MB input is about L2's size)
+        cstarts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        cends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier()
+        for i in range(args.steps if with_conv else 0):
+            flush.fill_(float(i))
+            cstarts[i].record(stream)
+            conv_call()
+            cends[i].record(stream)
+        barrier()
+        conv_ms = (sum(a.elapsed_time(b) for a, b in zip(cstarts, cends)) / args.steps
+                   if with_conv else float("nan"))
     clocks = clk.summary()
     st = int(status.item())
     if st != 0:
@@ -341,7 +379,8 @@ def run_gpu(args):
     pre_ms_mean = sum(pre_ms) / len(pre_ms)
     dec_ms = dec_ms_total / args.steps
     spec_ms = spec_ms_total / args.steps if with_spec else float("nan")
-    pre_ms_mean, dec_ms, spec_ms = max_over_ranks([pre_ms_mean, dec_ms, spec_ms], dev)
+    pre_ms_mean, dec_ms, spec_ms, conv_ms = max_over_ranks([pre_ms_mean, dec_ms, spec_ms, conv_ms],
+                                                          dev)
 
     # ---------------- e2e through the public API with host buffers
     names = ["q", "k", "v", "g", "beta", "gate"]
@@ -382,6 +421,8 @@ def run_gpu(args):
     pre_tflops = rate(pre_flops, pre_ms_mean) / 1e12
     spec_bytes = spec_algorithmic(dw, SPEC_K, sacc_host) if with_spec else 0
     spec_gbs = rate(spec_bytes, spec_ms) / 1e9
+    conv_bytes = conv_algorithmic(w, CONV_C, CONV_W) if with_conv else 0
+    conv_gbs = rate(conv_bytes, conv_ms) / 1e9
     tokens_s = replica_rate(T, ws, pre_ms_mean)
     seqsteps_s = replica_rate(dw.N, ws, dec_ms)
     result = {
@@ -426,10 +467,17 @@ def run_gpu(args):
                                      "frac": round(spec_gbs / pk["hbm"], 4),
                                      "traffic": recorded_traffic("spec_step_dram_bytes"),
                                      "algorithmic_bytes": spec_bytes}},
+        "conv_prefill": {"value": round(replica_rate(T, ws, conv_ms), 1), "unit": "tokens/s",
+                         "channels": CONV_C, "width": CONV_W, "ms_per_call": round(conv_ms, 4),
+                         "roofline": {"bound": "hbm", "achieved": round(conv_gbs, 1),
+                                      "peak": pk["hbm"], "unit": "GB/s",
+                                      "frac": round(conv_gbs / pk["hbm"], 4),
+                                      "traffic": recorded_traffic("conv_call_dram_bytes"),
+                                      "algorithmic_bytes": conv_bytes}},
         "e2e": {"value": round(replica_rate(T, ws, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * (prefill_launches(kda, w) * with_prefill + with_decode
-                                      + 2 * with_spec),
+                                      + 2 * with_spec + with_conv),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -533,7 +581,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["libkda", "reference"], default="libkda")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["both", "prefill", "decode", "spec"], default="both",
+    ap.add_argument("--workload", choices=["both", "prefill", "decode", "spec", "conv"],
+                    default="both",
                     help="time every part (default) or one of them (for profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

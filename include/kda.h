@@ -237,6 +237,42 @@ KDA_API kda_status kda_norm_gate_ex(const void* o, const void* residual, void* r
                             int H, int dv, kda_dtype dtype, void* stream);
 
 /*
+ * Short causal convolution with a per-sequence cache, run on the projections
+ * ahead of the recurrence ("[Feature][KDA] Add Kimi K3 KDA execution", section
+ * "KDA execution", step 2: run the causal convolution and update its cache).
+ * Depthwise over `channels` (a multiple of 8) with width W in {2, 3, 4}:
+ *     y[t, c] = act(bias[c] + sum_{i<W} weight[c, i] * xe[t - (W-1) + i, c])
+ * where xe is the sequence extended on the left by the W-1 inputs held in its
+ * cache slot, oldest first (zeros when has_initial_state[i] == 0).  The slot
+ * then holds the sequence's last W-1 extended inputs.  act: identity or SiLU.
+ *  x, y         [T, channels] dtype (f32 or bf16); y must not overlap x.
+ *  weight       [channels, W] dtype;  bias [channels] dtype or NULL.
+ *  cu_seqlens, state_indices, has_initial_state: as for kda_prefill_chunked
+ *               (index -1: padding, zero outputs, cache untouched; an empty
+ *               sequence leaves its cache alone).
+ *  conv_state_pool [num_slots, W-1, channels] dtype, updated in place.
+ * Values are formed in fp32 and rounded to dtype when stored.
+ */
+typedef enum { KDA_CONV_IDENTITY = 0, KDA_CONV_SILU = 1 } kda_conv_act;
+KDA_API kda_status kda_causal_conv1d_prefill(const void* x, const void* weight, const void* bias,
+                                     kda_dtype dtype, const int32_t* cu_seqlens, int N, int64_t T,
+                                     int channels, int width, const int32_t* state_indices,
+                                     const int32_t* has_initial_state, void* conv_state_pool,
+                                     int64_t num_slots, kda_conv_act act, void* y,
+                                     int32_t* dev_status, void* stream);
+
+/*
+ * One token per sequence through the same convolution: x, y [N, channels];
+ * the cache of state_indices[i] supplies the W-1 earlier inputs and is
+ * shifted by one (x appended).  Other arguments as for the prefill.
+ */
+KDA_API kda_status kda_causal_conv1d_decode(const void* x, const void* weight, const void* bias,
+                                    kda_dtype dtype, int N, int channels, int width,
+                                    const int32_t* state_indices, void* conv_state_pool,
+                                    int64_t num_slots, kda_conv_act act, void* y,
+                                    int32_t* dev_status, void* stream);
+
+/*
  * Chunked prefill without caller scratch.  The pages have no counterpart of
  * this entry point; it serves callers that cannot allocate device memory where
  * they run the prefill (for example code running under strict-mode stream

@@ -19,7 +19,8 @@ __all__ = [
     "kda_prefill_chunked", "kda_prefill_workspace_bytes", "kda_decode_step", "kda_norm_gate",
     "kda_status_string", "kda_version", "DEV_STATUS", "prefill_launches",
     "kda_prefill_chunked_static_scratch", "STATIC_SCRATCH_BYTES", "kda_decode_multi",
-    "kda_commit_accepted", "kda_norm_gate_ex", "KDA_F16",
+    "kda_commit_accepted", "kda_norm_gate_ex", "KDA_F16", "kda_causal_conv1d_prefill",
+    "kda_causal_conv1d_decode",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -52,6 +53,12 @@ _SIGNATURES = {
     "kda_commit_accepted": (ctypes.c_int, [
         _P, _P, _P, ctypes.c_int, ctypes.c_int, _P, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, _P, _P]),
+    "kda_causal_conv1d_prefill": (ctypes.c_int, [
+        _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int, _P, _P, _P,
+        _I64, ctypes.c_int, _P, _P, _P]),
+    "kda_causal_conv1d_decode": (ctypes.c_int, [
+        _P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _I64, ctypes.c_int,
+        _P, _P, _P]),
     "kda_norm_gate_ex": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _P, _F32, ctypes.c_int, _P, _I64,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]),
     "kda_norm_gate": (ctypes.c_int, [_P, _P, _P, _F32, ctypes.c_int, _P, _I64, ctypes.c_int,
@@ -223,6 +230,34 @@ def kda_commit_accepted(token_states, num_accepted, state_indices, state_pool, *
         _ptr(token_states), _ptr(num_accepted), _ptr(state_indices), N, K, _ptr(state_pool),
         state_pool.shape[0], _dtype(state_pool), H, dk, dv, _ptr(dev_status), _stream(stream))
     _check(st, "kda_commit_accepted")
+
+
+CONV_ACT = {"none": 0, "silu": 1}
+
+
+def kda_causal_conv1d_prefill(x, weight, cu_seqlens, state_indices, conv_state_pool, y, *, bias=None,
+                              has_initial_state=None, act: str = "silu", dev_status=None,
+                              stream=None):
+    """Short causal convolution over packed sequences (see ``include/kda.h``):
+    x, y [T, C]; weight [C, W]; conv_state_pool [slots, W-1, C]."""
+    T, C = x.shape
+    N = state_indices.shape[0]
+    st = load().kda_causal_conv1d_prefill(
+        _ptr(x), _ptr(weight), _ptr(bias), _dtype(x), _ptr(cu_seqlens), N, T, C, weight.shape[1],
+        _ptr(state_indices), _ptr(has_initial_state), _ptr(conv_state_pool), conv_state_pool.shape[0],
+        CONV_ACT[act], _ptr(y), _ptr(dev_status), _stream(stream))
+    _check(st, "kda_causal_conv1d_prefill")
+
+
+def kda_causal_conv1d_decode(x, weight, state_indices, conv_state_pool, y, *, bias=None,
+                             act: str = "silu", dev_status=None, stream=None):
+    """One token per sequence through the causal convolution: x, y [N, C]."""
+    N, C = x.shape
+    st = load().kda_causal_conv1d_decode(
+        _ptr(x), _ptr(weight), _ptr(bias), _dtype(x), N, C, weight.shape[1], _ptr(state_indices),
+        _ptr(conv_state_pool), conv_state_pool.shape[0], CONV_ACT[act], _ptr(y), _ptr(dev_status),
+        _stream(stream))
+    _check(st, "kda_causal_conv1d_decode")
 
 
 def kda_norm_gate_ex(o, gate, y, *, residual=None, residual_out=None, w=None, b=None,

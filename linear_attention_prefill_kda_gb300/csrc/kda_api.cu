@@ -25,7 +25,7 @@ kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR
 
 extern "C" {
 
-int kda_version(void) { return 103; }
+int kda_version(void) { return 104; }
 
 const char* kda_status_string(kda_status s) {
   switch (s) {
@@ -224,6 +224,64 @@ kda_status kda_norm_gate_ex(const void* o, const void* residual, void* residual_
   p.rows = rows; p.gate_row_stride = gate_row_stride;
   p.H = H; p.dv = dv; p.eps = eps; p.dtype = dtype; p.gate_act = gate_act;
   return from_cuda(kda::launch_norm_gate_ex(p, static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+kda_status conv_common(const void* weight, const void* bias, kda_dtype dtype, int N, int channels,
+                       int width, const int32_t* state_indices, void* pool, int64_t num_slots,
+                       kda_conv_act act, int32_t* dev_status) {
+  if (N < 0 || channels <= 0 || num_slots <= 0) return KDA_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype)) return KDA_ERR_UNSUPPORTED;
+  if (width < 2 || width > 4 || channels % 8 != 0) return KDA_ERR_UNSUPPORTED;
+  if (act != KDA_CONV_IDENTITY && act != KDA_CONV_SILU) return KDA_ERR_INVALID_ARG;
+  if (!ptr_ok(weight, true) || !ptr_ok(bias, false) || !ptr_ok(state_indices, N > 0) ||
+      !ptr_ok(pool, true) || !ptr_ok(dev_status, false))
+    return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+}  // namespace
+
+kda_status kda_causal_conv1d_prefill(const void* x, const void* weight, const void* bias,
+                                     kda_dtype dtype, const int32_t* cu_seqlens, int N, int64_t T,
+                                     int channels, int width, const int32_t* state_indices,
+                                     const int32_t* has_initial_state, void* conv_state_pool,
+                                     int64_t num_slots, kda_conv_act act, void* y,
+                                     int32_t* dev_status, void* stream) {
+  if (T < 0 || T > INT32_MAX) return KDA_ERR_INVALID_ARG;
+  const kda_status st = conv_common(weight, bias, dtype, N, channels, width, state_indices,
+                                    conv_state_pool, num_slots, act, dev_status);
+  if (st != KDA_OK) return st;
+  if (T / 64 + N > 65535) return KDA_ERR_INVALID_ARG;  // tile slots form the grid's y extent
+  if (!ptr_ok(cu_seqlens, true) || !ptr_ok(x, T > 0) || !ptr_ok(y, T > 0) ||
+      !ptr_ok(has_initial_state, false))
+    return KDA_ERR_INVALID_ARG;
+  if (N == 0 || T == 0) return KDA_OK;
+  kda::ConvParams p{};
+  p.x = x; p.w = weight; p.bias = bias; p.y = y;
+  p.cu_seqlens = cu_seqlens; p.state_indices = state_indices; p.has_initial_state = has_initial_state;
+  p.pool = conv_state_pool; p.dev_status = dev_status;
+  p.T = T; p.num_slots = num_slots; p.N = N; p.C = channels; p.W = width; p.act = act;
+  p.dtype = dtype;
+  return from_cuda(kda::launch_conv_prefill(p, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_causal_conv1d_decode(const void* x, const void* weight, const void* bias,
+                                    kda_dtype dtype, int N, int channels, int width,
+                                    const int32_t* state_indices, void* conv_state_pool,
+                                    int64_t num_slots, kda_conv_act act, void* y,
+                                    int32_t* dev_status, void* stream) {
+  const kda_status st = conv_common(weight, bias, dtype, N, channels, width, state_indices,
+                                    conv_state_pool, num_slots, act, dev_status);
+  if (st != KDA_OK) return st;
+  if (N > 65535) return KDA_ERR_INVALID_ARG;  // sequences form the grid's y extent
+  if (!ptr_ok(x, N > 0) || !ptr_ok(y, N > 0)) return KDA_ERR_INVALID_ARG;
+  if (N == 0) return KDA_OK;
+  kda::ConvParams p{};
+  p.x = x; p.w = weight; p.bias = bias; p.y = y;
+  p.state_indices = state_indices;
+  p.pool = conv_state_pool; p.dev_status = dev_status;
+  p.num_slots = num_slots; p.N = N; p.C = channels; p.W = width; p.act = act; p.dtype = dtype;
+  return from_cuda(kda::launch_conv_decode(p, static_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_norm_gate(const void* o, const void* gate, const void* w, float eps,

@@ -62,6 +62,18 @@ struct NormGateParams {
   int gate_act;     // kda_gate_act
 };
 
+struct ConvParams {
+  const void *x, *w, *bias;   // x [T or N, C]; w [C, W]; bias [C] or NULL
+  void* y;                    // same layout as x
+  const int32_t *cu_seqlens, *state_indices, *has_initial_state;  // cu_seqlens: prefill only
+  void* pool;                 // [num_slots, W-1, C]
+  int32_t* dev_status;
+  int64_t T, num_slots;
+  int N, C, W;
+  int act;                    // 0 identity, 1 SiLU
+  kda_dtype dtype;
+};
+
 struct NormGateExParams {
   const void *o, *residual, *gate, *w, *b;  // residual, w, b may be NULL
   void *y, *residual_out;                   // residual_out may be NULL
@@ -103,6 +115,8 @@ cudaError_t launch_decode_multi(const DecodeMultiParams& p, cudaStream_t stream)
 cudaError_t launch_commit(const CommitParams& p, cudaStream_t stream);
 cudaError_t launch_norm_gate(const NormGateParams& p, cudaStream_t stream);
 cudaError_t launch_norm_gate_ex(const NormGateExParams& p, cudaStream_t stream);
+cudaError_t launch_conv_prefill(const ConvParams& p, cudaStream_t stream);
+cudaError_t launch_conv_decode(const ConvParams& p, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
 // Upper bound over every option (what kda_prefill_workspace_bytes reports).
 size_t prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk);

@@ -172,6 +172,41 @@ def test_norm_gate_ex_empty_is_noop(lib):
     assert _ngx(lib, rows=0, o=None, gate=None, y=None) == 0
 
 
+def _convp(lib, **over):
+    a = dict(x=FAKE, w=FAKE, b=None, dt=1, cu=FAKE, N=3, T=100, C=256, W=4, idx=FAKE, his=None,
+             pool=FAKE, slots=8, act=1, y=FAKE, st=None)
+    a.update(over)
+    return lib.kda_causal_conv1d_prefill(a["x"], a["w"], a["b"], a["dt"], a["cu"], a["N"], a["T"],
+                                         a["C"], a["W"], a["idx"], a["his"], a["pool"], a["slots"],
+                                         a["act"], a["y"], a["st"], None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(W=5), -2), (dict(W=1), -2), (dict(C=100), -2), (dict(dt=2), -2), (dict(N=-1), -1),
+    (dict(T=-1), -1), (dict(slots=0), -1), (dict(act=2), -1), (dict(w=None), -1),
+    (dict(pool=None), -1), (dict(cu=None), -1), (dict(x=MIS), -1), (dict(b=MIS), -1),
+    (dict(T=65536 * 64), -1),
+])
+def test_conv_prefill_rejects(lib, over, expect):
+    assert _convp(lib, **over) == expect
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(W=5), -2), (dict(C=12), -2), (dict(N=70000), -1), (dict(idx=None), -1), (dict(y=MIS), -1),
+])
+def test_conv_decode_rejects(lib, over, expect):
+    a = dict(x=FAKE, w=FAKE, b=None, dt=0, N=3, C=256, W=4, idx=FAKE, pool=FAKE, slots=8, act=0,
+             y=FAKE, st=None)
+    a.update(over)
+    assert lib.kda_causal_conv1d_decode(a["x"], a["w"], a["b"], a["dt"], a["N"], a["C"], a["W"],
+                                        a["idx"], a["pool"], a["slots"], a["act"], a["y"], a["st"],
+                                        None) == expect
+
+
+def test_conv_empty_is_noop(lib):
+    assert _convp(lib, T=0, x=None, y=None) == 0
+
+
 def test_workspace_query(lib):
     assert kda.kda_prefill_workspace_bytes(8, 4096, 32, 128, 128, 64) >= 0
     assert lib.kda_prefill_workspace_bytes(-1, 10, 2, 64, 64, 64) == 0

@@ -9,6 +9,8 @@ import oracle
 import workloads as W
 from kda_testutil import (excess_error, max_abs, oracle_prefill, run_prefill, to_dev, tol_for)
 
+W_ = W  # the workloads module, for tests whose parameter W is a convolution width
+
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
@@ -360,6 +362,76 @@ def test_decode_multi_full_width(kda_gpu):
     ref_commit = oracle.commit_accepted(ts_ref, dd["num_accepted"][sample].numpy(), ref_idx,
                                         sub_pool)
     assert excess_error(pool[sidx.long().to(DEV)], ref_commit) <= tol
+
+
+@pytest.mark.parametrize("W", [2, 3, 4])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("act", ["none", "silu"])
+def test_conv_prefill(kda_gpu, W, dtype, act):
+    """Lengths 0, 1, W-2, W-1, 63, 64, 65, 200 (tiles of 64 tokens, inputs before
+    a tile from x or the cache), one padding sequence, one without initial
+    state; outputs and caches against the oracle, untouched slots unchanged."""
+    lens = (0, 1, max(W - 2, 1), W - 1, 63, 64, 65, 200, 9)
+    his = [1, 1, 0, 1, 1, 1, 0, 1, 1]
+    d = W_.make_conv(lens, 1032, W, dtype, num_slots=16, seed=800 + W, has_initial=his)
+    idx = d["state_indices"].clone()
+    idx[8] = -1
+    d["state_indices"] = idx
+    t = to_dev(d, DEV)
+    y = torch.full_like(t["x"], float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda_gpu.kda_causal_conv1d_prefill(t["x"], t["w"], t["cu_seqlens"], t["state_indices"], t["pool"],
+                                      y, bias=t["b"], has_initial_state=t["has_initial_state"],
+                                      act=act, dev_status=status)
+    torch.cuda.synchronize()
+    y_ref, p_ref = oracle.conv_prefill(d["x"], d["w"], d["cu_seqlens"], d["state_indices"], d["pool"],
+                                       bias=d["b"], has_initial_state=d["has_initial_state"], act=act)
+    assert int(status.item()) == 0
+    tol = 1e-5 if dtype == torch.float32 else 1e-3
+    assert excess_error(y, y_ref) <= tol
+    assert excess_error(t["pool"], p_ref) <= 0.0 + (1e-6 if dtype == torch.float32 else 0.0)
+    t0, t1 = int(d["cu_seqlens"][8]), int(d["cu_seqlens"][9])
+    assert torch.count_nonzero(y[t0:t1].float()).item() == 0  # padding rows exactly zero
+    used = set(int(i) for i in idx.tolist() if i >= 0)
+    for s_ in range(16):
+        if s_ not in used:
+            assert torch.equal(t["pool"][s_].cpu(), d["pool"][s_])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_conv_decode_steps_and_split(kda_gpu, dtype):
+    """A prefill of 40 tokens then 6 decode steps equals the oracle's prefill of
+    all 46 tokens (outputs and final cache), over a 12288-channel (3 x 32 x 128)
+    projection."""
+    C, W = 12288, 4
+    lens = (40, 17)
+    d = W_.make_conv(lens, C, W, dtype, num_slots=4, seed=91)
+    extra = torch.randn(6, 2, C, generator=torch.Generator().manual_seed(5)).to(dtype)
+    t = to_dev(d, DEV)
+    y = torch.empty_like(t["x"])
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda_gpu.kda_causal_conv1d_prefill(t["x"], t["w"], t["cu_seqlens"], t["state_indices"], t["pool"],
+                                      y, bias=t["b"], dev_status=status)
+    ys = []
+    for s_ in range(6):
+        xs = extra[s_].to(DEV)
+        ysd = torch.empty_like(xs)
+        kda_gpu.kda_causal_conv1d_decode(xs, t["w"], t["state_indices"], t["pool"], ysd, bias=t["b"],
+                                         dev_status=status)
+        ys.append(ysd)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    # the oracle over the concatenated sequences
+    xa = torch.cat([d["x"][:40], extra[:, 0], d["x"][40:], extra[:, 1]])
+    cua = torch.tensor([0, 46, 46 + 23], dtype=torch.int32)
+    y_ref, p_ref = oracle.conv_prefill(xa, d["w"], cua, d["state_indices"], d["pool"], bias=d["b"])
+    tol = 1e-5 if dtype == torch.float32 else 1e-3
+    assert excess_error(y[:40], y_ref[:40]) <= tol
+    assert excess_error(y[40:], y_ref[46:63]) <= tol
+    dec = torch.stack(ys)  # [6, 2, C]
+    assert excess_error(dec[:, 0], y_ref[40:46]) <= tol
+    assert excess_error(dec[:, 1], y_ref[63:69]) <= tol
+    assert excess_error(t["pool"], p_ref) <= (1e-6 if dtype == torch.float32 else 0.0)
 
 
 @pytest.mark.parametrize("dv", [16, 64, 128])

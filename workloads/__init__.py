@@ -204,3 +204,20 @@ def make_decode_draft(w: DecodeWorkload, K: int, seed=None):
     out = {name: x.reshape((w.N, K) + tuple(x.shape[1:])) for name, x in t.items()}
     out["num_accepted"] = torch.randint(0, K + 1, (w.N,), generator=gen, dtype=torch.int32)
     return out
+
+
+def make_conv(lengths, C: int, W: int, dtype, num_slots: int, seed: int, has_initial=None):
+    """Inputs of the short causal convolution: x [T, C] ~ N(0, 1) (the
+    projections), taps [C, W] ~ N(0, 0.5^2), bias [C] ~ N(0, 0.1^2), cache pool
+    [num_slots, W-1, C] ~ N(0, 1), distinct slots from a seeded permutation."""
+    gen = torch.Generator().manual_seed(int(seed))
+    T = int(sum(lengths))
+    x = torch.randn(T, C, generator=gen, dtype=torch.float64).to(dtype)
+    w = (0.5 * torch.randn(C, W, generator=gen, dtype=torch.float64)).to(dtype)
+    b = (0.1 * torch.randn(C, generator=gen, dtype=torch.float64)).to(dtype)
+    pool = torch.randn(num_slots, W - 1, C, generator=gen, dtype=torch.float32).to(dtype)
+    idx = _slots(gen, len(lengths), num_slots)
+    out = dict(x=x, w=w, b=b, pool=pool, state_indices=idx, cu_seqlens=cu_from_lengths(lengths))
+    if has_initial is not None:
+        out["has_initial_state"] = torch.tensor(has_initial, dtype=torch.int32)
+    return out
