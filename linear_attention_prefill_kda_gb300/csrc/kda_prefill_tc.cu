@@ -719,14 +719,19 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
 // Kernel 2: state carry, one CTA per (sequence, head)
 // =====================================================================
 namespace state {
-constexpr uint32_t STAGE = 82432;        // PA|KLT|U0 (65536) | ZERO (8192) | AQK (8192) | DECAY (512)
-constexpr uint32_t ST_PA = 0, ST_KLT = 32768, ST_U0 = 49152, ST_ZERO = 65536, ST_AQK = 73728,
-                   ST_DECAY = 81920;
+// A stage holds one chunk's operands: PA|KLT|U0 (65536, the main copy) and
+// AQK|DECAY (8704, the tail copy).  The output product reads the 8 KB before
+// AQK (the end of U0) as rows 0-63 of its A operand; those products land in
+// TMEM lanes 0-63, whose W S values have been consumed by then.
+constexpr uint32_t STAGE = 74240;
+constexpr uint32_t ST_PA = 0, ST_KLT = 32768, ST_U0 = 49152, ST_AQK = 65536, ST_DECAY = 73728;
 constexpr uint32_t S_SOP = 2 * STAGE;    // fp16 MN-major [K=c 128 x N=v 128] (K stride 2048)
 constexpr uint32_t S_UOP = S_SOP + 32768;  // fp16 MN-major [K=j 64 x N=v 128]
 constexpr uint32_t S_NW = S_UOP + 16384;   // fp32 [128]
-constexpr uint32_t S_SS = S_NW + 512;      // fp32 [2][64]
-constexpr uint32_t SMEM_BYTES = S_SS + 512;
+constexpr uint32_t S_SS = S_NW + 512;      // fp32 [2 chunk parities][2][64]
+constexpr uint32_t OSTG_ROW = 272;         // padded bf16 output row (256 B + 16)
+constexpr uint32_t S_OSTG = S_SS + 1024;   // bf16 [64][OSTG_ROW]: the finished output rows of a chunk
+constexpr uint32_t SMEM_BYTES = S_OSTG + 64 * OSTG_ROW;
 }  // namespace state
 
 // 8x8 transpose of 16-byte chunks within each group of 8 lanes: before, lane
@@ -824,10 +829,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     tc::mbar_init(&bar_o, 1);
     tc::mbar_fence_init();
   }
-  for (int i = tid; i < 8192 / 16; i += kThreads) {
-    reinterpret_cast<uint4*>(sm + ST_ZERO)[i] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(sm + STAGE + ST_ZERO)[i] = make_uint4(0, 0, 0, 0);
-  }
   float* s_ss = reinterpret_cast<float*>(sm + S_SS);
   // state row lrow, columns [64 hh, 64 hh + 64), fp32 in registers for the whole call
   TS* slot_state = reinterpret_cast<TS*>(p.state_pool) + ((int64_t)si.slot * H + head) * (D * D);
@@ -880,8 +881,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
 
   // Output epilogue of chunk kp (query-side warps only; they synchronise among
   // themselves with named barrier 1): read scale * O from TMEM, RMSNorm-gate,
-  // store bf16 rows.
-  auto epilogue = [&](int kp, bool ok_o) {
+  // and either leave the bf16 rows in the staging buffer, from which the
+  // key-side warps store them with coalesced writes while they wait for the
+  // state product (staged), or store them directly (the last chunk).
+  auto epilogue = [&](int kp, bool ok_o, bool staged) {
     const int c0 = kp * C;
     const int n = min(C, len - c0);
     const uint32_t tP = tmem + 128 * (kp & 1);
@@ -898,17 +901,21 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
 #pragma unroll
       for (int u = 0; u < 64; ++u) o[u] = 0.f;
     }
+    // row partial sums by chunk parity: the buffer of chunk kp is next
+    // rewritten in chunk kp + 2, after the barrier of chunk kp + 1
+    float* ssb = s_ss + 128 * (kp & 1);
     if (p.gate) {
       float ss = 0.f;
 #pragma unroll
       for (int u = 0; u < 64; ++u) ss += o[u] * o[u];
-      s_ss[hh * 64 + orow] = ss;
+      ssb[hh * 64 + orow] = ss;
       asm volatile("bar.sync 1, 128;" ::: "memory");
     }
-    if (ok_o && orow < n) {
-      bf16* dst = gout + ((t0 + c0 + orow) * H + head) * D + hh * 64;
+    if (ok_o && (staged || orow < n)) {
+      uint4* dst = staged ? reinterpret_cast<uint4*>(sm + S_OSTG + orow * OSTG_ROW + hh * 128)
+                          : reinterpret_cast<uint4*>(gout + ((t0 + c0 + orow) * H + head) * D + hh * 64);
       float inv = 1.f;
-      if (p.gate) inv = rsqrtf((s_ss[orow] + s_ss[64 + orow]) * (1.f / (float)D) + p.eps);
+      if (p.gate) inv = rsqrtf((ssb[orow] + ssb[64 + orow]) * (1.f / (float)D) + p.eps);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float y[8];
@@ -921,10 +928,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
 #pragma unroll
           for (int u = 0; u < 8; ++u) y[u] = o[8 * i + u];
         }
-        reinterpret_cast<uint4*>(dst)[i] = pack_bf8(y);
+        dst[i] = pack_bf8(y);
       }
     }
-    if (p.gate) asm volatile("bar.sync 1, 128;" ::: "memory");  // s_ss reusable
   };
 
   int64_t pending_ck = -1;  // checkpoint entry whose store is still to be issued
@@ -951,14 +957,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     tc::fence_after_sync();
     if (k + 1 < nchunks) last_issued = k + 1;
     if (tid == 0) {
-      if (k + 1 < nchunks) issue_load_main(k + 1);
-      // P = [W; Q e^G] S  -> tP (rows 0-63: W S, rows 64-127: Q e^G S)
+      // P = [W; Q e^G] S  -> tP (rows 0-63: W S, rows 64-127: Q e^G S); the
+      // next chunk's copy is issued behind it, off the chain
       constexpr uint32_t idP = tc::idesc_f16(128, 128, false, false, true);
       const uint32_t pa = tc::smem_u32(st + ST_PA), so = tc::smem_u32(sm + S_SOP);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         tc::mma_f16(tP, tc::sdesc(pa + kk * 256, 128, 2048), tc::sdesc(so + kk * 4096, 2048, 128), idP, kk > 0);
       tc::mma_commit(&bar_p);
+      if (k + 1 < nchunks) issue_load_main(k + 1);
     }
     store_pending_ck();
     bool ok_w = true;
@@ -968,7 +975,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
         const bool ok_o = __all_sync(0xffffffffu, tc::mbar_wait(&bar_o, ph ^ 1));
         tc::fence_after_sync();
         ok_w = ok_o;
-        epilogue(k - 1, ok_o);
+        epilogue(k - 1, ok_o, true);
       }
       if (p.gate) {
 #pragma unroll
@@ -1003,12 +1010,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     if (!ok) break;
     tc::fence_after_sync();
     if (tid == 0) {
-      // every thread passed the barrier, so the output product of chunk k-1
-      // (which the query side waited for) no longer reads the other stage
-      if (k + 1 < nchunks) issue_load_tail(k + 1);
       constexpr uint32_t idO = tc::idesc_f16(128, 128, false, false, true);
       constexpr uint32_t idS = tc::idesc_f16(128, 128, false, true, true);
-      const uint32_t z = tc::smem_u32(st + ST_ZERO), uo = tc::smem_u32(sm + S_UOP),
+      const uint32_t z = tc::smem_u32(st + ST_AQK) - 8192, uo = tc::smem_u32(sm + S_UOP),
                      kl = tc::smem_u32(st + ST_KLT);
 #pragma unroll
       for (int kk = 0; kk < C / 16; ++kk)
@@ -1018,6 +1022,22 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
       for (int kk = 0; kk < C / 16; ++kk)
         tc::mma_f16(tP, tc::sdesc(z + kk * 256, 128, 1024), tc::sdesc(uo + kk * 4096, 2048, 128), idO, true);
       tc::mma_commit(&bar_o);
+      // every thread passed the barrier above, so the output product of chunk
+      // k-1 (which the query side waited for) no longer reads the other stage
+      if (k + 1 < nchunks) issue_load_tail(k + 1);
+    }
+    if (!qside && k > 0) {
+      // the previous chunk's output rows, staged by the query side before the
+      // barrier: each instruction of a warp writes two whole 256-byte rows
+      const int np = min(C, len - (k - 1) * C);
+      const int kw = 2 * (warp >> 2) + (warp & 1);  // 0..3 over the key-side warps
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int row = 16 * kw + 2 * i + (lane >> 4), ch = lane & 15;
+        if (row < np)
+          reinterpret_cast<uint4*>(gout + ((t0 + (int64_t)(k - 1) * C + row) * H + head) * D)[ch] =
+              *reinterpret_cast<const uint4*>(sm + S_OSTG + row * OSTG_ROW + ch * 16);
+      }
     }
     // ---- state carry: S <- Diag(e^G_last) S + (K e^(G_last-G))^T U ----
     ok = cta_wait(&bar_s, ph);
@@ -1044,7 +1064,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   if (ok && nchunks > 0 && qside) {
     const bool ok_o = __all_sync(0xffffffffu, tc::mbar_wait(&bar_o, ph ^ 1));
     tc::fence_after_sync();
-    epilogue(nchunks - 1, ok_o);
+    epilogue(nchunks - 1, ok_o, false);
     if (!ok_o) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
   }
   if (!ok) {
