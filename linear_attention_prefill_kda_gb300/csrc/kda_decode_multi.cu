@@ -32,6 +32,8 @@ struct MultiShape {
   static constexpr int THREADS = CG * RG;
 };
 
+constexpr int kTokBlock = 8;  // tokens whose inputs are staged in shared memory at once
+
 template <int DK, int DV, typename TI, typename TS>
 __global__ void __launch_bounds__(MultiShape<DK, DV>::THREADS)
 decode_multi_kernel(DecodeMultiParams p) {
@@ -42,9 +44,10 @@ decode_multi_kernel(DecodeMultiParams p) {
   const int seq = (int)(blockIdx.x / (unsigned)p.H), head = (int)(blockIdx.x % (unsigned)p.H);
   const int H = p.H, K = p.K;
 
-  __shared__ float s_q[DK], s_k[DK], s_a[DK];
+  // the inputs of up to kTokBlock tokens, loaded together before they are used
+  __shared__ float s_q[kTokBlock][DK], s_k[kTokBlock][DK], s_a[kTokBlock][DK];
+  __shared__ float s_v[kTokBlock][DV], s_gt[kTokBlock][DV], s_beta[kTokBlock], s_qk[kTokBlock];
   __shared__ float s_pk[RG][DV], s_pq[RG][DV];
-  __shared__ float s_qk;
 
   const int32_t slot = p.state_indices[seq];
   if (slot < 0 || slot >= p.num_slots) {
@@ -60,84 +63,92 @@ decode_multi_kernel(DecodeMultiParams p) {
 #pragma unroll
   for (int m = 0; m < RPT; ++m) st[m] = load4(S + (rg + m * RG) * DV + cg * 4);
 
-  for (int t = 0; t < K; ++t) {
-    const int64_t row = ((int64_t)seq * K + t) * H + head;  // token-major [N*K, H, *]
-    const TI* q = reinterpret_cast<const TI*>(p.q) + row * DK;
-    const TI* k = reinterpret_cast<const TI*>(p.k) + row * DK;
-    const TI* g = reinterpret_cast<const TI*>(p.g) + row * DK;
-    for (int i = tid; i < DK; i += blockDim.x) {
-      s_q[i] = to_f32(q[i]);
-      s_k[i] = to_f32(k[i]);
-      s_a[i] = expf(to_f32(g[i]));
+  for (int tb = 0; tb < K; tb += kTokBlock) {
+    const int nb = min(kTokBlock, K - tb);
+    __syncthreads();  // the previous block's inputs are no longer read
+    for (int e = tid; e < nb * DK; e += blockDim.x) {
+      const int u = e / DK, i = e % DK;
+      const int64_t row = ((int64_t)seq * K + tb + u) * H + head;
+      s_q[u][i] = to_f32(reinterpret_cast<const TI*>(p.q)[row * DK + i]);
+      s_k[u][i] = to_f32(reinterpret_cast<const TI*>(p.k)[row * DK + i]);
+      s_a[u][i] = expf(to_f32(reinterpret_cast<const TI*>(p.g)[row * DK + i]));
     }
+    for (int e = tid; e < nb * DV; e += blockDim.x) {
+      const int u = e / DV, j = e % DV;
+      const int64_t row = ((int64_t)seq * K + tb + u) * H + head;
+      s_v[u][j] = to_f32(reinterpret_cast<const TI*>(p.v)[row * DV + j]);
+      if (p.gate) s_gt[u][j] = to_f32(reinterpret_cast<const TI*>(p.gate)[row * DV + j]);
+    }
+    if (tid < nb) s_beta[tid] = to_f32(reinterpret_cast<const TI*>(p.beta)[((int64_t)seq * K + tb + tid) * H + head]);
     __syncthreads();
-    if (tid < 32) {
+    // q . k of every token of the block (one warp per token)
+    for (int u = tid >> 5; u < nb; u += blockDim.x >> 5) {
       float acc = 0.f;
-      for (int i = tid; i < DK; i += 32) acc += s_q[i] * s_k[i];
+      for (int i = tid & 31; i < DK; i += 32) acc += s_q[u][i] * s_k[u][i];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (tid == 0) s_qk = acc;
+      if ((tid & 31) == 0) s_qk[u] = acc;
     }
-    float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+    for (int u = 0; u < nb; ++u) {
+      const int t = tb + u;
+      const int64_t row = ((int64_t)seq * K + t) * H + head;  // token-major [N*K, H, *]
+      float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) {
-      const int i = rg + m * RG;
-      const float a = s_a[i];
-      st[m].x *= a; st[m].y *= a; st[m].z *= a; st[m].w *= a;
-      const float ki = s_k[i], qi = s_q[i];
-      pk.x += ki * st[m].x; pk.y += ki * st[m].y; pk.z += ki * st[m].z; pk.w += ki * st[m].w;
-      pq.x += qi * st[m].x; pq.y += qi * st[m].y; pq.z += qi * st[m].z; pq.w += qi * st[m].w;
-    }
-    *reinterpret_cast<float4*>(&s_pk[rg][cg * 4]) = pk;
-    *reinterpret_cast<float4*>(&s_pq[rg][cg * 4]) = pq;
-    __syncthreads();
-    float tk[4] = {0.f, 0.f, 0.f, 0.f}, tq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int r = 0; r < RG; ++r) {
-      const float4 a = *reinterpret_cast<const float4*>(&s_pk[r][cg * 4]);
-      const float4 b = *reinterpret_cast<const float4*>(&s_pq[r][cg * 4]);
-      tk[0] += a.x; tk[1] += a.y; tk[2] += a.z; tk[3] += a.w;
-      tq[0] += b.x; tq[1] += b.y; tq[2] += b.z; tq[3] += b.w;
-    }
-    const float beta = to_f32(reinterpret_cast<const TI*>(p.beta)[row]);
-    const float4 v4 = load4(reinterpret_cast<const TI*>(p.v) + row * DV + cg * 4);
-    float u[4];
-    u[0] = beta * (v4.x - tk[0]);
-    u[1] = beta * (v4.y - tk[1]);
-    u[2] = beta * (v4.z - tk[2]);
-    u[3] = beta * (v4.w - tk[3]);
-#pragma unroll
-    for (int m = 0; m < RPT; ++m) {
-      const float ki = s_k[rg + m * RG];
-      st[m].x += ki * u[0]; st[m].y += ki * u[1]; st[m].z += ki * u[2]; st[m].w += ki * u[3];
-    }
-    if (p.token_states) {
-      TS* ts = reinterpret_cast<TS*>(p.token_states) + row * (DK * DV);
-#pragma unroll
-      for (int m = 0; m < RPT; ++m) store4_stream(ts + (rg + m * RG) * DV + cg * 4, st[m]);
-    }
-    if (rg == 0) {
-      const float qk = s_qk;
-      float o[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) o[c] = p.scale * (tq[c] + qk * u[c]);
-      if (p.gate) {
-        float ss = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
-        const unsigned mask = CG == 32 ? 0xffffffffu : ((1u << CG) - 1u);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-          if (off < CG) ss += __shfl_xor_sync(mask, ss, off);
-        const float inv = rsqrtf(ss / (float)DV + p.eps);
-        const float4 gt = load4(reinterpret_cast<const TI*>(p.gate) + row * DV + cg * 4);
-        const float4 w = load4(reinterpret_cast<const TI*>(p.norm_w) + cg * 4);
-        o[0] *= inv * w.x * gate_actf(gt.x, p.gate_act);
-        o[1] *= inv * w.y * gate_actf(gt.y, p.gate_act);
-        o[2] *= inv * w.z * gate_actf(gt.z, p.gate_act);
-        o[3] *= inv * w.w * gate_actf(gt.w, p.gate_act);
+      for (int m = 0; m < RPT; ++m) {
+        const int i = rg + m * RG;
+        const float a = s_a[u][i];
+        st[m].x *= a; st[m].y *= a; st[m].z *= a; st[m].w *= a;
+        const float ki = s_k[u][i], qi = s_q[u][i];
+        pk.x += ki * st[m].x; pk.y += ki * st[m].y; pk.z += ki * st[m].z; pk.w += ki * st[m].w;
+        pq.x += qi * st[m].x; pq.y += qi * st[m].y; pq.z += qi * st[m].z; pq.w += qi * st[m].w;
       }
-      store4(reinterpret_cast<TI*>(p.out) + row * DV + cg * 4, make_float4(o[0], o[1], o[2], o[3]));
+      __syncthreads();  // s_pk / s_pq of the previous token read by all (and s_qk ready)
+      *reinterpret_cast<float4*>(&s_pk[rg][cg * 4]) = pk;
+      *reinterpret_cast<float4*>(&s_pq[rg][cg * 4]) = pq;
+      __syncthreads();
+      float tk[4] = {0.f, 0.f, 0.f, 0.f}, tq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int r = 0; r < RG; ++r) {
+        const float4 a = *reinterpret_cast<const float4*>(&s_pk[r][cg * 4]);
+        const float4 b = *reinterpret_cast<const float4*>(&s_pq[r][cg * 4]);
+        tk[0] += a.x; tk[1] += a.y; tk[2] += a.z; tk[3] += a.w;
+        tq[0] += b.x; tq[1] += b.y; tq[2] += b.z; tq[3] += b.w;
+      }
+      const float beta = s_beta[u];
+      float u4[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) u4[c] = beta * (s_v[u][cg * 4 + c] - tk[c]);
+#pragma unroll
+      for (int m = 0; m < RPT; ++m) {
+        const float ki = s_k[u][rg + m * RG];
+        st[m].x += ki * u4[0]; st[m].y += ki * u4[1]; st[m].z += ki * u4[2]; st[m].w += ki * u4[3];
+      }
+      if (p.token_states) {
+        TS* ts = reinterpret_cast<TS*>(p.token_states) + row * (DK * DV);
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) store4_stream(ts + (rg + m * RG) * DV + cg * 4, st[m]);
+      }
+      if (rg == 0) {
+        const float qk = s_qk[u];
+        float o[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[c] = p.scale * (tq[c] + qk * u4[c]);
+        if (p.gate) {
+          float ss = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
+          const unsigned mask = CG == 32 ? 0xffffffffu : ((1u << CG) - 1u);
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1)
+            if (off < CG) ss += __shfl_xor_sync(mask, ss, off);
+          const float inv = rsqrtf(ss / (float)DV + p.eps);
+          const float4 w = load4(reinterpret_cast<const TI*>(p.norm_w) + cg * 4);
+          o[0] *= inv * w.x * gate_actf(s_gt[u][cg * 4 + 0], p.gate_act);
+          o[1] *= inv * w.y * gate_actf(s_gt[u][cg * 4 + 1], p.gate_act);
+          o[2] *= inv * w.z * gate_actf(s_gt[u][cg * 4 + 2], p.gate_act);
+          o[3] *= inv * w.w * gate_actf(s_gt[u][cg * 4 + 3], p.gate_act);
+        }
+        store4(reinterpret_cast<TI*>(p.out) + row * DV + cg * 4, make_float4(o[0], o[1], o[2], o[3]));
+      }
     }
-    __syncthreads();  // s_q / s_k / s_a / partial sums are reused by the next token
   }
   if (p.write_back) {
 #pragma unroll

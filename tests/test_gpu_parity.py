@@ -78,6 +78,27 @@ def test_prefill_edge_lengths(kda_gpu, chunk, d, state_dtype):
     assert torch.count_nonzero(out[t0:t1].float()).item() == 0  # padding rows exactly zero
 
 
+def test_prefill_many_sequences(kda_gpu):
+    """100 sequences of 1-150 tokens (the slot lookup scans 32 sequences per
+    step), a few empty ones and padding rows, tensor-core shape, checkpoints
+    every 128 tokens, SiLU gate and a mix of initial-state flags."""
+    gen = torch.Generator().manual_seed(61)
+    lens = torch.randint(1, 151, (100,), generator=gen)
+    lens[[7, 50, 93]] = 0
+    w = W.SCHED.replace(seqlens=tuple(int(x) for x in lens), H=2, num_slots=128, slot_range=None,
+                        checkpoint_every=128, seed=62)
+    d = W.make_prefill(w)
+    idx = d["state_indices"].clone()
+    idx[[3, 64]] = -1
+    d["state_indices"] = idx
+    d["gate_act"] = "silu"
+    d["has_initial_state"] = (torch.arange(100) % 3 != 0).to(torch.int32)
+    out, _ = _check_prefill(kda_gpu, w, d)
+    for i in (3, 64):
+        t0, t1 = int(d["cu_seqlens"][i]), int(d["cu_seqlens"][i + 1])
+        assert torch.count_nonzero(out[t0:t1].float()).item() == 0
+
+
 def test_prefill_tc_shape_mixed(kda_gpu):
     """The tensor-core shape (d=128, chunk 64, bf16) with short, partial and
     multi-chunk sequences, bf16 state, checkpoints and the fused norm-gate."""
@@ -396,6 +417,24 @@ def test_conv_prefill(kda_gpu, W, dtype, act):
     for s_ in range(16):
         if s_ not in used:
             assert torch.equal(t["pool"][s_].cpu(), d["pool"][s_])
+
+
+def test_conv_prefill_many_sequences(kda_gpu):
+    """70 sequences of 0-130 tokens (more than one 32-sequence lookup step)."""
+    gen = torch.Generator().manual_seed(71)
+    lens = tuple(int(x) for x in torch.randint(0, 131, (70,), generator=gen))
+    d = W_.make_conv(lens, 264, 4, torch.bfloat16, num_slots=80, seed=72)
+    t = to_dev(d, DEV)
+    y = torch.full_like(t["x"], float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda_gpu.kda_causal_conv1d_prefill(t["x"], t["w"], t["cu_seqlens"], t["state_indices"], t["pool"],
+                                      y, bias=t["b"], dev_status=status)
+    torch.cuda.synchronize()
+    y_ref, p_ref = oracle.conv_prefill(d["x"], d["w"], d["cu_seqlens"], d["state_indices"], d["pool"],
+                                       bias=d["b"])
+    assert int(status.item()) == 0
+    assert excess_error(y, y_ref) <= 1e-3
+    assert excess_error(t["pool"], p_ref) <= 0.0
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
