@@ -6,17 +6,22 @@
 // (zero without initial state); the cache then holds the sequence's last W-1
 // extended inputs, oldest first.  act = identity or SiLU.
 //
-// Prefill: a CTA covers 256 channels of one 64-token tile (tile k of sequence
-// i has slot cu[i]/64 + i + k, the chunk slots of the prefill); each warp
-// takes 8 of the tokens, each lane 8 channels, and loads all its inputs
-// before computing.  The W-1 inputs before a warp's tokens come from x or,
-// at the start of the sequence, from the cache; a sliding window of them
-// stays in registers.  Only the first warp of the first tile reads the old
-// cache, and the same threads write the new one after their last read of it,
-// so the in-place update needs no ordering across CTAs.
+// Prefill: a CTA covers one 64-token tile (tile k of sequence i has slot
+// cu[i]/64 + i + k, the chunk slots of the prefill) and 256 channels (128 for
+// fp32) in sub-blocks of 128.  Each sub-block -- the tile, the W-1 inputs
+// before it (from x, or at the start of the sequence from the cache), taps
+// and bias -- is staged in shared memory by its own group of 16-byte
+// asynchronous copies, so a CTA keeps 36 KB of loads in flight with few
+// registers, and the second group is still landing while the first is
+// computed.  Each warp then takes 8 of the tokens and each lane 4 channels,
+// with a sliding window of the W-1 previous inputs in registers.  Only the
+// first tile reads the old cache (in its staging) and it writes the new one
+// after the staging barrier, so the in-place update needs no ordering across
+// CTAs.
 // Memory bound: x is read once (plus W-1 halo rows per tile) and y written once.
 #include "kda_common.cuh"
 #include "kda_internal.h"
+#include "kda_tc.cuh"
 
 namespace kda {
 namespace {
@@ -36,32 +41,6 @@ __device__ __forceinline__ void store8(T* p, const float* v) {
   store4(p + 4, make_float4(v[4], v[5], v[6], v[7]));
 }
 
-// 8 consecutive elements kept as loaded (bf16: one 16-byte vector) until use
-template <typename T>
-struct Raw8;
-template <>
-struct Raw8<bf16> {
-  uint4 v;
-  __device__ __forceinline__ void load(const bf16* p) { v = *reinterpret_cast<const uint4*>(p); }
-  __device__ __forceinline__ void unpack(float* o) const {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __bfloat1622float2(h[i]);
-      o[2 * i] = f.x;
-      o[2 * i + 1] = f.y;
-    }
-  }
-};
-template <>
-struct Raw8<float> {
-  float4 a, b;
-  __device__ __forceinline__ void load(const float* p) { a = load4(p); b = load4(p + 4); }
-  __device__ __forceinline__ void unpack(float* o) const {
-    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
-  }
-};
-
 // taps of 8 consecutive channels: w[c0 .. c0+8, 0 .. W) is 8W contiguous
 // elements (16-byte aligned because c0 is a multiple of 8), read as vectors
 template <int W, typename T>
@@ -76,29 +55,63 @@ __device__ __forceinline__ void load_taps(const T* wp, float (&wt)[W][kVec]) {
 }
 
 constexpr int kPrefillThreads = 256;  // 8 warps x 8 tokens = one 64-token tile
+constexpr int kCh = 128;              // channels of a prefill CTA
+constexpr int kPV = 4;                // channels per lane (32 lanes x 4)
 
-template <int W, typename T>
-__global__ void __launch_bounds__(kPrefillThreads) conv_prefill_kernel(ConvParams p) {
+// SiLU a * sigmoid(a) = a / (1 + 2^(-a log2 e)), from the approximate base-2
+// exponential and reciprocal instructions (each within a few fp32 ulps; the
+// limits come out exactly: 0 for a -> -inf through 1/inf, a for a -> +inf)
+__device__ __forceinline__ float silu_approx(float a) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(a * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return a * r;
+}
+
+template <int ACT>
+__device__ __forceinline__ float conv_act(float a) {
+  return ACT == 1 ? silu_approx(a) : a;
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack4(float4 f, float* o) {
+  o[0] = f.x; o[1] = f.y; o[2] = f.z; o[3] = f.w;
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Sub-blocks of 128 channels per prefill CTA: two for 16-bit inputs (one
+// lookup of the sequence per 256 channels, and the second sub-block's copies
+// still in flight while the first is computed), one for fp32 (static shared
+// memory is limited to 48 KB).
+template <typename T>
+struct ConvSplit {
+  static constexpr int value = sizeof(T) == 2 ? 2 : 1;
+};
+
+template <int W, typename T, int ACT>
+__global__ void __launch_bounds__(kPrefillThreads, 4) conv_prefill_kernel(ConvParams p) {
   constexpr int WM = W - 1;
   constexpr int kSub = kTile / (kPrefillThreads / 32);  // tokens per warp (8)
+  constexpr int kSplit = ConvSplit<T>::value;
+  constexpr int kRows = kTile + WM;                     // WM halo rows + the tile
+  constexpr int kPerPiece = 16 / (int)sizeof(T);        // elements per 16-byte piece
+  constexpr int kPieces = kCh / kPerPiece;              // pieces per staged row
+  constexpr int kTapOff = kRows * kCh;                  // taps [128 channels][W]
+  constexpr int kBiasOff = kTapOff + kCh * W;           // bias [128 channels]
+  constexpr int kBlk = kBiasOff + kCh;                  // elements per sub-block
+  static_assert((kTapOff * sizeof(T)) % 16 == 0 && (kBiasOff * sizeof(T)) % 16 == 0 &&
+                    (kBlk * sizeof(T)) % 16 == 0,
+                "staged arrays must start on 16-byte boundaries");
+  __shared__ __align__(16) T s_buf[kSplit * kBlk];
   __shared__ int s_seq, s_k, s_slot, s_init;
   __shared__ int64_t s_t0, s_t1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t slot = blockIdx.y;
-  const int c0 = (blockIdx.x * 32 + lane) * kVec;
-  const bool chan = c0 < p.C;
-  // taps and bias depend only on the channels: fetched while warp 0 finds the
-  // sequence
-  float wt[W][kVec], bs[kVec];
-  if (chan) {
-    load_taps<W>(reinterpret_cast<const T*>(p.w) + (int64_t)c0 * W, wt);
-    if (p.bias) {
-      load8(reinterpret_cast<const T*>(p.bias) + c0, bs);
-    } else {
-#pragma unroll
-      for (int v = 0; v < kVec; ++v) bs[v] = 0.f;
-    }
-  }
+  const int C = p.C;
   // (sequence, tile) of this slot: sequence i owns slots [first(i), first(i+1))
   // with first(i) = cu[i]/64 + i; warp 0 scans 32 sequences per step and also
   // fetches the sequence's bounds, cache slot and initial-state flag
@@ -140,85 +153,118 @@ __global__ void __launch_bounds__(kPrefillThreads) conv_prefill_kernel(ConvParam
     if (k == 0 && tid == 0 && blockIdx.x == 0) latch_status(p.dev_status, KDA_DEV_BAD_SEQLENS);
     return;
   }
-  // this warp: tokens [ws, we) of tile k; the first warp of the first tile
-  // alone reads the old cache and writes the new one
-  const int64_t ws = t0 + (int64_t)k * kTile + warp * kSub;
-  const int64_t we = min(ws + kSub, t1);
-  const bool owner = k == 0 && warp == 0;
-  if (ws >= t1 && !(owner && t1 > t0)) return;
-  if (!chan) return;
-  const int C = p.C;
+  const int64_t base = t0 + (int64_t)k * kTile;  // first token of this tile
+  if (base >= t1) return;                        // a slot past the sequence's last tile
+  const int nt = (int)min((int64_t)kTile, t1 - base);
   const T* x = reinterpret_cast<const T*>(p.x);
   T* y = reinterpret_cast<T*>(p.y);
+  const int tb = warp * kSub;  // this warp's first token in the tile
+  const int n = min(kSub, nt - tb);
+  const int cbase = blockIdx.x * kSplit * kCh;
   const int32_t sidx = s_slot;
   if (sidx < 0 || sidx >= p.num_slots) {
-    if (sidx != -1 && owner && c0 == 0) latch_status(p.dev_status, KDA_DEV_BAD_INDEX);
-    const float z[kVec] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int64_t t = ws; t < we; ++t) store8(y + t * C + c0, z);
+    if (sidx != -1 && k == 0 && tid == 0 && blockIdx.x == 0) latch_status(p.dev_status, KDA_DEV_BAD_INDEX);
+#pragma unroll
+    for (int sb = 0; sb < kSplit; ++sb) {
+      const int c0 = cbase + sb * kCh + lane * kPV;
+      if (c0 < C)
+        for (int u = 0; u < n; ++u) store4(y + (base + tb + u) * C + c0, make_float4(0.f, 0.f, 0.f, 0.f));
+    }
     return;
   }
-  T* cache = reinterpret_cast<T*>(p.pool) + (int64_t)sidx * WM * C + c0;
+  T* cache = reinterpret_cast<T*>(p.pool) + (int64_t)sidx * WM * C;
   const bool init = s_init != 0;
-  // the W-1 inputs before ws (oldest first): from x, or from the cache for the
-  // first tokens of the sequence (the owner's window is the old cache itself)
-  float win[WM][kVec];
+  // Stage each sub-block as its own group of 16-byte asynchronous copies: row
+  // r is the extended input at token base - WM + r, from x, or (first tile,
+  // r < WM) from cache row r, zero without initial state; then the taps and
+  // the bias of its channels (zero without bias).
 #pragma unroll
-  for (int j = 0; j < WM; ++j) {
-    const int64_t tt = ws - WM + j;
-    if (tt >= t0) {
-      load8(x + tt * C + c0, win[j]);
-    } else if (init) {
-      load8(cache + (tt - t0 + WM) * (int64_t)C, win[j]);
-    } else {
-#pragma unroll
-      for (int v = 0; v < kVec; ++v) win[j][v] = 0.f;
-    }
-  }
-  // all of this warp's inputs are loaded before the arithmetic starts
-  Raw8<T> raw[kSub];
-#pragma unroll
-  for (int u = 0; u < kSub; ++u)
-    if (ws + u < we) raw[u].load(x + (ws + u) * C + c0);
-#pragma unroll
-  for (int u = 0; u < kSub; ++u) {
-    if (ws + u >= we) break;
-    float acc[kVec], xu[kVec];
-    raw[u].unpack(xu);
-#pragma unroll
-    for (int v = 0; v < kVec; ++v) {
-      float a = bs[v];
-#pragma unroll
-      for (int j = 0; j < WM; ++j) a += wt[j][v] * win[j][v];
-      a += wt[WM][v] * xu[v];
-      acc[v] = p.act == 1 ? a * sigmoidf_(a) : a;
-    }
-    store8(y + (ws + u) * C + c0, acc);
-#pragma unroll
-    for (int j = 0; j + 1 < WM; ++j)
-#pragma unroll
-      for (int v = 0; v < kVec; ++v) win[j][v] = win[j + 1][v];
-#pragma unroll
-    for (int v = 0; v < kVec; ++v) win[WM - 1][v] = xu[v];
-  }
-  if (owner) {
-    // new cache: the last W-1 extended inputs of the sequence, oldest first
-    float nw[WM][kVec];
-#pragma unroll
-    for (int j = 0; j < WM; ++j) {
-      const int64_t tt = t1 - WM + j;
-      if (tt >= t0) {
-        load8(x + tt * C + c0, nw[j]);
-      } else if (init) {
-        // an input still in the old cache (sequences shorter than W-1): only
-        // these threads write the cache, and they have not yet
-        load8(cache + (tt - t0 + WM) * (int64_t)C, nw[j]);
-      } else {
-#pragma unroll
-        for (int v = 0; v < kVec; ++v) nw[j][v] = 0.f;
+  for (int sb = 0; sb < kSplit; ++sb) {
+    T* buf = s_buf + sb * kBlk;
+    const int cb = cbase + sb * kCh;
+    const int nc = min(kCh, C - cb);  // channels of this sub-block (a multiple of 8)
+    if (nc > 0) {
+      for (int i = tid; i < (WM + nt) * kPieces; i += kPrefillThreads) {
+        const int r = i / kPieces, pc = i - r * kPieces;
+        const int c = cb + pc * kPerPiece;
+        const int64_t t = base - WM + r;
+        const T* src = t >= t0 ? x + t * C + c : cache + (int64_t)r * C + c;
+        const bool valid = pc * kPerPiece < nc && (t >= t0 || init);
+        tc::cp_async16(buf + r * kCh + pc * kPerPiece, valid ? src : x, valid);
+      }
+      const T* wsrc = reinterpret_cast<const T*>(p.w) + (int64_t)cb * W;
+      const T* bsrc = p.bias ? reinterpret_cast<const T*>(p.bias) + cb : x;
+      for (int i = tid; i < (kCh * W + kCh) / kPerPiece; i += kPrefillThreads) {
+        const int e = i * kPerPiece;  // element offset in [taps | bias]
+        const bool tap = e < kCh * W;
+        const bool valid = tap ? e < nc * W : (p.bias != nullptr && e - kCh * W < nc);
+        const T* src = tap ? wsrc + e : bsrc + (e - kCh * W);
+        tc::cp_async16(buf + kTapOff + e, valid ? src : x, valid);
       }
     }
+    tc::cp_async_commit();
+  }
 #pragma unroll
-    for (int j = 0; j < WM; ++j) store8(cache + (int64_t)j * C, nw[j]);
+  for (int sb = 0; sb < kSplit; ++sb) {
+    if (sb == 0)
+      cp_async_wait_group<kSplit - 1>();
+    else
+      cp_async_wait_group<0>();
+    __syncthreads();
+    const T* buf = s_buf + sb * kBlk;
+    const int c0 = cbase + sb * kCh + lane * kPV;
+    if (c0 >= C) continue;
+    const T* sx = buf + lane * kPV;
+    if (n > 0) {
+      // taps of this lane's 4 channels: 4W contiguous staged elements
+      float wt[W][kPV], bs[kPV];
+#pragma unroll
+      for (int q = 0; q < W; ++q) {
+        float e[4];
+        unpack4<T>(load4(buf + kTapOff + lane * kPV * W + 4 * q), e);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) wt[(4 * q + u) % W][(4 * q + u) / W] = e[u];
+      }
+      unpack4<T>(load4(buf + kBiasOff + lane * kPV), bs);
+      float win[WM][kPV];
+#pragma unroll
+      for (int j = 0; j < WM; ++j) unpack4<T>(load4(sx + (tb + j) * kCh), win[j]);
+      T* yw = y + (base + tb) * C + c0;
+#pragma unroll
+      for (int u = 0; u < kSub; ++u) {
+        if (u >= n) break;
+        float xu[kPV], acc[kPV];
+        unpack4<T>(load4(sx + (tb + WM + u) * kCh), xu);
+#pragma unroll
+        for (int v = 0; v < kPV; ++v) {
+          float a = bs[v];
+#pragma unroll
+          for (int j = 0; j < WM; ++j) a += wt[j][v] * win[j][v];
+          a += wt[WM][v] * xu[v];
+          acc[v] = conv_act<ACT>(a);
+        }
+        store4(yw + (int64_t)u * C, make_float4(acc[0], acc[1], acc[2], acc[3]));
+#pragma unroll
+        for (int j = 0; j + 1 < WM; ++j)
+#pragma unroll
+          for (int v = 0; v < kPV; ++v) win[j][v] = win[j + 1][v];
+#pragma unroll
+        for (int v = 0; v < kPV; ++v) win[WM - 1][v] = xu[v];
+      }
+    }
+    // New cache, written by the last warp of the first tile once every read
+    // of the old one (the staging above) is done: the sequence's last W-1
+    // extended inputs, oldest first.  A sequence inside one tile has them all
+    // staged.
+    if (k == 0 && warp == kPrefillThreads / 32 - 1) {
+      const int64_t len = t1 - t0;
+#pragma unroll
+      for (int j = 0; j < WM; ++j) {
+        const int64_t t = t1 - WM + j;
+        const float4 v = len <= kTile ? load4(sx + (len + j) * kCh) : load4(x + t * C + c0);
+        store4(cache + (int64_t)j * C + c0, v);
+      }
+    }
   }
 }
 
@@ -254,24 +300,33 @@ __global__ void __launch_bounds__(kThreads) conv_decode_kernel(ConvParams p) {
 #pragma unroll
     for (int j = 0; j < WM; ++j) a += wt[j][v] * win[j][v];
     a += wt[WM][v] * xv[v];
-    acc[v] = p.act == 1 ? a * sigmoidf_(a) : a;
+    acc[v] = p.act == 1 ? silu_approx(a) : a;
   }
   store8(y, acc);
 #pragma unroll
   for (int j = 0; j < WM; ++j) store8(cache + (int64_t)j * C, j + 1 < WM ? win[j + 1] : xv);
 }
 
+template <int W, typename T>
+cudaError_t launch_prefill_w(const ConvParams& p, dim3 grid, cudaStream_t stream) {
+  if (p.act == 1)
+    conv_prefill_kernel<W, T, 1><<<grid, kPrefillThreads, 0, stream>>>(p);
+  else
+    conv_prefill_kernel<W, T, 0><<<grid, kPrefillThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_prefill_t(const ConvParams& p, cudaStream_t stream) {
   const int64_t slots = p.T / kTile + p.N;
-  dim3 grid((unsigned)((p.C + 32 * kVec - 1) / (32 * kVec)), (unsigned)slots);  // 256 channels x 64 tokens
+  constexpr int ch = ConvSplit<T>::value * kCh;  // channels per CTA
+  dim3 grid((unsigned)((p.C + ch - 1) / ch), (unsigned)slots);
   switch (p.W) {
-    case 2: conv_prefill_kernel<2, T><<<grid, kPrefillThreads, 0, stream>>>(p); break;
-    case 3: conv_prefill_kernel<3, T><<<grid, kPrefillThreads, 0, stream>>>(p); break;
-    case 4: conv_prefill_kernel<4, T><<<grid, kPrefillThreads, 0, stream>>>(p); break;
+    case 2: return launch_prefill_w<2, T>(p, grid, stream);
+    case 3: return launch_prefill_w<3, T>(p, grid, stream);
+    case 4: return launch_prefill_w<4, T>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 template <typename T>

@@ -391,10 +391,13 @@ def test_decode_multi_full_width(kda_gpu):
 def test_conv_prefill(kda_gpu, W, dtype, act):
     """Lengths 0, 1, W-2, W-1, 63, 64, 65, 200 (tiles of 64 tokens, inputs before
     a tile from x or the cache), one padding sequence, one without initial
-    state; outputs and caches against the oracle, untouched slots unchanged."""
+    state; outputs and caches against the oracle, untouched slots unchanged.
+    1032 channels leave a last block of 8; width 3 runs without bias."""
     lens = (0, 1, max(W - 2, 1), W - 1, 63, 64, 65, 200, 9)
     his = [1, 1, 0, 1, 1, 1, 0, 1, 1]
     d = W_.make_conv(lens, 1032, W, dtype, num_slots=16, seed=800 + W, has_initial=his)
+    if W == 3:
+        d["b"] = None
     idx = d["state_indices"].clone()
     idx[8] = -1
     d["state_indices"] = idx
