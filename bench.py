@@ -130,29 +130,40 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def kernel_source_hash() -> str:
-    """sha256 over the CUDA sources of the library (identifies the kernels a
-    recorded ncu traffic figure belongs to)."""
-    import glob
+# The CUDA sources behind each recorded traffic figure: a figure stays valid
+# while these files are unchanged, whatever else in the library changes.
+_COMMON_SRC = ["kda_common.cuh", "kda_internal.h"]
+TRAFFIC_SOURCES = {
+    "prefill": ["kda_prefill.cu", "kda_prefill_tc.cu", "kda_prefill_shared.cuh", "kda_tc.cuh"]
+    + _COMMON_SRC,
+    "decode": ["kda_decode.cu"] + _COMMON_SRC,
+    "spec": ["kda_decode_multi.cu"] + _COMMON_SRC,
+    "conv": ["kda_conv.cu", "kda_tc.cuh"] + _COMMON_SRC,
+}
+
+
+def kernel_source_hash(group: str) -> str:
+    """sha256 over the CUDA sources of one kernel group (identifies the kernels
+    a recorded ncu traffic figure belongs to)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_prefill_kda_gb300", "csrc")
-    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode())
+    for name in sorted(TRAFFIC_SOURCES[group]):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode())
             h.update(fh.read())
     return h.hexdigest()
 
 
-def recorded_traffic(name: str):
+def recorded_traffic(group: str, name: str):
     """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json)
-    for the current kernel sources, else None."""
+    for the current sources of the kernel group, else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        rec = json.load(f)
-    if rec.get("csrc_sha256") != kernel_source_hash():
+        rec = json.load(f).get(group)
+    if not rec or rec.get("sources_sha256") != kernel_source_hash(group):
         return None
     v = rec.get(name)
     return None if v is None else int(v)
@@ -448,7 +459,7 @@ def run_gpu(args):
         "prefill_ms": round(pre_ms_mean, 4),
         "roofline": {"bound": "hbm", "achieved": round(pre_gbs, 1), "peak": pk["hbm"],
                      "unit": "GB/s", "frac": round(pre_gbs / pk["hbm"], 4),
-                     "traffic": recorded_traffic("prefill_call_dram_bytes"),
+                     "traffic": recorded_traffic("prefill", "prefill_call_dram_bytes"),
                      "peak_source": pk["source"],
                      "algorithmic_bytes": pre_bytes, "algorithmic_flops": pre_flops,
                      "achieved_tflops": round(pre_tflops, 2),
@@ -457,7 +468,7 @@ def run_gpu(args):
                    "ms_per_step": round(dec_ms, 4),
                    "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": pk["hbm"],
                                 "unit": "GB/s", "frac": round(dec_gbs / pk["hbm"], 4),
-                                "traffic": recorded_traffic("decode_step_dram_bytes"),
+                                "traffic": recorded_traffic("decode", "decode_step_dram_bytes"),
                                 "algorithmic_bytes": dec_bytes}},
         "spec_decode": {"value": round(replica_rate(dw.N * SPEC_K, ws, spec_ms), 1),
                         "unit": "draft tokens verified/s", "draft_tokens": SPEC_K,
@@ -465,14 +476,14 @@ def run_gpu(args):
                         "roofline": {"bound": "hbm", "achieved": round(spec_gbs, 1),
                                      "peak": pk["hbm"], "unit": "GB/s",
                                      "frac": round(spec_gbs / pk["hbm"], 4),
-                                     "traffic": recorded_traffic("spec_step_dram_bytes"),
+                                     "traffic": recorded_traffic("spec", "spec_step_dram_bytes"),
                                      "algorithmic_bytes": spec_bytes}},
         "conv_prefill": {"value": round(replica_rate(T, ws, conv_ms), 1), "unit": "tokens/s",
                          "channels": CONV_C, "width": CONV_W, "ms_per_call": round(conv_ms, 4),
                          "roofline": {"bound": "hbm", "achieved": round(conv_gbs, 1),
                                       "peak": pk["hbm"], "unit": "GB/s",
                                       "frac": round(conv_gbs / pk["hbm"], 4),
-                                      "traffic": recorded_traffic("conv_call_dram_bytes"),
+                                      "traffic": recorded_traffic("conv", "conv_call_dram_bytes"),
                                       "algorithmic_bytes": conv_bytes}},
         "e2e": {"value": round(replica_rate(T, ws, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

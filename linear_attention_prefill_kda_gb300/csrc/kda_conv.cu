@@ -13,8 +13,9 @@
 // and bias -- is staged in shared memory by its own group of 16-byte
 // asynchronous copies, so a CTA keeps 36 KB of loads in flight with few
 // registers, and the second group is still landing while the first is
-// computed.  Each warp then takes 8 of the tokens and each lane 4 channels,
-// with a sliding window of the W-1 previous inputs in registers.  Only the
+// computed.  Each warp then takes 8 of the tokens and each lane 4 channels
+// (as 2 pairs for the packed fp32 instructions), with a sliding window of the
+// W-1 previous inputs in registers.  Only the
 // first tile reads the old cache (in its staging) and it writes the new one
 // after the staging barrier, so the in-place update needs no ordering across
 // CTAs.
@@ -68,9 +69,47 @@ __device__ __forceinline__ float silu_approx(float a) {
   return a * r;
 }
 
+// Packed fp32 pair arithmetic (two IEEE round-to-nearest operations in one
+// instruction, sm_100 family): the same results as the scalar forms, half
+// the instructions.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// The activation on a pair of channels (SiLU as in silu_approx, with the
+// multiplications and the addition packed).
 template <int ACT>
-__device__ __forceinline__ float conv_act(float a) {
-  return ACT == 1 ? silu_approx(a) : a;
+__device__ __forceinline__ float2 conv_act2(float2 a) {
+  if (ACT != 1) return a;
+  const float2 m = fmul2(a, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+  float2 e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.x) : "f"(m.x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.y) : "f"(m.y));
+  const float2 den = fadd2(e, make_float2(1.f, 1.f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.x) : "f"(den.x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.y) : "f"(den.y));
+  return fmul2(a, r);
 }
 
 template <typename T>
@@ -184,22 +223,31 @@ __global__ void __launch_bounds__(kPrefillThreads, 4) conv_prefill_kernel(ConvPa
     const int cb = cbase + sb * kCh;
     const int nc = min(kCh, C - cb);  // channels of this sub-block (a multiple of 8)
     if (nc > 0) {
-      for (int i = tid; i < (WM + nt) * kPieces; i += kPrefillThreads) {
-        const int r = i / kPieces, pc = i - r * kPieces;
-        const int c = cb + pc * kPerPiece;
-        const int64_t t = base - WM + r;
-        const T* src = t >= t0 ? x + t * C + c : cache + (int64_t)r * C + c;
-        const bool valid = pc * kPerPiece < nc && (t >= t0 || init);
-        tc::cp_async16(buf + r * kCh + pc * kPerPiece, valid ? src : x, valid);
+      // each thread keeps one 16-byte column of the rows and steps down them
+      constexpr int kRowStep = kPrefillThreads / kPieces;
+      const int pc = tid % kPieces, r0 = tid / kPieces;
+      const bool cvalid = pc * kPerPiece < nc;
+      const int c = cb + pc * kPerPiece;
+      const T* src = x + (base - WM + r0) * C + c;  // dereferenced only at tokens >= t0
+      T* dst = buf + r0 * kCh + pc * kPerPiece;
+      for (int r = r0; r < WM + nt; r += kRowStep, src += (int64_t)kRowStep * C, dst += kRowStep * kCh) {
+        if (r < WM && k == 0) {  // before the sequence: the cached input, zero without one
+          const bool v = cvalid && init;
+          tc::cp_async16(dst, v ? cache + (int64_t)r * C + c : x, v);
+        } else {
+          tc::cp_async16(dst, cvalid ? src : x, cvalid);
+        }
       }
-      const T* wsrc = reinterpret_cast<const T*>(p.w) + (int64_t)cb * W;
-      const T* bsrc = p.bias ? reinterpret_cast<const T*>(p.bias) + cb : x;
-      for (int i = tid; i < (kCh * W + kCh) / kPerPiece; i += kPrefillThreads) {
-        const int e = i * kPerPiece;  // element offset in [taps | bias]
+      // taps and bias: one piece per thread
+      constexpr int kTapPieces = (kCh * W + kCh) / kPerPiece;
+      static_assert(kTapPieces <= kPrefillThreads, "one tap piece per thread");
+      if (tid < kTapPieces) {
+        const int e = tid * kPerPiece;  // element offset in [taps | bias]
         const bool tap = e < kCh * W;
         const bool valid = tap ? e < nc * W : (p.bias != nullptr && e - kCh * W < nc);
-        const T* src = tap ? wsrc + e : bsrc + (e - kCh * W);
-        tc::cp_async16(buf + kTapOff + e, valid ? src : x, valid);
+        const T* tsrc = tap ? reinterpret_cast<const T*>(p.w) + (int64_t)cb * W + e
+                            : (p.bias ? reinterpret_cast<const T*>(p.bias) + cb + (e - kCh * W) : x);
+        tc::cp_async16(buf + kTapOff + e, valid ? tsrc : x, valid);
       }
     }
     tc::cp_async_commit();
@@ -236,12 +284,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 4) conv_prefill_kernel(ConvPa
         float xu[kPV], acc[kPV];
         unpack4<T>(load4(sx + (tb + WM + u) * kCh), xu);
 #pragma unroll
-        for (int v = 0; v < kPV; ++v) {
-          float a = bs[v];
+        for (int v = 0; v < kPV; v += 2) {  // channel pairs
+          float2 a = make_float2(bs[v], bs[v + 1]);
 #pragma unroll
-          for (int j = 0; j < WM; ++j) a += wt[j][v] * win[j][v];
-          a += wt[WM][v] * xu[v];
-          acc[v] = conv_act<ACT>(a);
+          for (int j = 0; j < WM; ++j)
+            a = ffma2(make_float2(wt[j][v], wt[j][v + 1]), make_float2(win[j][v], win[j][v + 1]), a);
+          a = ffma2(make_float2(wt[WM][v], wt[WM][v + 1]), make_float2(xu[v], xu[v + 1]), a);
+          const float2 r = conv_act2<ACT>(a);
+          acc[v] = r.x;
+          acc[v + 1] = r.y;
         }
         store4(yw + (int64_t)u * C, make_float4(acc[0], acc[1], acc[2], acc[3]));
 #pragma unroll

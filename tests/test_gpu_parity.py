@@ -440,6 +440,32 @@ def test_conv_prefill_many_sequences(kda_gpu):
     assert excess_error(t["pool"], p_ref) <= 0.0
 
 
+@pytest.mark.parametrize("dtype,W", [(torch.bfloat16, 4), (torch.float32, 3)])
+def test_conv_prefill_many_items_per_cta(kda_gpu, dtype, W):
+    """The scheduler's 8-sequence mix (4096 tokens) over 12288 channels: several
+    thousand (tile, channel block) items, so every CTA of the persistent grid
+    takes many in turn; one sequence without initial state, one padding."""
+    lens = (1576, 586, 148, 147, 122, 303, 788, 426)
+    his = [1, 0, 1, 1, 1, 1, 1, 1]
+    d = W_.make_conv(lens, 12288, W, dtype, num_slots=12, seed=1234 + W, has_initial=his)
+    idx = d["state_indices"].clone()
+    idx[4] = -1
+    d["state_indices"] = idx
+    t = to_dev(d, DEV)
+    y = torch.full_like(t["x"], float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda_gpu.kda_causal_conv1d_prefill(t["x"], t["w"], t["cu_seqlens"], t["state_indices"], t["pool"],
+                                      y, bias=t["b"], has_initial_state=t["has_initial_state"],
+                                      dev_status=status)
+    torch.cuda.synchronize()
+    y_ref, p_ref = oracle.conv_prefill(d["x"], d["w"], d["cu_seqlens"], d["state_indices"], d["pool"],
+                                       bias=d["b"], has_initial_state=d["has_initial_state"])
+    assert int(status.item()) == 0
+    tol = 1e-5 if dtype == torch.float32 else 1e-3
+    assert excess_error(y, y_ref) <= tol
+    assert excess_error(t["pool"], p_ref) <= (1e-6 if dtype == torch.float32 else 0.0)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_conv_decode_steps_and_split(kda_gpu, dtype):
     """A prefill of 40 tokens then 6 decode steps equals the oracle's prefill of
