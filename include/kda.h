@@ -252,6 +252,12 @@ KDA_API kda_status kda_norm_gate_ex(const void* o, const void* residual, void* r
  *               sequence leaves its cache alone).
  *  conv_state_pool [num_slots, W-1, channels] dtype, updated in place.
  * Values are formed in fp32 and rounded to dtype when stored.
+ * Host-side errors: KDA_ERR_UNSUPPORTED for a width outside {2, 3, 4},
+ * channels not a multiple of 8 or a dtype other than f32/bf16;
+ * KDA_ERR_INVALID_ARG for a NULL or misaligned pointer, negative sizes,
+ * an unknown act, or T/64 + N > 65535 (the prefill's 64-token tile slots;
+ * the decode's limit is N <= 65535).  Device-side (dev_status): a bad index
+ * or bad cu_seqlens as for kda_prefill_chunked.
  */
 typedef enum { KDA_CONV_IDENTITY = 0, KDA_CONV_SILU = 1 } kda_conv_act;
 KDA_API kda_status kda_causal_conv1d_prefill(const void* x, const void* weight, const void* bias,
