@@ -566,8 +566,14 @@ def cpu_baseline(w, d, budget_s=15.0):
         _oracle_prefill_once(w, dd)
         t_total += time.perf_counter() - t0
         n += 1
+    # the same oracle on one thread, one call
+    t0 = time.perf_counter()
+    _oracle_prefill_once(w, dd, nthreads=1)
+    t_one = time.perf_counter() - t0
     return {"value": round(n * w.T / t_total, 1), "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
+            "one_thread": {"value": round(w.T / t_one, 1), "unit": "tokens/s",
+                           "sample": f"1 full call, {t_one:.1f} s"},
             "sample": f"{n} full calls of {w.name} (fp64 C oracle, OpenMP over (sequence, head), "
                       f"pool reduced to the 8 touched slots), {t_total:.1f} s on "
                       f"{os.cpu_count()} host cores"}

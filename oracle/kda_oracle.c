@@ -257,12 +257,13 @@ int kda_oracle_prefill(const double* q, const double* k, const double* v, const 
   const size_t sd = (size_t)dk * dv;
   const int64_t pairs = (int64_t)N * H;
 #ifdef _OPENMP
-  if (nthreads > 0) omp_set_num_threads(nthreads);
+  /* a thread count for this call only (the process-wide default is untouched) */
+  const int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
 #else
   (void)nthreads;
 #endif
   int failed = 0;
-#pragma omp parallel
+#pragma omp parallel num_threads(nt)
   {
     double* S = (double*)malloc(sizeof(double) * sd);
     double* u = (double*)malloc(sizeof(double) * (size_t)dv);
