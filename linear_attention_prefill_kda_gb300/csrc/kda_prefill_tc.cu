@@ -143,13 +143,13 @@ constexpr uint32_t S_REGION = 98304;
 //  phase 3 (solve and W, U0):
 constexpr uint32_t S_AKK = 0;           // fp32 [64][65]   beta-scaled strictly-lower A
 constexpr uint32_t S_TF = 16640;        // fp32 [64][65]   (I + A)^-1
-constexpr uint32_t S_MB = 33280;        // fp32 [3][16][17] block products of the solve
+constexpr uint32_t S_MB = 33280;        // fp32 [2][16][17] + [32][33] block products of the solve
 constexpr uint32_t S_KW = 49152;        // bf16 MN-major [K=j 64 x N=c 128]: K e^G
 constexpr uint32_t S_VB = 65536;        // bf16 MN-major [K=j 64 x N=v 128]: V
 constexpr uint32_t S_TP = 81920;        // bf16 K-major [128 x 64] (SBO 1024): T Diag(beta), rows 64-127 zero
 //  exact path (extreme decay) instead of phase 2:
 constexpr uint32_t S_FK = 0, S_FQ = 16384, S_FG = 32768, S_FAKK = 65536, S_FAQK = 81920;
-static_assert(S_MB + 3 * 16 * 17 * 4 <= S_KW, "solve scratch overlaps the W operand");
+static_assert(S_MB + (2 * 16 * 17 + 32 * 33) * 4 <= S_KW, "solve scratch overlaps the W operand");
 static_assert(S_RAWK >= S_LOP + 16384 && S_RAWK + 3 * RAW_BYTES <= S_REGION, "raw rows overlap phase-1 operands");
 // per-chunk scalars after the region
 constexpr uint32_t S_BETA = S_REGION;          // fp32 [64]
@@ -610,47 +610,119 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     for (int rr = 0; rr < 16; ++rr) s_tf[(16 * b + rr) * 65 + 16 * b + jj] = x[rr];
   }
   __syncthreads();
-  // off-diagonal 16x16 blocks, nearest the diagonal first:
-  //   M = sum_{bk=bj}^{bi-1} A[bi][bk] T[bk][bj],  T[bi][bj] = -T[bi][bi] M
-  // each thread owns 2x2 output tiles (rows rr, rr+8; columns cc, cc+8)
-  float* s_mb = reinterpret_cast<float*>(sm + S_MB);
-  for (int dist = 1; dist < 4; ++dist) {
-    const int ntiles = (4 - dist) * 64;
-    if (tid < ntiles) {
-      const int t = tid;
-      const int pi = t >> 6, rr = (t >> 3) & 7, cc = t & 7;
-      const int bj = pi, bi = pi + dist;
-      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-      for (int bk = bj; bk < bi; ++bk) {
-        const float* ar0 = s_akk + (16 * bi + rr) * 65 + 16 * bk;
-        const float* ar1 = ar0 + 8 * 65;
-        const float* tcol = s_tf + (16 * bk) * 65 + 16 * bj + cc;
-#pragma unroll
-        for (int l = 0; l < 16; ++l) {
-          const float x0 = ar0[l], x1 = ar1[l], y0 = tcol[l * 65], y1 = tcol[l * 65 + 8];
-          a00 += x0 * y0; a01 += x0 * y1; a10 += x1 * y0; a11 += x1 * y1;
-        }
-      }
-      float* mb = s_mb + pi * 272;
-      mb[rr * 17 + cc] = a00; mb[rr * 17 + cc + 8] = a01;
-      mb[(rr + 8) * 17 + cc] = a10; mb[(rr + 8) * 17 + cc + 8] = a11;
-    }
-    __syncthreads();
-    if (tid < ntiles) {
-      const int t = tid;
-      const int pi = t >> 6, rr = (t >> 3) & 7, cc = t & 7;
-      const int bj = pi, bi = pi + dist;
-      const float* tr0 = s_tf + (16 * bi + rr) * 65 + 16 * bi;
-      const float* tr1 = tr0 + 8 * 65;
-      const float* mb = s_mb + pi * 272 + cc;
+  // Off-diagonal blocks by two-level blocking.  For a block lower-triangular
+  // M = [[M11, 0], [M21, M22]], M^-1 has the block -M22^-1 M21 M11^-1 below
+  // its diagonal.  Level 1 (16-row halves of each 32-row half):
+  //   T10 = -T11 (A10 T00),  T32 = -T33 (A32 T22)
+  // level 2 (the 32x32 block): T[32:64, 0:32] = -T_bot Y, Y = A[32:64, 0:32] T_top,
+  // with T_top = [[T00, 0], [T10, T11]], so Y's right half (A T11) and the T00
+  // term of its left half are formed by threads 128-255 while threads 0-127
+  // do level 1.  Four barrier phases after the diagonal blocks.
+  {
+    float* s_x = reinterpret_cast<float*>(sm + S_MB);  // [2][16][17]: A10 T00, A32 T22
+    float* s_y = s_x + 2 * 16 * 17;                    // [32][33]:    Y
+    const int t = tid & 127;
+    // threads 0-127: level-1 block pb (rows 16(b+1).., columns 16b..), 2x2 tile
+    const int pb = t >> 6, b = 2 * pb, rr = (t >> 3) & 7, cc = t & 7;
+    // threads 128-255: rows yr, yr + 16 and columns cc, cc + 8 of a Y half
+    const int yr = (t >> 3) & 15;
+    if (tid < 128) {
+      // X = A[b+1][b] T[b][b]
+      const float* ar0 = s_akk + (16 * (b + 1) + rr) * 65 + 16 * b;
+      const float* ar1 = ar0 + 8 * 65;
+      const float* tcol = s_tf + (16 * b) * 65 + 16 * b + cc;
       float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
 #pragma unroll
       for (int l = 0; l < 16; ++l) {
-        const float x0 = tr0[l], x1 = tr1[l], y0 = mb[l * 17], y1 = mb[l * 17 + 8];
+        const float x0 = ar0[l], x1 = ar1[l], y0 = tcol[l * 65], y1 = tcol[l * 65 + 8];
         a00 += x0 * y0; a01 += x0 * y1; a10 += x1 * y0; a11 += x1 * y1;
       }
-      float* dst = s_tf + (16 * bi + rr) * 65 + 16 * bj + cc;
+      float* xb = s_x + pb * 272;
+      xb[rr * 17 + cc] = a00; xb[rr * 17 + cc + 8] = a01;
+      xb[(rr + 8) * 17 + cc] = a10; xb[(rr + 8) * 17 + cc + 8] = a11;
+    } else {
+      // Y[:, 16:32] = A[32:64, 16:32] T11
+      const float* ar0 = s_akk + (32 + yr) * 65 + 16;
+      const float* ar1 = ar0 + 16 * 65;
+      const float* tcol = s_tf + 16 * 65 + 16 + cc;
+      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+#pragma unroll
+      for (int l = 0; l < 16; ++l) {
+        const float x0 = ar0[l], x1 = ar1[l], y0 = tcol[l * 65], y1 = tcol[l * 65 + 8];
+        a00 += x0 * y0; a01 += x0 * y1; a10 += x1 * y0; a11 += x1 * y1;
+      }
+      s_y[yr * 33 + 16 + cc] = a00; s_y[yr * 33 + 24 + cc] = a01;
+      s_y[(yr + 16) * 33 + 16 + cc] = a10; s_y[(yr + 16) * 33 + 24 + cc] = a11;
+    }
+    __syncthreads();
+    if (tid < 128) {
+      // T[b+1][b] = -T[b+1][b+1] X
+      const float* tr0 = s_tf + (16 * (b + 1) + rr) * 65 + 16 * (b + 1);
+      const float* tr1 = tr0 + 8 * 65;
+      const float* xb = s_x + pb * 272 + cc;
+      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+#pragma unroll
+      for (int l = 0; l < 16; ++l) {
+        const float x0 = tr0[l], x1 = tr1[l], y0 = xb[l * 17], y1 = xb[l * 17 + 8];
+        a00 += x0 * y0; a01 += x0 * y1; a10 += x1 * y0; a11 += x1 * y1;
+      }
+      float* dst = s_tf + (16 * (b + 1) + rr) * 65 + 16 * b + cc;
       dst[0] = -a00; dst[8] = -a01; dst[8 * 65] = -a10; dst[8 * 65 + 8] = -a11;
+    } else {
+      // Y[:, 0:16] = A[32:64, 0:16] T00 (the T10 term follows)
+      const float* ar0 = s_akk + (32 + yr) * 65;
+      const float* ar1 = ar0 + 16 * 65;
+      const float* tcol = s_tf + cc;
+      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+#pragma unroll
+      for (int l = 0; l < 16; ++l) {
+        const float x0 = ar0[l], x1 = ar1[l], y0 = tcol[l * 65], y1 = tcol[l * 65 + 8];
+        a00 += x0 * y0; a01 += x0 * y1; a10 += x1 * y0; a11 += x1 * y1;
+      }
+      s_y[yr * 33 + cc] = a00; s_y[yr * 33 + 8 + cc] = a01;
+      s_y[(yr + 16) * 33 + cc] = a10; s_y[(yr + 16) * 33 + 8 + cc] = a11;
+    }
+    __syncthreads();
+    {
+      // Y[:, 0:16] += A[32:64, 16:32] T10: rows qr, qr + 16, column qc
+      const int qc = tid & 15, qr = tid >> 4;
+      const float* ar0 = s_akk + (32 + qr) * 65 + 16;
+      const float* ar1 = ar0 + 16 * 65;
+      const float* tcol = s_tf + 16 * 65 + qc;
+      float a0 = s_y[qr * 33 + qc], a1 = s_y[(qr + 16) * 33 + qc];
+#pragma unroll
+      for (int l = 0; l < 16; ++l) {
+        const float y = tcol[l * 65];
+        a0 += ar0[l] * y;
+        a1 += ar1[l] * y;
+      }
+      s_y[qr * 33 + qc] = a0;
+      s_y[(qr + 16) * 33 + qc] = a1;
+    }
+    __syncthreads();
+    {
+      // T[32:64, 0:32] = -T_bot Y.  Rows 16h + ir, 16h + ir + 8 of the bottom
+      // half (h uniform per warp), columns jc, jc + 16; T_bot's row i is
+      // nonzero in columns k <= i only, so the sum stops at 16(h + 1).
+      const int h = tid >> 7, ir = (tid >> 4) & 7, jc = tid & 15;
+      const float* tr0 = s_tf + (32 + 16 * h + ir) * 65 + 32;
+      const float* tr1 = tr0 + 8 * 65;
+      const float* yc = s_y + jc;
+      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float x0 = tr0[k], x1 = tr1[k], y0 = yc[k * 33], y1 = yc[k * 33 + 16];
+        a00 += x0 * y0; a01 += x0 * y1; a10 += x1 * y0; a11 += x1 * y1;
+      }
+      if (h == 1) {
+#pragma unroll
+        for (int k = 16; k < 32; ++k) {
+          const float x0 = tr0[k], x1 = tr1[k], y0 = yc[k * 33], y1 = yc[k * 33 + 16];
+          a00 += x0 * y0; a01 += x0 * y1; a10 += x1 * y0; a11 += x1 * y1;
+        }
+      }
+      float* dst = s_tf + (32 + 16 * h + ir) * 65 + jc;
+      dst[0] = -a00; dst[16] = -a01; dst[8 * 65] = -a10; dst[8 * 65 + 16] = -a11;
     }
     __syncthreads();
   }
