@@ -134,6 +134,14 @@ KDA_API size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int 
  *
  * State is carried in fp32 inside a call and rounded (to nearest even) to
  * state_dtype only when stored: at checkpoints and at the final write-back.
+ *
+ * Numerics.  The tensor-core path (bf16 inputs, dk = dv = 128, chunk 64)
+ * forms the in-chunk products A_kk, A_qk from split bf16 operands (fp32
+ * accuracy) and the state-coupled products from fp16 operands, all with fp32
+ * accumulation.  That relies on the method's regime: q and k rows of unit L2
+ * norm and beta in [0, 1], where I - beta k k^T is a contraction and the
+ * state and the intermediate rows stay O(1).  A chunk whose decay spread
+ * exceeds e^60 in some channel is computed by an exact element-wise path.
  */
 KDA_API kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, const void* g,
                                const void* beta, kda_dtype in_dtype, const int32_t* cu_seqlens,
