@@ -1,6 +1,7 @@
-"""bench.py's oracle arm (``--impl reference``) on the CPU: one JSON line with
-the keys the line carries on the GPU arm, and under a multi-rank launch only
-rank 0 does the work and prints."""
+"""bench.py on the CPU: the oracle arm (``--impl reference``) prints one JSON
+line with the keys the line carries on the GPU arm, and under a multi-rank
+launch only rank 0 does the work and prints; the algorithmic bytes the GPU
+arm's roofline objects divide by time match counts written out by hand."""
 import json
 import os
 import subprocess
@@ -41,3 +42,52 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_roofline_numerators_match_hand_counts():
+    """The algorithmic bytes the bench divides by time, against counts written
+    out by hand from the workload shapes."""
+    sys.path.insert(0, ROOT)
+    import workloads as W
+    b = _bench_module()
+    # scheduler-step prefill: T = 4096, H = 32, d = 128, bf16 in, fp32 state,
+    # 8 live sequences, checkpoints every 256 tokens (6+2+0+0+0+1+3+1 = 13)
+    w = W.SCHED
+    d = W.make_prefill(w)
+    T, H, dd = 4096, 32, 128
+    state = dd * dd * 4
+    expect = (4 * T * H * dd * 2          # q, k, g, v
+              + T * H * 2                 # beta
+              + T * H * dd * 2            # out
+              + T * H * dd * 2 + dd * 2   # gate, norm weight
+              + 2 * 8 * H * state         # state read + write
+              + 13 * H * state)           # checkpoints
+    assert expect == 262_406_400
+    assert b.prefill_algorithmic(w, d)[0] == expect
+    # decode: 256 sequences, fp32 states read and written, 641 bf16 values per
+    # (sequence, head) of q, k, g, v, beta, out, the gate, the weight, indices
+    dw = W.DECODE
+    expect = 2 * 256 * H * state + 256 * H * (3 * dd + dd + 1 + dd) * 2 + 256 * H * dd * 2 + dd * 2 + 256 * 4
+    assert expect == 1_086_342_400
+    assert b.decode_algorithmic(dw)[0] == expect
+    # verification of 4 draft tokens: state read, 4 states written, inputs and
+    # outputs of 4 tokens, and the commit of every sequence with a_i > 0
+    dr = W.make_decode_draft(dw, 4)
+    n_acc = int((dr["num_accepted"] > 0).sum())
+    expect = (256 * H * state + 4 * 256 * H * state + 4 * 256 * H * (3 * dd + dd + 1 + dd) * 2
+              + 4 * 256 * H * dd * 2 + dd * 2 + 2 * n_acc * H * state + 256 * 8)
+    assert b.spec_algorithmic(dw, 4, dr["num_accepted"]) == expect
+    # convolution over 12288 channels, width 4: x read and y written, taps and
+    # bias, 8 caches of 3 rows read and written
+    C = 3 * H * dd
+    expect = 2 * T * C * 2 + C * 5 * 2 + 2 * 8 * 3 * C * 2
+    assert expect == 202_629_120
+    assert b.conv_algorithmic(w, C, 4) == expect
