@@ -186,17 +186,21 @@ def prefill_algorithmic(w, d):
         b += T * H * dv * ib + dv * ib              # gate, norm weight
     b += 2 * n_seq * H * dk * dv * sb               # state read + write
     b += n_ck * H * dk * dv * sb                    # checkpoints
-    # FLOPs per chunk-head with n rows: decay-weighted KK^T and QK^T (2 n^2 dk
-    # halves), the solve and the six n x d x d / n x n x d products.
+    # FLOPs per chunk-head with n rows (a multiply-add is 2): the decay-weighted
+    # KK^T and QK^T (lower triangles), the triangular inverse, W = T'(K e^G)
+    # and U0 = T' V (T' lower triangular), the three n x dk x dv products with
+    # the state (W S, (Q e^G) S, (K e^(G_last - G))^T U), A_qk U, and the decay
+    # scaling of the operands.
     fl = 0
     for L in lens:
         for c0 in range(0, L, C):
             n = min(C, L - c0)
             tri = n * (n + 1) / 2
             fl += H * (2 * 2 * tri * dk          # A_kk, A_qk
+                       + n * n * n / 3           # triangular inverse
+                       + 2 * tri * (dk + dv)     # W, U0
+                       + 2 * n * dk * dv * 3     # W S, Q S, K^T U
                        + 2 * tri * dv            # A_qk U
-                       + n * n * n / 3           # forward substitution
-                       + 2 * n * dk * dv * 3     # K S, Q S, K^T U
                        + 4 * n * dk)             # decay scaling
     return int(b), float(fl)
 

@@ -91,3 +91,18 @@ def test_roofline_numerators_match_hand_counts():
     expect = 2 * T * C * 2 + C * 5 * 2 + 2 * 8 * 3 * C * 2
     assert expect == 202_629_120
     assert b.conv_algorithmic(w, C, 4) == expect
+
+
+def test_prefill_flop_count_matches_hand_count():
+    """Full 64-row chunks with d = 128: 2 (KK^T, QK^T lower triangles) x
+    2 x 2080 x 128, the triangular inverse 64^3 / 3, W and U0 2 x 2080 x 256,
+    the three state products 6 x 64 x 128 x 128, A_qk U 2 x 2080 x 128 and the
+    decay scaling 4 x 64 x 128 FLOPs per chunk-head."""
+    sys.path.insert(0, ROOT)
+    import workloads as W
+    b = _bench_module()
+    per_chunk = (4 * 2080 * 128 + 64 ** 3 / 3 + 2 * 2080 * 256 + 6 * 64 * 128 * 128
+                 + 2 * 2080 * 128 + 4 * 64 * 128)
+    w = W.SCHED.replace(seqlens=(128, 64), H=2, num_slots=4, slot_range=None)
+    d = W.make_prefill(w)
+    assert abs(b.prefill_algorithmic(w, d)[1] - 3 * 2 * per_chunk) < 1e-3
