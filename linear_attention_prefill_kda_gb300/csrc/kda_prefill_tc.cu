@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   float* s_egm = reinterpret_cast<float*>(sm + S_EGM);
   float* s_eglm = reinterpret_cast<float*>(sm + S_EGLM);
   int* s_misc = reinterpret_cast<int*>(sm + S_MISC);
-  __shared__ __align__(8) uint64_t bar, bar_l;
+  __shared__ __align__(8) uint64_t bar, bar_l, bar_fin;
   __shared__ uint32_t s_tmem;
 
   // Thread roles.  A warp may only touch the TMEM lane quarter of its SM
@@ -305,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   if (tid == 0) {
     tc::mbar_init(&bar, 1);
     tc::mbar_init(&bar_l, 1);
+    tc::mbar_init(&bar_fin, 1);
     tc::mbar_fence_init();
     tc::mbar_arrive_expect_tx(&bar_l, sizeof(LTable));
     tc::bulk_g2s(sm + S_LOP, &g_ltable, sizeof(LTable), &bar_l);
@@ -358,6 +359,19 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
+  // Error exit after a timed-out wait: let this CTA's asynchronous work still
+  // in flight finish (each wait bounded) before its TMEM is freed and its
+  // shared memory released -- the L-operand copy when that was the wait that
+  // failed, every product issued so far (a commit tracks all of them), and
+  // this thread's 16-byte copies.
+  auto drain = [&](bool l_pending) {
+    if (tid == 0) {
+      if (l_pending) tc::mbar_wait(&bar_l, 0);
+      tc::mma_commit(&bar_fin);
+      tc::mbar_wait(&bar_fin, 0);
+    }
+    tc::cp_async_wait_all();
+  };
   // ---- G = L g : inclusive in-chunk cumulative sum, rows duplicated in both lane halves ----
   bool ok_l = true;
   if (tid == 0) ok_l = tc::mbar_wait(&bar_l, 0);  // the L operand has landed
@@ -391,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   __syncthreads();
   if (!ok) {
     if (tid == 0) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
+    drain(!ok_l);
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
@@ -554,8 +569,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   tc::fence_before_sync();
   __syncthreads();  // region reads done; phase-3 buffers may be written
   if (!ok) {
-    tc::cp_async_wait_all();
     if (tid == 0) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
+    drain(false);
+    tc::fence_before_sync();
+    __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
     return;
   }
@@ -781,7 +798,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
       }
     }
   }
-  if (!ok && tid == 0) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
+  if (!ok) {
+    if (tid == 0) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
+    drain(false);
+  }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, 256);
@@ -869,7 +889,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   using namespace state;
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ __align__(8) uint64_t bar_ld[2];
-  __shared__ __align__(8) uint64_t bar_p, bar_s, bar_o;
+  __shared__ __align__(8) uint64_t bar_p, bar_s, bar_o, bar_fin;
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, hh = warp >> 2;
@@ -899,6 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     tc::mbar_init(&bar_p, 1);
     tc::mbar_init(&bar_s, 1);
     tc::mbar_init(&bar_o, 1);
+    tc::mbar_init(&bar_fin, 1);
     tc::mbar_fence_init();
   }
   float* s_ss = reinterpret_cast<float*>(sm + S_SS);
@@ -1142,8 +1163,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   if (!ok) {
     if (tid == 0) {
       latch_status(p.dev_status, KDA_DEV_TIMEOUT);
-      // let the bulk copies still in flight land before the CTA exits
+      // let the bulk copies still in flight land, and every product issued
+      // so far finish (a commit tracks all of them), before the CTA frees its
+      // TMEM and exits; each wait bounded
       for (int j = last_landed + 1; j <= last_issued; ++j) tc::mbar_wait(&bar_ld[j & 1], (j >> 1) & 1);
+      tc::mma_commit(&bar_fin);
+      tc::mbar_wait(&bar_fin, 0);
     }
   } else {
     store_pending_ck();
