@@ -345,6 +345,12 @@ def run_gpu(args):
         conv_call()
     barrier()
 
+    def gpu_lead():
+        # ~0.2 ms of GPU spin ahead of a start event, so that the host's own
+        # time to enqueue the timed call never shows up as GPU idle inside the
+        # timed interval (the spin itself lies before the start event)
+        torch.cuda._sleep(400_000)
+
     with ClockSampler(local) as clk:
         # prefill: per-iteration events around the call, L2 flushed before each
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -352,6 +358,7 @@ def run_gpu(args):
         barrier()
         for i in range(args.steps if with_prefill else 0):
             flush.fill_(float(i))
+            gpu_lead()
             starts[i].record(stream)
             prefill_call()
             ends[i].record(stream)
@@ -360,6 +367,7 @@ def run_gpu(args):
         # decode: back-to-back steps (each streams 1.07 GB through HBM)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
+        gpu_lead()
         e0.record(stream)
         for i in range(args.steps):
             decode_call(i)
@@ -369,6 +377,7 @@ def run_gpu(args):
         # speculative verification: K=4 draft tokens per sequence + commit
         e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
+        gpu_lead()
         e2.record(stream)
         for i in range(args.steps if with_spec else 0):
             spec_call()
@@ -382,6 +391,7 @@ def run_gpu(args):
         barrier()
         for i in range(args.steps if with_conv else 0):
             flush.fill_(float(i))
+            gpu_lead()
             cstarts[i].record(stream)
             conv_call()
             cends[i].record(stream)
@@ -445,6 +455,8 @@ def run_gpu(args):
         e2e_steps(2, w0)
     barrier()
     x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if with_prefill:
+        gpu_lead()
     x0.record(stream)
     if with_prefill:
         e2e_steps(args.steps, x0)

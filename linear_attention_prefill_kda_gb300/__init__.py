@@ -104,6 +104,41 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr()) if t.numel() > 0 else None
 
 
+def _need(t, name, shape=None, dtype=None):
+    """Raise ValueError unless ``t`` (when given) is a CUDA tensor of ``shape``
+    (None entries match any size) and ``dtype``.  The C ABI takes bare device
+    pointers, so a host tensor, a mismatched size or an int64 index array would
+    otherwise be read as something it is not."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if shape is not None and (t.dim() != len(shape) or any(
+            s is not None and int(a) != int(s) for a, s in zip(t.shape, shape))):
+        want = tuple("*" if s is None else int(s) for s in shape)
+        raise ValueError(f"{name} must have shape {want}, got {tuple(t.shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _need_prefill(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, checkpoints,
+                  ckpt_offsets, gate, norm_w, has_initial_state, dev_status):
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = state_indices.shape[0]
+    for name, t, shape in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("g", g, (T, H, dk)),
+                           ("v", v, (T, H, dv)), ("beta", beta, (T, H)), ("out", out, (T, H, dv)),
+                           ("gate", gate, (T, H, dv)), ("norm_w", norm_w, (dv,))):
+        _need(t, name, shape, q.dtype)
+    _need(cu_seqlens, "cu_seqlens", (N + 1,), torch.int32)
+    _need(state_indices, "state_indices", (N,), torch.int32)
+    _need(has_initial_state, "has_initial_state", (N,), torch.int32)
+    _need(ckpt_offsets, "ckpt_offsets", (N + 1,), torch.int32)
+    _need(state_pool, "state_pool", (None, H, dk, dv))
+    _need(checkpoints, "checkpoints", (None, H, dk, dv), state_pool.dtype)
+    _need(dev_status, "dev_status", None, torch.int32)
+
+
 def _dtype(t: torch.Tensor) -> int:
     if t.dtype == torch.float32:
         return KDA_F32
@@ -154,6 +189,9 @@ def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_indices, state_pool,
     """Chunked varlen prefill (see ``include/kda.h``).  All tensors on one
     CUDA device; ``state_pool`` is updated in place, ``out`` (and
     ``checkpoints``/``ckpt_offsets`` when given) are written."""
+    _need_prefill(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, checkpoints,
+                  ckpt_offsets, gate, norm_w, has_initial_state, dev_status)
+    _need(workspace, "workspace")
     T, H, dk = q.shape
     dv = v.shape[-1]
     N = state_indices.shape[0]
@@ -177,6 +215,8 @@ def kda_prefill_chunked_static_scratch(q, k, v, g, beta, cu_seqlens, state_indic
     """kda_prefill_chunked for callers that cannot allocate: the library's own
     device array (STATIC_SCRATCH_BYTES) replaces the workspace.  Calls share
     that array, so calls that overlap on the GPU race; see include/kda.h."""
+    _need_prefill(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, checkpoints,
+                  ckpt_offsets, gate, norm_w, has_initial_state, dev_status)
     T, H, dk = q.shape
     dv = v.shape[-1]
     N = state_indices.shape[0]
@@ -196,6 +236,13 @@ def kda_decode_step(q, k, v, g, beta, state_indices, state_pool, out, *, gate=No
     """One recurrent decode step for N one-token sequences (see ``include/kda.h``)."""
     N, H, dk = q.shape
     dv = v.shape[-1]
+    for name, t, shape in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("g", g, (N, H, dk)),
+                           ("v", v, (N, H, dv)), ("beta", beta, (N, H)), ("out", out, (N, H, dv)),
+                           ("gate", gate, (N, H, dv)), ("norm_w", norm_w, (dv,))):
+        _need(t, name, shape, q.dtype)
+    _need(state_indices, "state_indices", (N,), torch.int32)
+    _need(state_pool, "state_pool", (None, H, dk, dv))
+    _need(dev_status, "dev_status", None, torch.int32)
     st = load().kda_decode_step(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(state_indices), N,
         _ptr(state_pool), state_pool.shape[0], _dtype(state_pool), _ptr(out), _ptr(gate),
@@ -214,6 +261,15 @@ def kda_decode_multi(q, k, v, g, beta, state_indices, state_pool, out, token_sta
     """
     N, K, H, dk = q.shape
     dv = v.shape[-1]
+    for name, t, shape in (("q", q, (N, K, H, dk)), ("k", k, (N, K, H, dk)),
+                           ("g", g, (N, K, H, dk)), ("v", v, (N, K, H, dv)),
+                           ("beta", beta, (N, K, H)), ("out", out, (N, K, H, dv)),
+                           ("gate", gate, (N, K, H, dv)), ("norm_w", norm_w, (dv,))):
+        _need(t, name, shape, q.dtype)
+    _need(state_indices, "state_indices", (N,), torch.int32)
+    _need(state_pool, "state_pool", (None, H, dk, dv))
+    _need(token_states, "token_states", (N, K, H, dk, dv), state_pool.dtype)
+    _need(dev_status, "dev_status", None, torch.int32)
     st = load().kda_decode_multi(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(state_indices), N, K,
         _ptr(state_pool), state_pool.shape[0], _dtype(state_pool), _ptr(out), _ptr(token_states),
@@ -226,6 +282,11 @@ def kda_commit_accepted(token_states, num_accepted, state_indices, state_pool, *
                         dev_status=None, stream=None):
     """state_pool[idx_i] = token_states[i, a_i - 1] where a_i >= 1 (see ``include/kda.h``)."""
     N, K, H, dk, dv = token_states.shape
+    _need(token_states, "token_states")
+    _need(num_accepted, "num_accepted", (N,), torch.int32)
+    _need(state_indices, "state_indices", (N,), torch.int32)
+    _need(state_pool, "state_pool", (None, H, dk, dv), token_states.dtype)
+    _need(dev_status, "dev_status", None, torch.int32)
     st = load().kda_commit_accepted(
         _ptr(token_states), _ptr(num_accepted), _ptr(state_indices), N, K, _ptr(state_pool),
         state_pool.shape[0], _dtype(state_pool), H, dk, dv, _ptr(dev_status), _stream(stream))
@@ -242,6 +303,14 @@ def kda_causal_conv1d_prefill(x, weight, cu_seqlens, state_indices, conv_state_p
     x, y [T, C]; weight [C, W]; conv_state_pool [slots, W-1, C]."""
     T, C = x.shape
     N = state_indices.shape[0]
+    Wd = weight.shape[-1]
+    for name, t, shape in (("x", x, (T, C)), ("y", y, (T, C)), ("weight", weight, (C, Wd)),
+                           ("bias", bias, (C,)), ("conv_state_pool", conv_state_pool, (None, Wd - 1, C))):
+        _need(t, name, shape, x.dtype)
+    _need(cu_seqlens, "cu_seqlens", (N + 1,), torch.int32)
+    _need(state_indices, "state_indices", (N,), torch.int32)
+    _need(has_initial_state, "has_initial_state", (N,), torch.int32)
+    _need(dev_status, "dev_status", None, torch.int32)
     st = load().kda_causal_conv1d_prefill(
         _ptr(x), _ptr(weight), _ptr(bias), _dtype(x), _ptr(cu_seqlens), N, T, C, weight.shape[1],
         _ptr(state_indices), _ptr(has_initial_state), _ptr(conv_state_pool), conv_state_pool.shape[0],
@@ -253,6 +322,12 @@ def kda_causal_conv1d_decode(x, weight, state_indices, conv_state_pool, y, *, bi
                              act: str = "silu", dev_status=None, stream=None):
     """One token per sequence through the causal convolution: x, y [N, C]."""
     N, C = x.shape
+    Wd = weight.shape[-1]
+    for name, t, shape in (("x", x, (N, C)), ("y", y, (N, C)), ("weight", weight, (C, Wd)),
+                           ("bias", bias, (C,)), ("conv_state_pool", conv_state_pool, (None, Wd - 1, C))):
+        _need(t, name, shape, x.dtype)
+    _need(state_indices, "state_indices", (N,), torch.int32)
+    _need(dev_status, "dev_status", None, torch.int32)
     st = load().kda_causal_conv1d_decode(
         _ptr(x), _ptr(weight), _ptr(bias), _dtype(x), N, C, weight.shape[1], _ptr(state_indices),
         _ptr(conv_state_pool), conv_state_pool.shape[0], CONV_ACT[act], _ptr(y), _ptr(dev_status),
@@ -268,7 +343,13 @@ def kda_norm_gate_ex(o, gate, y, *, residual=None, residual_out=None, w=None, b=
     slice of a packed projection output): its row stride is passed as
     gate_row_stride."""
     rows, H, dv = o.shape
-    if tuple(gate.shape) != (rows, H, dv) or gate.stride(2) != 1 or gate.stride(1) != dv:
+    for name, t, shape in (("o", o, (rows, H, dv)), ("y", y, (rows, H, dv)),
+                           ("residual", residual, (rows, H, dv)),
+                           ("residual_out", residual_out, (rows, H, dv)), ("w", w, (dv,)),
+                           ("b", b, (dv,))):
+        _need(t, name, shape, o.dtype)
+    _need(gate, "gate", (rows, H, dv), o.dtype)
+    if gate.stride(2) != 1 or gate.stride(1) != dv:
         raise ValueError("gate must be [rows, H, dv] with contiguous heads and values")
     gptr = ctypes.c_void_p(gate.data_ptr()) if gate.numel() > 0 else None
     st = load().kda_norm_gate_ex(_ptr(o), _ptr(residual), _ptr(residual_out), gptr,
@@ -281,6 +362,9 @@ def kda_norm_gate_ex(o, gate, y, *, residual=None, residual_out=None, w=None, b=
 def kda_norm_gate(o, gate, w, y, *, eps: float = 1e-6, gate_act: str = "sigmoid", stream=None):
     """y = o / sqrt(mean(o^2)+eps) * w * act(gate) over the last dim of [rows, H, dv]."""
     rows, H, dv = o.shape
+    for name, t, shape in (("o", o, (rows, H, dv)), ("gate", gate, (rows, H, dv)), ("w", w, (dv,)),
+                           ("y", y, (rows, H, dv))):
+        _need(t, name, shape, o.dtype)
     st = load().kda_norm_gate(_ptr(o), _ptr(gate), _ptr(w), float(eps), GATE_ACT[gate_act],
                               _ptr(y), rows, H, dv, _dtype(o), _stream(stream))
     _check(st, "kda_norm_gate")

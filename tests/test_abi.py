@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import linear_attention_prefill_kda_gb300 as kda
 
@@ -230,3 +231,31 @@ def test_static_scratch_entry_rejects_oversize_on_host(lib):
     assert lib.kda_prefill_chunked_static_scratch(
         FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, 100, FAKE, None, FAKE, 4, 0, FAKE, None, 0, 0,
         None, None, None, 1e-6, 0, 2, 96, 96, 64, 0.0, None, None) == -2
+
+
+def test_binding_rejects_host_tensors_before_any_call():
+    """The binding hands bare device pointers to the ABI: host tensors are
+    refused with ValueError before the library is called."""
+    import pytest as _pt
+    q = torch.zeros(8, 2, 16, dtype=torch.bfloat16)
+    b = torch.zeros(8, 2, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 8], dtype=torch.int32)
+    idx = torch.zeros(1, dtype=torch.int32)
+    pool = torch.zeros(2, 2, 16, 16)
+    calls = [
+        lambda: kda.kda_prefill_chunked(q, q, q, q, b, cu, idx, pool, q),
+        lambda: kda.kda_prefill_chunked_static_scratch(q, q, q, q, b, cu, idx, pool, q),
+        lambda: kda.kda_decode_step(q[:1], q[:1], q[:1], q[:1], b[:1], idx, pool, q[:1]),
+        lambda: kda.kda_decode_multi(q[None, :1], q[None, :1], q[None, :1], q[None, :1], b[None, :1],
+                                     idx, pool, q[None, :1]),
+        lambda: kda.kda_commit_accepted(torch.zeros(1, 1, 2, 16, 16), idx, idx, pool),
+        lambda: kda.kda_causal_conv1d_prefill(q[:, 0], q[0, :, :2].T.contiguous(), cu, idx,
+                                              q[None, :1, 0], q[:, 0]),
+        lambda: kda.kda_causal_conv1d_decode(q[:1, 0], q[0, :, :2].T.contiguous(), idx,
+                                             q[None, :1, 0], q[:1, 0]),
+        lambda: kda.kda_norm_gate(q, q, q[0, 0], q),
+        lambda: kda.kda_norm_gate_ex(q, q, q),
+    ]
+    for call in calls:
+        with _pt.raises(ValueError, match="CUDA tensor"):
+            call()

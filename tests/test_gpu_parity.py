@@ -567,6 +567,36 @@ def test_norm_gate(kda_gpu, dv, dtype, inplace, act):
         assert torch.equal(od.cpu(), o)  # input preserved
 
 
+def test_binding_rejects_mismatched_arguments(kda_gpu):
+    """A size that disagrees with q, an int64 index array or a host tensor among
+    device tensors raise ValueError in the binding; nothing is launched."""
+    w = W.VARLEN
+    d = W.make_prefill(w)
+    t = to_dev(d, DEV)
+    T = t["q"].shape[0]
+    out = torch.full((T, w.H, w.dv), 7.0, device=DEV, dtype=w.in_dtype)
+    ws = torch.empty(kda_gpu.kda_prefill_workspace_bytes(w.N, T, w.H, w.dk, w.dv, w.chunk) + 16,
+                     dtype=torch.uint8, device=DEV)
+
+    def call(**over):
+        a = dict(t, out=out)
+        a.update(over)
+        kda_gpu.kda_prefill_chunked(a["q"], a["k"], a["v"], a["g"], a["beta"], a["cu_seqlens"],
+                                    a["state_indices"], a["pool"], a["out"], chunk=w.chunk,
+                                    workspace=ws)
+
+    with pytest.raises(ValueError, match="k must have shape"):
+        call(k=t["k"][:-1])
+    with pytest.raises(ValueError, match="state_indices must be torch.int32"):
+        call(state_indices=t["state_indices"].long())
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        call(beta=d["beta"])
+    with pytest.raises(ValueError, match="out must have shape"):
+        call(out=out[:, :, :-1].contiguous())
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())  # nothing ran
+
+
 @pytest.mark.parametrize("dim", [64, 128])
 def test_graph_capture_replay(kda_gpu, dim):
     """A prefill and a decode step captured in one CUDA graph and replayed give
