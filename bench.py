@@ -10,15 +10,22 @@ Workloads (seeded synthetic inputs, no dataset):
            states kept) followed by the commit of the accepted prefixes.
   conv     the short causal convolution (width 4, SiLU) over the scheduler
            step's q, k, v projections (12288 channels), with its cache pool.
-A step is one prefill call, one decode step, one verify + commit and one
-convolution call; each is timed in its own loop with CUDA events on the launching stream, the L2 flushed (a 256 MiB
-write) before every timed prefill call (the decode step streams 1.07 GB, far
-above L2).  ``value`` is prefill tokens/s; the decode and verification
-figures sit under ``decode``, ``spec_decode`` and ``conv_prefill``.  ``e2e``
-is prefill tokens/s with every step's inputs copied in from pinned host memory
-and its output copied back, steps pipelined over two copy streams.
-``--impl reference`` times the fp64 CPU oracle on the same workload instead.  Under torchrun each rank runs an independent replica (the
-path has no exchange step) and rank 0 reports the aggregate.
+  long     one 32768-token prompt as 8 calls of 4096 tokens carrying a bf16
+           state through the pool, bf16 checkpoints every 256 tokens, no gate.
+A step is one prefill call, one decode step, one verify + commit, one
+convolution call and the 8 long-prompt calls; each is timed in its own loop
+with CUDA events on the launching stream, the L2 flushed (a 256 MiB write)
+before every timed prefill, convolution and long-prompt call (the decode step
+streams 1.07 GB, far above L2).  ``value`` is prefill tokens/s of the
+scheduler step; the other figures sit under ``decode``, ``spec_decode``,
+``conv_prefill`` and ``longprompt``.  ``e2e`` is scheduler-step prefill
+tokens/s with every step's inputs copied in from pinned host memory and its
+output copied back, steps pipelined over two copy streams.
+``--impl reference`` times the fp64 CPU oracle on the same workload instead.
+``--gpus N`` (N > 1) runs N independent replicas, one process per GPU: launched
+without torchrun, the script starts them itself under torch.distributed.run;
+launched as ranks (WORLD_SIZE set), each rank is one replica.  The path has no
+exchange step, so no collective touches the data; rank 0 reports the aggregate.
 """
 from __future__ import annotations
 
@@ -301,6 +308,33 @@ def run_gpu(args):
         cdev = {k: v.to(dev) for k, v in cdat.items()}
         cy = torch.empty_like(cdev["x"])
 
+    # ---------------- long prompt with bf16 state: 32768 tokens as 8 calls of
+    # 4096 carrying the state through the pool, checkpoints every 256 tokens
+    with_long = args.workload in ("both", "longprompt")
+    lw = W.LONGPROMPT
+    LSEG = 4096
+    if with_long:
+        ld = W.make_prefill(lw)
+        lsrc = {k: ld[k].to(dev) for k in ("q", "k", "v", "g", "beta")}
+        lpool0 = ld["pool"].to(dev)
+        lpool = lpool0.clone()
+        lidx = ld["state_indices"].to(dev)
+        lcu = W.cu_from_lengths([LSEG]).to(dev)
+        lout = torch.empty(lw.T, lw.H, lw.dv, device=dev, dtype=lw.in_dtype)
+        lck = torch.empty(lw.T // lw.checkpoint_every, lw.H, lw.dk, lw.dv, device=dev,
+                          dtype=lw.state_dtype)
+        lwsb = kda.kda_prefill_workspace_bytes(1, LSEG, lw.H, lw.dk, lw.dv, lw.chunk)
+        lws = torch.empty(lwsb, dtype=torch.uint8, device=dev) if lwsb else None
+        lper = LSEG // lw.checkpoint_every
+
+    def long_call(c):
+        sl = slice(c * LSEG, (c + 1) * LSEG)
+        kda.kda_prefill_chunked(lsrc["q"][sl], lsrc["k"][sl], lsrc["v"][sl], lsrc["g"][sl],
+                                lsrc["beta"][sl], lcu, lidx, lpool, lout[sl], chunk=lw.chunk,
+                                checkpoints=lck[c * lper:(c + 1) * lper],
+                                checkpoint_every=lw.checkpoint_every, workspace=lws,
+                                dev_status=status, stream=stream)
+
     def conv_call():
         if not with_conv:
             return
@@ -343,6 +377,10 @@ def run_gpu(args):
         decode_call(0)
         spec_call()
         conv_call()
+        if with_long:
+            lpool.copy_(lpool0)
+            for c in range(lw.T // LSEG):
+                long_call(c)
     barrier()
 
     def gpu_lead():
@@ -398,6 +436,23 @@ def run_gpu(args):
         barrier()
         conv_ms = (sum(a.elapsed_time(b) for a, b in zip(cstarts, cends)) / args.steps
                    if with_conv else float("nan"))
+        # long prompt: each step is the 8 carried calls from the initial state;
+        # every call timed on its own, the L2 flushed before it
+        ncall = lw.T // LSEG
+        lstarts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps * ncall)]
+        lends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps * ncall)]
+        barrier()
+        for i in range(args.steps if with_long else 0):
+            lpool.copy_(lpool0)
+            for c in range(ncall):
+                flush.fill_(float(i))
+                gpu_lead()
+                lstarts[i * ncall + c].record(stream)
+                long_call(c)
+                lends[i * ncall + c].record(stream)
+        barrier()
+        long_ms = (sum(a.elapsed_time(b) for a, b in zip(lstarts, lends)) / (args.steps * ncall)
+                   if with_long else float("nan"))
     clocks = clk.summary()
     st = int(status.item())
     if st != 0:
@@ -406,8 +461,8 @@ def run_gpu(args):
     pre_ms_mean = sum(pre_ms) / len(pre_ms)
     dec_ms = dec_ms_total / args.steps
     spec_ms = spec_ms_total / args.steps if with_spec else float("nan")
-    pre_ms_mean, dec_ms, spec_ms, conv_ms = max_over_ranks([pre_ms_mean, dec_ms, spec_ms, conv_ms],
-                                                          dev)
+    pre_ms_mean, dec_ms, spec_ms, conv_ms, long_ms = max_over_ranks(
+        [pre_ms_mean, dec_ms, spec_ms, conv_ms, long_ms], dev)
 
     # ---------------- e2e through the public API with host buffers
     # Every step copies its inputs in from pinned host memory and its output
@@ -480,6 +535,9 @@ def run_gpu(args):
     spec_bytes = spec_algorithmic(dw, SPEC_K, sacc_host) if with_spec else 0
     spec_gbs = rate(spec_bytes, spec_ms) / 1e9
     conv_bytes = conv_algorithmic(w, CONV_C, CONV_W) if with_conv else 0
+    lw_seg = lw.replace(seqlens=(LSEG,))
+    long_bytes, long_flops = prefill_algorithmic(lw_seg, {"cu_seqlens": W.cu_from_lengths([LSEG])})
+    long_gbs = rate(long_bytes, long_ms) / 1e9
     conv_gbs = rate(conv_bytes, conv_ms) / 1e9
     tokens_s = replica_rate(T, ws, pre_ms_mean)
     seqsteps_s = replica_rate(dw.N, ws, dec_ms)
@@ -532,12 +590,25 @@ def run_gpu(args):
                                       "frac": round(conv_gbs / pk["hbm"], 4),
                                       "traffic": recorded_traffic("conv", "conv_call_dram_bytes"),
                                       "algorithmic_bytes": conv_bytes}},
+        "longprompt": {"workload": lw.name, "value": round(replica_rate(LSEG, ws, long_ms), 1),
+                       "unit": "tokens/s", "calls": lw.T // LSEG, "tokens_per_call": LSEG,
+                       "ms_per_call": round(long_ms, 4), "state_dtype": "bf16",
+                       "checkpoint_every": lw.checkpoint_every,
+                       "roofline": {"bound": "hbm", "achieved": round(long_gbs, 1),
+                                    "peak": pk["hbm"], "unit": "GB/s",
+                                    "frac": round(long_gbs / pk["hbm"], 4),
+                                    "traffic": recorded_traffic("prefill",
+                                                                "longprompt_call_dram_bytes"),
+                                    "algorithmic_bytes": long_bytes,
+                                    "algorithmic_flops": long_flops,
+                                    "achieved_tflops": round(rate(long_flops, long_ms) / 1e12, 2)}},
         "e2e": {"value": round(replica_rate(T, ws, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipelined": "step i+1's inputs copied in while step i computes and its output "
                              "is copied out (two copy streams, double-buffered staging)"},
         "gpu_launches": args.steps * (prefill_launches(kda, w) * with_prefill + with_decode
-                                      + 2 * with_spec + with_conv),
+                                      + 2 * with_spec + with_conv
+                                      + (lw.T // LSEG) * prefill_launches(kda, lw) * with_long),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -639,6 +710,20 @@ def _nan_to_none(x):
     return x
 
 
+def spawn_replicas(n: int, argv) -> int:
+    """Run this script as ``n`` replica processes (one per GPU, ranks 0..n-1)
+    under torch.distributed.run on this node and return its exit status.  Each
+    replica runs the whole workload on its own GPU; rank 0 prints the line."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd, cwd=ROOT).returncode
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -647,12 +732,22 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["libkda", "reference"], default="libkda")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["both", "prefill", "decode", "spec", "conv"],
+    ap.add_argument("--workload", choices=["both", "prefill", "decode", "spec", "conv",
+                                           "longprompt"],
                     default="both",
                     help="time every part (default) or one of them (for profiling runs)")
-    args = ap.parse_args(argv)
+    raw = list(sys.argv[1:] if argv is None else argv)
+    args = ap.parse_args(raw)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # not launched as ranks yet: start one replica per GPU ourselves
+        sys.exit(spawn_replicas(args.gpus, raw))
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but launched with WORLD_SIZE={world}")
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
         print(json.dumps(_nan_to_none(res)), flush=True)

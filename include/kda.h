@@ -297,8 +297,10 @@ KDA_API kda_status kda_causal_conv1d_decode(const void* x, const void* weight, c
  * library holds until the process exits.  A call whose scratch need
  * (kda_prefill_workspace_bytes bounds it) exceeds that size returns
  * KDA_ERR_WORKSPACE without launching.  The first call on each device looks up
- * the array's device address and caches it, so make that first call before
- * any stream capture starts.  Every call shares the array: calls whose kernels
+ * the array's device address and caches it for the device's current context,
+ * so make that first call before any stream capture starts; after
+ * cudaDeviceReset (or from another context) the next call looks it up again,
+ * and that call, too, belongs before any capture.  Every call shares the array: calls whose kernels
  * overlap on the GPU (different streams, or different host threads) race on it
  * and must be serialised by the caller.  No allocation happens in this call.
  */
@@ -310,6 +312,18 @@ KDA_API kda_status kda_prefill_chunked_static_scratch(
     void* out, void* checkpoints, int32_t checkpoint_every, int64_t checkpoint_capacity,
     int32_t* ckpt_offsets, const void* gate, const void* norm_w, float eps, kda_gate_act gate_act,
     int H, int dk, int dv, int chunk, float scale, int32_t* dev_status, void* stream);
+
+/*
+ * Testing only: the number of polls the first bounded on-chip wait of each
+ * prefill kernel makes before it gives up (the other waits keep their limit,
+ * so the clean-up after a timed-out wait still lets every copy and product in
+ * flight finish).  tries < 0 restores the default.  The setting is process
+ * wide and applies to kda_prefill_chunked and
+ * kda_prefill_chunked_static_scratch launches made after the call; it exists
+ * so that a test can make a wait run out (KDA_DEV_TIMEOUT) without touching
+ * any other part of the GPU.  Not for production use.
+ */
+KDA_API void kda_testing_set_first_wait_tries(int32_t tries);
 
 /* A static, human-readable name for a kda_status value. */
 KDA_API const char* kda_status_string(kda_status status);

@@ -20,7 +20,7 @@ __all__ = [
     "kda_status_string", "kda_version", "DEV_STATUS", "prefill_launches",
     "kda_prefill_chunked_static_scratch", "STATIC_SCRATCH_BYTES", "kda_decode_multi",
     "kda_commit_accepted", "kda_norm_gate_ex", "KDA_F16", "kda_causal_conv1d_prefill",
-    "kda_causal_conv1d_decode",
+    "kda_causal_conv1d_decode", "kda_testing_set_first_wait_tries",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -68,6 +68,7 @@ _SIGNATURES = {
         _P, _P, _I32, _I64, _P, _P, _P, _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_int, _F32, _P, _P]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "kda_testing_set_first_wait_tries": (None, [_I32]),
     "kda_version": (ctypes.c_int, []),
 }
 
@@ -104,14 +105,21 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr()) if t.numel() > 0 else None
 
 
-def _need(t, name, shape=None, dtype=None):
-    """Raise ValueError unless ``t`` (when given) is a CUDA tensor of ``shape``
-    (None entries match any size) and ``dtype``.  The C ABI takes bare device
-    pointers, so a host tensor, a mismatched size or an int64 index array would
-    otherwise be read as something it is not."""
+def _need(t, name, shape=None, dtype=None, device=None):
+    """Raise ValueError unless ``t`` (when given) is a CUDA tensor on ``device``
+    (the device of the call's first tensor), of ``shape`` (None entries match
+    any size) and ``dtype``.  The C ABI takes bare device pointers and launches
+    on the current device, so a host tensor, a tensor on another GPU, a
+    mismatched size or an int64 index array would otherwise be read as
+    something it is not."""
     if t is None:
         return
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device} but the call's tensors are on {device}: "
+                         "every tensor of a call must be on one CUDA device")
+    if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if shape is not None and (t.dim() != len(shape) or any(
             s is not None and int(a) != int(s) for a, s in zip(t.shape, shape))):
@@ -121,22 +129,36 @@ def _need(t, name, shape=None, dtype=None):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _one_device(dev, **tensors):
+    """Raise ValueError unless every given tensor is on ``dev``; runs before
+    the per-tensor checks so that a mixed call is named as such."""
+    for name, t in tensors.items():
+        if isinstance(t, torch.Tensor) and t.device != dev:
+            raise ValueError(f"{name} is on {t.device} but the call's tensors are on {dev}: "
+                             "every tensor of a call must be on one CUDA device")
+
+
 def _need_prefill(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, checkpoints,
                   ckpt_offsets, gate, norm_w, has_initial_state, dev_status):
     T, H, dk = q.shape
     dv = v.shape[-1]
     N = state_indices.shape[0]
+    dev = q.device
+    _one_device(dev, k=k, v=v, g=g, beta=beta, cu_seqlens=cu_seqlens, state_indices=state_indices,
+                state_pool=state_pool, out=out, checkpoints=checkpoints, ckpt_offsets=ckpt_offsets,
+                gate=gate, norm_w=norm_w, has_initial_state=has_initial_state, dev_status=dev_status)
     for name, t, shape in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("g", g, (T, H, dk)),
                            ("v", v, (T, H, dv)), ("beta", beta, (T, H)), ("out", out, (T, H, dv)),
                            ("gate", gate, (T, H, dv)), ("norm_w", norm_w, (dv,))):
-        _need(t, name, shape, q.dtype)
-    _need(cu_seqlens, "cu_seqlens", (N + 1,), torch.int32)
-    _need(state_indices, "state_indices", (N,), torch.int32)
-    _need(has_initial_state, "has_initial_state", (N,), torch.int32)
-    _need(ckpt_offsets, "ckpt_offsets", (N + 1,), torch.int32)
-    _need(state_pool, "state_pool", (None, H, dk, dv))
-    _need(checkpoints, "checkpoints", (None, H, dk, dv), state_pool.dtype)
-    _need(dev_status, "dev_status", None, torch.int32)
+        _need(t, name, shape, q.dtype, dev)
+    _need(cu_seqlens, "cu_seqlens", (N + 1,), torch.int32, dev)
+    _need(state_indices, "state_indices", (N,), torch.int32, dev)
+    _need(has_initial_state, "has_initial_state", (N,), torch.int32, dev)
+    _need(ckpt_offsets, "ckpt_offsets", (N + 1,), torch.int32, dev)
+    _need(state_pool, "state_pool", (None, H, dk, dv), None, dev)
+    _need(checkpoints, "checkpoints", (None, H, dk, dv), state_pool.dtype, dev)
+    _need(dev_status, "dev_status", None, torch.int32, dev)
+    return dev
 
 
 def _dtype(t: torch.Tensor) -> int:
@@ -149,9 +171,13 @@ def _dtype(t: torch.Tensor) -> int:
     raise ValueError(f"unsupported dtype {t.dtype}")
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _stream(stream, dev) -> ctypes.c_void_p:
+    """Raw handle of ``stream`` (default: the current stream of ``dev``, the
+    device of the call's tensors); a given stream must belong to ``dev``."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(dev)
+    elif stream.device != dev:
+        raise ValueError(f"stream is on {stream.device} but the call's tensors are on {dev}")
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -166,6 +192,13 @@ def kda_status_string(status: int) -> str:
 
 def kda_version() -> int:
     return load().kda_version()
+
+
+def kda_testing_set_first_wait_tries(tries: int) -> None:
+    """Testing only (see ``include/kda.h``): polls of the first bounded wait
+    of each prefill kernel launched from now on; a negative value restores the
+    default."""
+    load().kda_testing_set_first_wait_tries(int(tries))
 
 
 def kda_prefill_workspace_bytes(N: int, T: int, H: int, dk: int, dv: int, chunk: int) -> int:
@@ -189,20 +222,21 @@ def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_indices, state_pool,
     """Chunked varlen prefill (see ``include/kda.h``).  All tensors on one
     CUDA device; ``state_pool`` is updated in place, ``out`` (and
     ``checkpoints``/``ckpt_offsets`` when given) are written."""
-    _need_prefill(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, checkpoints,
-                  ckpt_offsets, gate, norm_w, has_initial_state, dev_status)
-    _need(workspace, "workspace")
+    dev = _need_prefill(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, checkpoints,
+                        ckpt_offsets, gate, norm_w, has_initial_state, dev_status)
+    _need(workspace, "workspace", None, None, dev)
     T, H, dk = q.shape
     dv = v.shape[-1]
     N = state_indices.shape[0]
     cap = checkpoints.shape[0] if checkpoints is not None else 0
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = load().kda_prefill_chunked(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(cu_seqlens), N, T,
-        _ptr(state_indices), _ptr(has_initial_state), _ptr(state_pool), state_pool.shape[0],
-        _dtype(state_pool), _ptr(out), _ptr(checkpoints), int(checkpoint_every), cap,
-        _ptr(ckpt_offsets), _ptr(gate), _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk, dv,
-        int(chunk), float(scale), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
+    with torch.cuda.device(dev):
+        st = load().kda_prefill_chunked(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(cu_seqlens), N, T,
+            _ptr(state_indices), _ptr(has_initial_state), _ptr(state_pool), state_pool.shape[0],
+            _dtype(state_pool), _ptr(out), _ptr(checkpoints), int(checkpoint_every), cap,
+            _ptr(ckpt_offsets), _ptr(gate), _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk, dv,
+            int(chunk), float(scale), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream, dev))
     _check(st, "kda_prefill_chunked")
 
 
@@ -215,18 +249,19 @@ def kda_prefill_chunked_static_scratch(q, k, v, g, beta, cu_seqlens, state_indic
     """kda_prefill_chunked for callers that cannot allocate: the library's own
     device array (STATIC_SCRATCH_BYTES) replaces the workspace.  Calls share
     that array, so calls that overlap on the GPU race; see include/kda.h."""
-    _need_prefill(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, checkpoints,
-                  ckpt_offsets, gate, norm_w, has_initial_state, dev_status)
+    dev = _need_prefill(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, checkpoints,
+                        ckpt_offsets, gate, norm_w, has_initial_state, dev_status)
     T, H, dk = q.shape
     dv = v.shape[-1]
     N = state_indices.shape[0]
     cap = checkpoints.shape[0] if checkpoints is not None else 0
-    st = load().kda_prefill_chunked_static_scratch(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(cu_seqlens), N, T,
-        _ptr(state_indices), _ptr(has_initial_state), _ptr(state_pool), state_pool.shape[0],
-        _dtype(state_pool), _ptr(out), _ptr(checkpoints), int(checkpoint_every), cap,
-        _ptr(ckpt_offsets), _ptr(gate), _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk, dv,
-        int(chunk), float(scale), _ptr(dev_status), _stream(stream))
+    with torch.cuda.device(dev):
+        st = load().kda_prefill_chunked_static_scratch(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(cu_seqlens), N, T,
+            _ptr(state_indices), _ptr(has_initial_state), _ptr(state_pool), state_pool.shape[0],
+            _dtype(state_pool), _ptr(out), _ptr(checkpoints), int(checkpoint_every), cap,
+            _ptr(ckpt_offsets), _ptr(gate), _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk, dv,
+            int(chunk), float(scale), _ptr(dev_status), _stream(stream, dev))
     _check(st, "kda_prefill_chunked_static_scratch")
 
 
@@ -236,18 +271,22 @@ def kda_decode_step(q, k, v, g, beta, state_indices, state_pool, out, *, gate=No
     """One recurrent decode step for N one-token sequences (see ``include/kda.h``)."""
     N, H, dk = q.shape
     dv = v.shape[-1]
+    dev = q.device
+    _one_device(dev, k=k, v=v, g=g, beta=beta, state_indices=state_indices, state_pool=state_pool,
+                out=out, gate=gate, norm_w=norm_w, dev_status=dev_status)
     for name, t, shape in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("g", g, (N, H, dk)),
                            ("v", v, (N, H, dv)), ("beta", beta, (N, H)), ("out", out, (N, H, dv)),
                            ("gate", gate, (N, H, dv)), ("norm_w", norm_w, (dv,))):
-        _need(t, name, shape, q.dtype)
-    _need(state_indices, "state_indices", (N,), torch.int32)
-    _need(state_pool, "state_pool", (None, H, dk, dv))
-    _need(dev_status, "dev_status", None, torch.int32)
-    st = load().kda_decode_step(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(state_indices), N,
-        _ptr(state_pool), state_pool.shape[0], _dtype(state_pool), _ptr(out), _ptr(gate),
-        _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk, dv, float(scale), _ptr(dev_status),
-        _stream(stream))
+        _need(t, name, shape, q.dtype, dev)
+    _need(state_indices, "state_indices", (N,), torch.int32, dev)
+    _need(state_pool, "state_pool", (None, H, dk, dv), None, dev)
+    _need(dev_status, "dev_status", None, torch.int32, dev)
+    with torch.cuda.device(dev):
+        st = load().kda_decode_step(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(state_indices), N,
+            _ptr(state_pool), state_pool.shape[0], _dtype(state_pool), _ptr(out), _ptr(gate),
+            _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk, dv, float(scale), _ptr(dev_status),
+            _stream(stream, dev))
     _check(st, "kda_decode_step")
 
 
@@ -261,20 +300,25 @@ def kda_decode_multi(q, k, v, g, beta, state_indices, state_pool, out, token_sta
     """
     N, K, H, dk = q.shape
     dv = v.shape[-1]
+    dev = q.device
+    _one_device(dev, k=k, v=v, g=g, beta=beta, state_indices=state_indices, state_pool=state_pool,
+                out=out, token_states=token_states, gate=gate, norm_w=norm_w,
+                dev_status=dev_status)
     for name, t, shape in (("q", q, (N, K, H, dk)), ("k", k, (N, K, H, dk)),
                            ("g", g, (N, K, H, dk)), ("v", v, (N, K, H, dv)),
                            ("beta", beta, (N, K, H)), ("out", out, (N, K, H, dv)),
                            ("gate", gate, (N, K, H, dv)), ("norm_w", norm_w, (dv,))):
-        _need(t, name, shape, q.dtype)
-    _need(state_indices, "state_indices", (N,), torch.int32)
-    _need(state_pool, "state_pool", (None, H, dk, dv))
-    _need(token_states, "token_states", (N, K, H, dk, dv), state_pool.dtype)
-    _need(dev_status, "dev_status", None, torch.int32)
-    st = load().kda_decode_multi(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(state_indices), N, K,
-        _ptr(state_pool), state_pool.shape[0], _dtype(state_pool), _ptr(out), _ptr(token_states),
-        int(bool(write_back)), _ptr(gate), _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk,
-        dv, float(scale), _ptr(dev_status), _stream(stream))
+        _need(t, name, shape, q.dtype, dev)
+    _need(state_indices, "state_indices", (N,), torch.int32, dev)
+    _need(state_pool, "state_pool", (None, H, dk, dv), None, dev)
+    _need(token_states, "token_states", (N, K, H, dk, dv), state_pool.dtype, dev)
+    _need(dev_status, "dev_status", None, torch.int32, dev)
+    with torch.cuda.device(dev):
+        st = load().kda_decode_multi(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype(q), _ptr(state_indices), N, K,
+            _ptr(state_pool), state_pool.shape[0], _dtype(state_pool), _ptr(out), _ptr(token_states),
+            int(bool(write_back)), _ptr(gate), _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk,
+            dv, float(scale), _ptr(dev_status), _stream(stream, dev))
     _check(st, "kda_decode_multi")
 
 
@@ -282,14 +326,18 @@ def kda_commit_accepted(token_states, num_accepted, state_indices, state_pool, *
                         dev_status=None, stream=None):
     """state_pool[idx_i] = token_states[i, a_i - 1] where a_i >= 1 (see ``include/kda.h``)."""
     N, K, H, dk, dv = token_states.shape
-    _need(token_states, "token_states")
-    _need(num_accepted, "num_accepted", (N,), torch.int32)
-    _need(state_indices, "state_indices", (N,), torch.int32)
-    _need(state_pool, "state_pool", (None, H, dk, dv), token_states.dtype)
-    _need(dev_status, "dev_status", None, torch.int32)
-    st = load().kda_commit_accepted(
-        _ptr(token_states), _ptr(num_accepted), _ptr(state_indices), N, K, _ptr(state_pool),
-        state_pool.shape[0], _dtype(state_pool), H, dk, dv, _ptr(dev_status), _stream(stream))
+    dev = token_states.device
+    _one_device(dev, num_accepted=num_accepted, state_indices=state_indices,
+                state_pool=state_pool, dev_status=dev_status)
+    _need(token_states, "token_states", None, None, dev)
+    _need(num_accepted, "num_accepted", (N,), torch.int32, dev)
+    _need(state_indices, "state_indices", (N,), torch.int32, dev)
+    _need(state_pool, "state_pool", (None, H, dk, dv), token_states.dtype, dev)
+    _need(dev_status, "dev_status", None, torch.int32, dev)
+    with torch.cuda.device(dev):
+        st = load().kda_commit_accepted(
+            _ptr(token_states), _ptr(num_accepted), _ptr(state_indices), N, K, _ptr(state_pool),
+            state_pool.shape[0], _dtype(state_pool), H, dk, dv, _ptr(dev_status), _stream(stream, dev))
     _check(st, "kda_commit_accepted")
 
 
@@ -304,17 +352,22 @@ def kda_causal_conv1d_prefill(x, weight, cu_seqlens, state_indices, conv_state_p
     T, C = x.shape
     N = state_indices.shape[0]
     Wd = weight.shape[-1]
+    dev = x.device
+    _one_device(dev, weight=weight, cu_seqlens=cu_seqlens, state_indices=state_indices,
+                conv_state_pool=conv_state_pool, y=y, bias=bias,
+                has_initial_state=has_initial_state, dev_status=dev_status)
     for name, t, shape in (("x", x, (T, C)), ("y", y, (T, C)), ("weight", weight, (C, Wd)),
                            ("bias", bias, (C,)), ("conv_state_pool", conv_state_pool, (None, Wd - 1, C))):
-        _need(t, name, shape, x.dtype)
-    _need(cu_seqlens, "cu_seqlens", (N + 1,), torch.int32)
-    _need(state_indices, "state_indices", (N,), torch.int32)
-    _need(has_initial_state, "has_initial_state", (N,), torch.int32)
-    _need(dev_status, "dev_status", None, torch.int32)
-    st = load().kda_causal_conv1d_prefill(
-        _ptr(x), _ptr(weight), _ptr(bias), _dtype(x), _ptr(cu_seqlens), N, T, C, weight.shape[1],
-        _ptr(state_indices), _ptr(has_initial_state), _ptr(conv_state_pool), conv_state_pool.shape[0],
-        CONV_ACT[act], _ptr(y), _ptr(dev_status), _stream(stream))
+        _need(t, name, shape, x.dtype, dev)
+    _need(cu_seqlens, "cu_seqlens", (N + 1,), torch.int32, dev)
+    _need(state_indices, "state_indices", (N,), torch.int32, dev)
+    _need(has_initial_state, "has_initial_state", (N,), torch.int32, dev)
+    _need(dev_status, "dev_status", None, torch.int32, dev)
+    with torch.cuda.device(dev):
+        st = load().kda_causal_conv1d_prefill(
+            _ptr(x), _ptr(weight), _ptr(bias), _dtype(x), _ptr(cu_seqlens), N, T, C, weight.shape[1],
+            _ptr(state_indices), _ptr(has_initial_state), _ptr(conv_state_pool), conv_state_pool.shape[0],
+            CONV_ACT[act], _ptr(y), _ptr(dev_status), _stream(stream, dev))
     _check(st, "kda_causal_conv1d_prefill")
 
 
@@ -323,15 +376,19 @@ def kda_causal_conv1d_decode(x, weight, state_indices, conv_state_pool, y, *, bi
     """One token per sequence through the causal convolution: x, y [N, C]."""
     N, C = x.shape
     Wd = weight.shape[-1]
+    dev = x.device
+    _one_device(dev, weight=weight, state_indices=state_indices, conv_state_pool=conv_state_pool,
+                y=y, bias=bias, dev_status=dev_status)
     for name, t, shape in (("x", x, (N, C)), ("y", y, (N, C)), ("weight", weight, (C, Wd)),
                            ("bias", bias, (C,)), ("conv_state_pool", conv_state_pool, (None, Wd - 1, C))):
-        _need(t, name, shape, x.dtype)
-    _need(state_indices, "state_indices", (N,), torch.int32)
-    _need(dev_status, "dev_status", None, torch.int32)
-    st = load().kda_causal_conv1d_decode(
-        _ptr(x), _ptr(weight), _ptr(bias), _dtype(x), N, C, weight.shape[1], _ptr(state_indices),
-        _ptr(conv_state_pool), conv_state_pool.shape[0], CONV_ACT[act], _ptr(y), _ptr(dev_status),
-        _stream(stream))
+        _need(t, name, shape, x.dtype, dev)
+    _need(state_indices, "state_indices", (N,), torch.int32, dev)
+    _need(dev_status, "dev_status", None, torch.int32, dev)
+    with torch.cuda.device(dev):
+        st = load().kda_causal_conv1d_decode(
+            _ptr(x), _ptr(weight), _ptr(bias), _dtype(x), N, C, weight.shape[1], _ptr(state_indices),
+            _ptr(conv_state_pool), conv_state_pool.shape[0], CONV_ACT[act], _ptr(y), _ptr(dev_status),
+            _stream(stream, dev))
     _check(st, "kda_causal_conv1d_decode")
 
 
@@ -343,28 +400,34 @@ def kda_norm_gate_ex(o, gate, y, *, residual=None, residual_out=None, w=None, b=
     slice of a packed projection output): its row stride is passed as
     gate_row_stride."""
     rows, H, dv = o.shape
+    dev = o.device
+    _one_device(dev, gate=gate, y=y, residual=residual, residual_out=residual_out, w=w, b=b)
     for name, t, shape in (("o", o, (rows, H, dv)), ("y", y, (rows, H, dv)),
                            ("residual", residual, (rows, H, dv)),
                            ("residual_out", residual_out, (rows, H, dv)), ("w", w, (dv,)),
                            ("b", b, (dv,))):
-        _need(t, name, shape, o.dtype)
-    _need(gate, "gate", (rows, H, dv), o.dtype)
+        _need(t, name, shape, o.dtype, dev)
+    _need(gate, "gate", (rows, H, dv), o.dtype, dev)
     if gate.stride(2) != 1 or gate.stride(1) != dv:
         raise ValueError("gate must be [rows, H, dv] with contiguous heads and values")
     gptr = ctypes.c_void_p(gate.data_ptr()) if gate.numel() > 0 else None
-    st = load().kda_norm_gate_ex(_ptr(o), _ptr(residual), _ptr(residual_out), gptr,
-                                 int(gate.stride(0)) if rows > 1 else 0, _ptr(w), _ptr(b),
-                                 float(eps), GATE_ACT[gate_act], _ptr(y), rows, H, dv, _dtype(o),
-                                 _stream(stream))
+    with torch.cuda.device(dev):
+        st = load().kda_norm_gate_ex(_ptr(o), _ptr(residual), _ptr(residual_out), gptr,
+                                     int(gate.stride(0)) if rows > 1 else 0, _ptr(w), _ptr(b),
+                                     float(eps), GATE_ACT[gate_act], _ptr(y), rows, H, dv, _dtype(o),
+                                     _stream(stream, dev))
     _check(st, "kda_norm_gate_ex")
 
 
 def kda_norm_gate(o, gate, w, y, *, eps: float = 1e-6, gate_act: str = "sigmoid", stream=None):
     """y = o / sqrt(mean(o^2)+eps) * w * act(gate) over the last dim of [rows, H, dv]."""
     rows, H, dv = o.shape
+    dev = o.device
+    _one_device(dev, gate=gate, w=w, y=y)
     for name, t, shape in (("o", o, (rows, H, dv)), ("gate", gate, (rows, H, dv)), ("w", w, (dv,)),
                            ("y", y, (rows, H, dv))):
-        _need(t, name, shape, o.dtype)
-    st = load().kda_norm_gate(_ptr(o), _ptr(gate), _ptr(w), float(eps), GATE_ACT[gate_act],
-                              _ptr(y), rows, H, dv, _dtype(o), _stream(stream))
+        _need(t, name, shape, o.dtype, dev)
+    with torch.cuda.device(dev):
+        st = load().kda_norm_gate(_ptr(o), _ptr(gate), _ptr(w), float(eps), GATE_ACT[gate_act],
+                                  _ptr(y), rows, H, dv, _dtype(o), _stream(stream, dev))
     _check(st, "kda_norm_gate")

@@ -3,6 +3,8 @@
 // synchronisation, no host read of device memory.
 #include <math.h>
 
+#include <atomic>
+
 #include "../../include/kda.h"
 #include "kda_internal.h"
 
@@ -23,9 +25,23 @@ kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR
 
 }  // namespace
 
+namespace kda {
+namespace {
+std::atomic<int32_t> g_first_wait_tries{-1};
+}
+uint32_t prefill_first_wait_tries() {
+  const int32_t t = g_first_wait_tries.load(std::memory_order_relaxed);
+  return t < 0 ? kDefaultWaitTries : (uint32_t)t;
+}
+}  // namespace kda
+
 extern "C" {
 
-int kda_version(void) { return 104; }
+int kda_version(void) { return 105; }
+
+void kda_testing_set_first_wait_tries(int32_t tries) {
+  kda::g_first_wait_tries.store(tries < 0 ? -1 : tries, std::memory_order_relaxed);
+}
 
 const char* kda_status_string(kda_status s) {
   switch (s) {
@@ -102,6 +118,7 @@ kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, cons
   p.eps = eps;
   p.in_dtype = in_dtype; p.state_dtype = state_dtype;
   p.gate_act = gate_act;
+  p.first_wait_tries = kda::prefill_first_wait_tries();
   return from_cuda(kda::launch_prefill(p, st));
 }
 

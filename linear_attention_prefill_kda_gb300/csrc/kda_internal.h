@@ -103,7 +103,15 @@ struct PrefillParams {
   float scale, eps;
   kda_dtype in_dtype, state_dtype;
   int gate_act;  // kda_gate_act
+  uint32_t first_wait_tries;  // polls of each prefill kernel's first bounded wait
 };
+
+// Polls of a bounded on-chip wait before it gives up (mbarrier try_wait polls).
+constexpr uint32_t kDefaultWaitTries = 1u << 22;
+
+// Polls of the first bounded wait of each prefill kernel (the testing hook
+// kda_testing_set_first_wait_tries; the default otherwise).
+uint32_t prefill_first_wait_tries();
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device), so
 // later calls (including those made during stream capture) skip the

@@ -13,16 +13,22 @@
 // process exits.
 //
 // Host code cannot use the array's name as a device address (on the host it
-// names a stand-in object), so the address is looked up once per device with
-// cudaGetSymbolAddress, on the first call made with that device current, and
-// cached.  That first call per device should therefore happen before any
-// stream capture begins.
+// names a stand-in object), so the address is looked up with
+// cudaGetSymbolAddress on the first call made with a device current, and
+// cached for that device's current CUDA context.  That first call per device
+// should therefore happen before any stream capture begins.  The cache is keyed
+// by the context's id, which the driver never reuses within a process: after
+// cudaDeviceReset (or in another context on the same device) the library's
+// module is loaded again at another address, and the next call looks the
+// address up again -- that call, too, belongs before any capture.
 //
 // All calls share the one array; each call overwrites what it needs before
 // reading it (nothing in it has to start at zero), and two calls whose
 // kernels overlap on the GPU race on it.
 #include "../../include/kda.h"
 #include "kda_internal.h"
+
+#include <cuda.h>
 
 #include <mutex>
 
@@ -32,22 +38,60 @@ __device__ __align__(256) unsigned char g_static_scratch[KDA_STATIC_SCRATCH_BYTE
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct Cached {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+Cached g_scratch[kMaxDevices] = {};
 
-// Device address of g_static_scratch on the current device (looked up once).
+// Id of the calling thread's current context, through the driver entry points
+// the runtime hands out (the library does not link the driver library).
+cudaError_t current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static cudaError_t resolved = cudaErrorUnknown;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *a = nullptr, *b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) == cudaSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess && qb == cudaDriverEntryPointSuccess && a && b) {
+      get_current = reinterpret_cast<GetCurrent>(a);
+      get_id = reinterpret_cast<GetId>(b);
+      resolved = cudaSuccess;
+    }
+  });
+  if (resolved != cudaSuccess) return resolved;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of g_static_scratch in the current device's current context
+// (looked up once per context).  With no context current yet, the lookup
+// itself makes the device's primary context current, and its id is taken
+// afterwards.
 cudaError_t static_scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned long long id = 0;
+  const bool known = current_context_id(&id) == cudaSuccess;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (!known || !g_scratch[dev].ptr || g_scratch[dev].ctx_id != id) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_static_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = ptr;
+    e = current_context_id(&id);
+    if (e != cudaSuccess) return e;
+    g_scratch[dev].ptr = ptr;
+    g_scratch[dev].ctx_id = id;
   }
-  *out = g_scratch_ptr[dev];
+  *out = g_scratch[dev].ptr;
   return cudaSuccess;
 }
 

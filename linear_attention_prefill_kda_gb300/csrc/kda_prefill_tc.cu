@@ -116,8 +116,8 @@ __device__ __forceinline__ void unpack_half8(uint4 u, float* x) {
 
 // Bounded wait on an mbarrier phase by every thread; returns false (for all
 // threads) when any thread gave up.
-__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity) {
-  const bool ok = tc::mbar_wait(bar, parity);
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, uint32_t tries = kDefaultWaitTries) {
+  const bool ok = tc::mbar_wait(bar, parity, tries);
   return __syncthreads_and(ok) != 0;
 }
 
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   };
   // ---- G = L g : inclusive in-chunk cumulative sum, rows duplicated in both lane halves ----
   bool ok_l = true;
-  if (tid == 0) ok_l = tc::mbar_wait(&bar_l, 0);  // the L operand has landed
+  if (tid == 0) ok_l = tc::mbar_wait(&bar_l, 0, p.first_wait_tries);  // the L operand has landed
   if (tid == 0 && ok_l) {
     constexpr uint32_t idG = tc::idesc_f16(128, 128, true, false, true);
     const uint32_t la = tc::smem_u32(sm + S_LOP), gb = tc::smem_u32(sm + S_GOP);
@@ -384,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     tc::mma_commit(&bar);
   }
   uint32_t phase = 0;
-  bool ok = cta_wait(&bar, phase) && __syncthreads_and(ok_l);
+  ok_l = __syncthreads_and(ok_l) != 0;  // without the L operand no product was issued
+  bool ok = ok_l && cta_wait(&bar, phase);
   phase ^= 1;
   tc::fence_after_sync();
   const int m = min(C / 2 - 1, n - 1);
@@ -1044,7 +1045,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     const uint32_t tP = tmem + 128 * (k & 1);
     tc::fence_proxy_async();
     tc::fence_before_sync();
-    ok = cta_wait(&bar_ld[k & 1], (k >> 1) & 1);
+    ok = cta_wait(&bar_ld[k & 1], (k >> 1) & 1, k == 0 ? p.first_wait_tries : kDefaultWaitTries);
     if (!ok) break;
     last_landed = k;
     tc::fence_after_sync();

@@ -22,3 +22,16 @@ def kda_gpu():
     import linear_attention_prefill_kda_gb300 as kda
     kda.load()  # raises if libkda.so is absent
     return kda
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With KDA_PARITY_REPORT set, write the errors the parity tests measured
+    per named workload (raw max-abs and excess over the half-ulp allowance)."""
+    path = os.environ.get("KDA_PARITY_REPORT")
+    if not path:
+        return
+    from kda_testutil import PARITY_ERRORS
+    if PARITY_ERRORS:
+        import json
+        with open(path, "w") as f:
+            json.dump(PARITY_ERRORS, f, indent=1, sort_keys=True)

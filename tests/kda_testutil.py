@@ -38,6 +38,25 @@ def excess_error(gpu: torch.Tensor, ref: np.ndarray) -> float:
     return float(np.max(np.abs(g - ref) - half_ulp(ref, gpu.dtype)))
 
 
+# Errors measured by the parity tests of the named workloads, written out at
+# the end of the session when KDA_PARITY_REPORT names a file (conftest).
+PARITY_ERRORS: dict = {}
+
+
+def record(workload: str, what: str, gpu: torch.Tensor, ref: np.ndarray) -> None:
+    """Keep the raw max-abs error and its excess over the half-ulp allowance
+    for one compared quantity of a named workload (the worst over calls)."""
+    g = gpu.detach().double().cpu().numpy()
+    if g.size == 0:
+        return
+    raw = float(np.max(np.abs(g - ref)))
+    exc = float(np.max(np.abs(g - ref) - half_ulp(ref, gpu.dtype)))
+    ent = PARITY_ERRORS.setdefault(workload, {}).setdefault(what, {"raw_max_abs": 0.0,
+                                                                   "excess_over_half_ulp": -1e30})
+    ent["raw_max_abs"] = max(ent["raw_max_abs"], raw)
+    ent["excess_over_half_ulp"] = max(ent["excess_over_half_ulp"], exc)
+
+
 def max_abs(gpu: torch.Tensor, ref: np.ndarray) -> float:
     g = gpu.detach().double().cpu().numpy()
     return float(np.max(np.abs(g - ref))) if g.size else 0.0

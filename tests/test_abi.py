@@ -259,3 +259,36 @@ def test_binding_rejects_host_tensors_before_any_call():
     for call in calls:
         with _pt.raises(ValueError, match="CUDA tensor"):
             call()
+
+
+def test_binding_rejects_tensors_on_two_devices():
+    """Every tensor of a call must sit on the device of its first tensor: the
+    ABI launches on one device and would read another device's pointers as its
+    own.  The device check comes before the CUDA check, so a mix of host and
+    'meta' tensors exercises it without a GPU; nothing reaches the library."""
+    q = torch.zeros(8, 2, 16, dtype=torch.bfloat16)
+    b = torch.zeros(8, 2, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 8], dtype=torch.int32)
+    idx = torch.zeros(1, dtype=torch.int32)
+    pool = torch.zeros(2, 2, 16, 16)
+    qm = q.to("meta")
+    calls = [
+        lambda: kda.kda_prefill_chunked(q, qm, q, q, b, cu, idx, pool, q),
+        lambda: kda.kda_prefill_chunked(q, q, q, q, b, cu, idx, pool.to("meta"), q),
+        lambda: kda.kda_prefill_chunked(q, q, q, q, b, cu.to("meta"), idx, pool, q),
+        lambda: kda.kda_prefill_chunked_static_scratch(q, q, q, q, b, cu, idx, pool, qm),
+        lambda: kda.kda_decode_step(q[:1], q[:1], qm[:1], q[:1], b[:1], idx, pool, q[:1]),
+        lambda: kda.kda_decode_multi(q[None, :1], q[None, :1], q[None, :1], q[None, :1],
+                                     b[None, :1], idx.to("meta"), pool, q[None, :1]),
+        lambda: kda.kda_commit_accepted(torch.zeros(1, 1, 2, 16, 16), idx, idx,
+                                        pool.to("meta")),
+        lambda: kda.kda_causal_conv1d_prefill(q[:, 0], q[0, :, :2].T.contiguous(), cu, idx,
+                                              q[None, :1, 0], qm[:, 0]),
+        lambda: kda.kda_causal_conv1d_decode(q[:1, 0], q[0, :, :2].T.contiguous(), idx,
+                                             q[None, :1, 0].to("meta"), q[:1, 0]),
+        lambda: kda.kda_norm_gate(q, qm, q[0, 0], q),
+        lambda: kda.kda_norm_gate_ex(q, q, qm),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError, match="one CUDA device"):
+            call()

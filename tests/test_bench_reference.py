@@ -12,9 +12,10 @@ CMD = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "-
        "--warmup", "3"]
 
 
-def _run(extra_env):
+def _run(extra_env, extra_args=()):
     env = dict(os.environ, **extra_env)
-    return subprocess.run(CMD, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return subprocess.run(CMD + list(extra_args), cwd=ROOT, env=env, capture_output=True,
+                          text=True, timeout=600)
 
 
 def test_reference_arm_prints_one_json_line():
@@ -39,9 +40,28 @@ def test_reference_arm_prints_one_json_line():
 
 
 def test_reference_arm_other_ranks_exit_quietly():
-    r = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    r = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, ["--gpus", "2"])
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_gpus_flag_launches_that_many_replicas():
+    """``--gpus 2`` without a launcher starts two ranks itself; rank 0 alone
+    prints one line, which reports both."""
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run(CMD + ["--gpus", "2"], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+
+
+def test_gpus_flag_must_match_the_launch():
+    r = _run({"RANK": "0", "WORLD_SIZE": "2", "LOCAL_RANK": "0"})  # --gpus defaults to 1
+    assert r.returncode != 0 and "WORLD_SIZE" in r.stderr
 
 
 def _bench_module():
@@ -91,6 +111,13 @@ def test_roofline_numerators_match_hand_counts():
     expect = 2 * T * C * 2 + C * 5 * 2 + 2 * 8 * 3 * C * 2
     assert expect == 202_629_120
     assert b.conv_algorithmic(w, C, 4) == expect
+    # one 4096-token call of the long prompt: bf16 inputs, no gate, bf16 state
+    # read and written once, 16 bf16 checkpoints
+    lw = W.LONGPROMPT.replace(seqlens=(4096,))
+    bstate = dd * dd * 2
+    expect = 4 * T * H * dd * 2 + T * H * 2 + T * H * dd * 2 + 2 * H * bstate + 16 * H * bstate
+    assert expect == 186_908_672
+    assert b.prefill_algorithmic(lw, {"cu_seqlens": W.cu_from_lengths([4096])})[0] == expect
 
 
 def test_prefill_flop_count_matches_hand_count():

@@ -7,7 +7,8 @@ import torch
 
 import oracle
 import workloads as W
-from kda_testutil import (excess_error, max_abs, oracle_prefill, run_prefill, to_dev, tol_for)
+from kda_testutil import (excess_error, max_abs, oracle_prefill, record, run_prefill, to_dev,
+                          tol_for)
 
 W_ = W  # the workloads module, for tests whose parameter W is a convolution width
 
@@ -15,7 +16,7 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
 
-def _check_prefill(kda, w, d, *, heads=None, ckpt=True):
+def _check_prefill(kda, w, d, *, heads=None, ckpt=True, label=None):
     pool0 = d["pool"].clone()
     out, pool, ck, offs, status = run_prefill(kda, d, w, DEV, ckpt=ckpt)
     assert int(status.item()) == 0, kda.DEV_STATUS[int(status.item())]
@@ -25,12 +26,16 @@ def _check_prefill(kda, w, d, *, heads=None, ckpt=True):
     idx = d["state_indices"].tolist()
     lens = (d["cu_seqlens"][1:] - d["cu_seqlens"][:-1]).tolist()
     # outputs
+    if label:
+        record(label, "out", out[:, hsel], o_ref)
     assert excess_error(out[:, hsel], o_ref) <= tol
     # touched slots, untouched slots bit-exact
     touched = [s for s, L in zip(idx, lens) if s >= 0 and L > 0]
     pool_cpu = pool.cpu()
     for s in range(w.num_slots):
         if s in touched:
+            if label:
+                record(label, "final_state", pool_cpu[s][hsel], p_ref[s])
             assert excess_error(pool_cpu[s][hsel], p_ref[s]) <= tol, s
         else:
             assert torch.equal(pool_cpu[s], pool0[s]), f"slot {s} modified"
@@ -43,20 +48,22 @@ def _check_prefill(kda, w, d, *, heads=None, ckpt=True):
             for i, s in enumerate(idx):
                 if s >= 0:
                     real.extend(range(int(offs_ref[i]), int(offs_ref[i + 1])))
+            if label:
+                record(label, "checkpoints", ck[real][:, hsel], ck_ref[real])
             assert excess_error(ck[real][:, hsel], ck_ref[real]) <= tol
     return out, pool
 
 
 def test_prefill_tiny(kda_gpu):
-    _check_prefill(kda_gpu, W.TINY, W.make_prefill(W.TINY))
+    _check_prefill(kda_gpu, W.TINY, W.make_prefill(W.TINY), label=W.TINY.name)
 
 
 def test_prefill_varlen(kda_gpu):
-    _check_prefill(kda_gpu, W.VARLEN, W.make_prefill(W.VARLEN))
+    _check_prefill(kda_gpu, W.VARLEN, W.make_prefill(W.VARLEN), label=W.VARLEN.name)
 
 
 def test_prefill_sched_full(kda_gpu):
-    _check_prefill(kda_gpu, W.SCHED, W.make_prefill(W.SCHED))
+    _check_prefill(kda_gpu, W.SCHED, W.make_prefill(W.SCHED), label=W.SCHED.name)
 
 
 @pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
@@ -160,11 +167,10 @@ def test_prefill_bad_index_latches_status(kda_gpu):
 
 def test_prefill_longprompt_bf16_state(kda_gpu):
     """One 32768-token sequence as 8 calls of 4096 carrying bf16 state through
-    the pool, against the one-shot fp64 oracle (sampled heads) and against a
+    the pool, against the one-shot fp64 oracle (every head) and against a
     single 32768-token call; checkpoint positions bit-exact."""
     w = W.LONGPROMPT
     d = W.make_prefill(w)
-    heads = [0, 11, 22, 31]
     pool_init = d["pool"].clone()
     slot = int(d["state_indices"][0])
     T, seg = w.T, 4096
@@ -200,23 +206,29 @@ def test_prefill_longprompt_bf16_state(kda_gpu):
     # the two GPU runs agree
     assert max_abs(out8, out1.double().cpu().numpy()) <= tol
     assert max_abs(ck8, ck1.double().cpu().numpy()) <= tol
-    # against the fp64 oracle (sampled heads)
-    o_ref, p_ref, ck_ref, _ = oracle_prefill(oracle, d, w, heads=heads)
-    assert excess_error(out8[:, heads], o_ref) <= tol
-    assert excess_error(out1[:, heads], o_ref) <= tol
-    assert excess_error(ck8[:, heads], ck_ref) <= tol
-    assert excess_error(dev_pool[slot][heads], p_ref[slot]) <= tol
-    assert excess_error(pool1[slot][heads], p_ref[slot]) <= tol
+    # against the fp64 oracle, all 32 heads
+    o_ref, p_ref, ck_ref, _ = oracle_prefill(oracle, d, w)
+    for name, x, ref in (("out (8 calls)", out8, o_ref), ("out (one call)", out1, o_ref),
+                         ("checkpoints (8 calls)", ck8, ck_ref), ("checkpoints (one call)", ck1, ck_ref),
+                         ("final_state (8 calls)", dev_pool[slot], p_ref[slot]),
+                         ("final_state (one call)", pool1[slot], p_ref[slot])):
+        record(w.name, name, x, ref)
+    assert excess_error(out8, o_ref) <= tol
+    assert excess_error(out1, o_ref) <= tol
+    assert excess_error(ck8, ck_ref) <= tol
+    assert excess_error(ck1, ck_ref) <= tol
+    assert excess_error(dev_pool[slot], p_ref[slot]) <= tol
+    assert excess_error(pool1[slot], p_ref[slot]) <= tol
 
 
 def test_decode_full_64_steps(kda_gpu):
     """256 sequences x 64 in-place steps on a 1024-slot fp32 pool; the oracle
-    follows a sample of 16 sequences (all heads) at every step."""
+    follows every sequence and head at every step."""
     w = W.DECODE
     pd = W.make_decode_pool(w)
     pool0 = pd["pool"]
     idx = pd["state_indices"]
-    sample = list(range(0, w.N, w.N // 16))
+    sample = list(range(w.N))
     ref_pool = pool0[idx[sample].long()].double().numpy().copy()
     ref_idx = np.arange(len(sample), dtype=np.int32)
     dev_pool = pool0.to(DEV)
@@ -235,10 +247,12 @@ def test_decode_full_64_steps(kda_gpu):
                                         ref_idx, ref_pool, gate=sd["gate"][sample],
                                         norm_w=pd["norm_w"], eps=pd["eps"])
         worst = max(worst, excess_error(out[sample], y_ref))
+        record(w.name, "out (every step)", out[sample], y_ref)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert worst <= tol, worst
     final = dev_pool[didx[sample].long()]
+    record(w.name, "final_state", final, ref_pool)
     assert excess_error(final, ref_pool) <= tol
     # slots outside the batch are untouched, byte for byte
     mask = torch.ones(w.num_slots, dtype=torch.bool)
@@ -353,7 +367,8 @@ def test_decode_multi_and_commit(kda_gpu, d, K, in_dtype, state_dtype):
 
 def test_decode_multi_full_width(kda_gpu):
     """256 sequences x 4 draft tokens at 32 heads, d = 128 (the decode batch);
-    the oracle follows 16 sampled sequences."""
+    every sequence against the oracle, in groups of 32 so that the fp64
+    per-token states stay at half a gigabyte per group."""
     w, K = W.DECODE, 4
     pd = W.make_decode_pool(w)
     dd = W.make_decode_draft(w, K)
@@ -370,19 +385,20 @@ def test_decode_multi_full_width(kda_gpu):
                                 dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    sample = list(range(0, w.N, w.N // 16))
-    sidx = idx[sample]
-    sub_pool = pd["pool"][sidx.long()]
-    ref_idx = np.arange(len(sample), dtype=np.int32)
-    y_ref, ts_ref, _ = oracle.decode_multi(
-        *(dd[n][sample] for n in ("q", "k", "v", "g", "beta")), ref_idx, sub_pool,
-        gate=dd["gate"][sample], norm_w=pd["norm_w"], eps=pd["eps"])
     tol = tol_for(w.state_dtype)
-    assert excess_error(out[sample], y_ref) <= tol
-    assert excess_error(ts[sample], ts_ref) <= tol
-    ref_commit = oracle.commit_accepted(ts_ref, dd["num_accepted"][sample].numpy(), ref_idx,
-                                        sub_pool)
-    assert excess_error(pool[sidx.long().to(DEV)], ref_commit) <= tol
+    for g0 in range(0, w.N, 32):
+        sample = list(range(g0, g0 + 32))
+        sidx = idx[sample]
+        sub_pool = pd["pool"][sidx.long()]
+        ref_idx = np.arange(len(sample), dtype=np.int32)
+        y_ref, ts_ref, _ = oracle.decode_multi(
+            *(dd[n][sample] for n in ("q", "k", "v", "g", "beta")), ref_idx, sub_pool,
+            gate=dd["gate"][sample], norm_w=pd["norm_w"], eps=pd["eps"])
+        assert excess_error(out[sample], y_ref) <= tol
+        assert excess_error(ts[sample], ts_ref) <= tol
+        ref_commit = oracle.commit_accepted(ts_ref, dd["num_accepted"][sample].numpy(), ref_idx,
+                                            sub_pool)
+        assert excess_error(pool[sidx.long().to(DEV)], ref_commit) <= tol
 
 
 @pytest.mark.parametrize("W", [2, 3, 4])
@@ -589,7 +605,7 @@ def test_binding_rejects_mismatched_arguments(kda_gpu):
         call(k=t["k"][:-1])
     with pytest.raises(ValueError, match="state_indices must be torch.int32"):
         call(state_indices=t["state_indices"].long())
-    with pytest.raises(ValueError, match="CUDA tensor"):
+    with pytest.raises(ValueError, match="one CUDA device"):
         call(beta=d["beta"])
     with pytest.raises(ValueError, match="out must have shape"):
         call(out=out[:, :, :-1].contiguous())

@@ -1,0 +1,46 @@
+"""A bounded on-chip wait that runs out: with the testing hook set to zero
+polls, the first wait of each tensor-core prefill kernel gives up at once.  The
+call must still return, the kernels must report KDA_DEV_TIMEOUT (3) instead of
+hanging or trapping, and nothing may be written to the pool; after the hook is
+reset, the next call on the same stream must match the oracle.
+
+Nothing here makes the GPU fault: a wait gives up on its own count, and the
+kernels' clean-up lets every bulk copy and tensor-core product in flight finish
+before their shared and tensor memory is released."""
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from kda_testutil import excess_error, max_abs, oracle_prefill, run_prefill, tol_for
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def test_first_wait_timeout_reports_and_recovers(kda_gpu):
+    kda = kda_gpu
+    w = W.SCHED.replace(seqlens=(150, 64, 1), H=4, num_slots=8, slot_range=None,
+                        checkpoint_every=64, seed=808)
+    d = W.make_prefill(w)
+    pool0 = d["pool"].clone()
+    try:
+        kda.kda_testing_set_first_wait_tries(0)
+        out, pool, ck, offs, status = run_prefill(kda, d, w, DEV)
+        assert int(status.item()) == 3, kda.DEV_STATUS.get(int(status.item()))
+        # every state chain gave up before its first product: no slot written
+        assert torch.equal(pool.cpu(), pool0)
+    finally:
+        kda.kda_testing_set_first_wait_tries(-1)
+    # the same call again, limits back to normal, on a fresh status word
+    d2 = dict(d, pool=pool0.clone())
+    out, pool, ck, offs, status = run_prefill(kda, d2, w, DEV)
+    assert int(status.item()) == 0
+    o_ref, p_ref, ck_ref, offs_ref = oracle_prefill(oracle, d2, w)
+    tol = tol_for(w.state_dtype)
+    assert excess_error(out, o_ref) <= tol
+    touched = d["state_indices"].long().tolist()
+    assert max_abs(pool[touched], p_ref[touched]) <= tol
+    assert offs.cpu().tolist() == offs_ref.tolist()
+    n = int(offs_ref[-1])
+    assert max_abs(ck[:n], ck_ref[:n]) <= tol

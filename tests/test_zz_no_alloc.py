@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import workloads as W
-from kda_testutil import max_abs, to_dev, tol_for
+from kda_testutil import excess_error, max_abs, to_dev, tol_for
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -35,14 +35,16 @@ def _run(kda, d, w, pool, *, static, ws=None):
 
 def test_static_scratch_matches_workspace_entry_point(kda_gpu):
     kda = kda_gpu
-    # tensor-core shape; its scratch (20 chunk slots x 8 heads x 74 KB) fits the array
+    import oracle
+    # tensor-core shape; its scratch fits the array
     w = W.SCHED.replace(seqlens=(300, 100, 700), H=8, num_slots=16, slot_range=None,
                         checkpoint_every=128, seed=501)
     need = kda.kda_prefill_workspace_bytes(w.N, w.T, w.H, w.dk, w.dv, w.chunk)
     assert 0 < need <= kda.STATIC_SCRATCH_BYTES
     ws = torch.empty(need, dtype=torch.uint8, device=DEV)
-    pool0 = W.make_prefill(w)["pool"].to(DEV)
-    pool_ref, pool_static = pool0.clone(), pool0.clone()
+    pool0 = W.make_prefill(w)["pool"]
+    pool_ref, pool_static = pool0.to(DEV), pool0.to(DEV)
+    pool_oracle = pool0.double().numpy()
     tol = tol_for(w.state_dtype)
     for call in range(2):  # consecutive calls carry the state and reuse the scratch
         d = W.make_prefill(w, seed=w.seed + call)
@@ -50,10 +52,21 @@ def test_static_scratch_matches_workspace_entry_point(kda_gpu):
         o_st, ck_st, off_st = _run(kda, d, w, pool_static, static=True)
         written = int(off_ref[-1].item())  # entries past the last offset are never written
         assert written == 7
-        assert max_abs(o_st, o_ref.double().cpu().numpy()) <= tol
-        assert max_abs(ck_st[:written], ck_ref[:written].double().cpu().numpy()) <= tol
-        assert max_abs(pool_static, pool_ref.double().cpu().numpy()) <= tol
+        # the same kernels on the same inputs: identical bits, whichever scratch they use
+        assert torch.equal(o_st, o_ref)
+        assert torch.equal(ck_st[:written], ck_ref[:written])
+        assert torch.equal(pool_static, pool_ref)
         assert torch.equal(off_st, off_ref)
+        # and both within the bound of the fp64 oracle carried through the same calls
+        d["pool"] = pool_oracle
+        y, pool_oracle, ck, offs = oracle.prefill(
+            d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["state_indices"],
+            d["pool"], checkpoint_every=w.checkpoint_every, gate=d["gate"], norm_w=d["norm_w"],
+            eps=d["eps"], scale=d["scale"])
+        assert excess_error(o_st, y) <= tol
+        assert max_abs(ck_st[:written], ck) <= tol
+        assert max_abs(pool_static, pool_oracle) <= tol
+        assert off_st.cpu().tolist() == list(offs)
 
 
 def test_static_scratch_rejects_oversize(kda_gpu):
