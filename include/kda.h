@@ -314,16 +314,18 @@ KDA_API kda_status kda_prefill_chunked_static_scratch(
     int H, int dk, int dv, int chunk, float scale, int32_t* dev_status, void* stream);
 
 /*
- * Testing only: the number of polls the first bounded on-chip wait of each
- * prefill kernel makes before it gives up (the other waits keep their limit,
- * so the clean-up after a timed-out wait still lets every copy and product in
- * flight finish).  tries < 0 restores the default.  The setting is process
- * wide and applies to kda_prefill_chunked and
+ * Testing only: the number of polls the first bounded on-chip wait of a
+ * tensor-core prefill kernel makes before it gives up (the other waits keep
+ * their limit, so the clean-up after a timed-out wait still lets every copy
+ * and product in flight finish).  `kernels` selects the kernels the setting
+ * applies to: bit 0 the intra-chunk kernel (each CTA's first wait), bit 1 the
+ * state kernel (each chain's first wait); tries < 0 restores the default for
+ * both.  The setting is process wide and applies to kda_prefill_chunked and
  * kda_prefill_chunked_static_scratch launches made after the call; it exists
  * so that a test can make a wait run out (KDA_DEV_TIMEOUT) without touching
  * any other part of the GPU.  Not for production use.
  */
-KDA_API void kda_testing_set_first_wait_tries(int32_t tries);
+KDA_API void kda_testing_set_first_wait_tries(int32_t tries, int32_t kernels);
 
 /* A static, human-readable name for a kda_status value. */
 KDA_API const char* kda_status_string(kda_status status);

@@ -68,7 +68,7 @@ _SIGNATURES = {
         _P, _P, _I32, _I64, _P, _P, _P, _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_int, _F32, _P, _P]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
-    "kda_testing_set_first_wait_tries": (None, [_I32]),
+    "kda_testing_set_first_wait_tries": (None, [_I32, _I32]),
     "kda_version": (ctypes.c_int, []),
 }
 
@@ -194,11 +194,11 @@ def kda_version() -> int:
     return load().kda_version()
 
 
-def kda_testing_set_first_wait_tries(tries: int) -> None:
+def kda_testing_set_first_wait_tries(tries: int, kernels: int = 3) -> None:
     """Testing only (see ``include/kda.h``): polls of the first bounded wait
-    of each prefill kernel launched from now on; a negative value restores the
-    default."""
-    load().kda_testing_set_first_wait_tries(int(tries))
+    of the prefill kernels selected by ``kernels`` (bit 0 intra-chunk, bit 1
+    state) launched from now on; a negative value restores the default."""
+    load().kda_testing_set_first_wait_tries(int(tries), int(kernels))
 
 
 def kda_prefill_workspace_bytes(N: int, T: int, H: int, dk: int, dv: int, chunk: int) -> int:

@@ -27,10 +27,10 @@ kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR
 
 namespace kda {
 namespace {
-std::atomic<int32_t> g_first_wait_tries{-1};
+std::atomic<int32_t> g_first_wait_tries[2] = {{-1}, {-1}};
 }
-uint32_t prefill_first_wait_tries() {
-  const int32_t t = g_first_wait_tries.load(std::memory_order_relaxed);
+uint32_t prefill_first_wait_tries(int which) {
+  const int32_t t = g_first_wait_tries[which & 1].load(std::memory_order_relaxed);
   return t < 0 ? kDefaultWaitTries : (uint32_t)t;
 }
 }  // namespace kda
@@ -39,8 +39,10 @@ extern "C" {
 
 int kda_version(void) { return 105; }
 
-void kda_testing_set_first_wait_tries(int32_t tries) {
-  kda::g_first_wait_tries.store(tries < 0 ? -1 : tries, std::memory_order_relaxed);
+void kda_testing_set_first_wait_tries(int32_t tries, int32_t kernels) {
+  for (int which = 0; which < 2; ++which)
+    if (tries < 0 || (kernels >> which) & 1)
+      kda::g_first_wait_tries[which].store(tries < 0 ? -1 : tries, std::memory_order_relaxed);
 }
 
 const char* kda_status_string(kda_status s) {
@@ -118,7 +120,8 @@ kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, cons
   p.eps = eps;
   p.in_dtype = in_dtype; p.state_dtype = state_dtype;
   p.gate_act = gate_act;
-  p.first_wait_tries = kda::prefill_first_wait_tries();
+  p.intra_first_wait_tries = kda::prefill_first_wait_tries(0);
+  p.state_first_wait_tries = kda::prefill_first_wait_tries(1);
   return from_cuda(kda::launch_prefill(p, st));
 }
 

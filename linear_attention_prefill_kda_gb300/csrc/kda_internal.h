@@ -103,15 +103,17 @@ struct PrefillParams {
   float scale, eps;
   kda_dtype in_dtype, state_dtype;
   int gate_act;  // kda_gate_act
-  uint32_t first_wait_tries;  // polls of each prefill kernel's first bounded wait
+  // polls of the first bounded wait of the intra-chunk and of the state kernel
+  uint32_t intra_first_wait_tries, state_first_wait_tries;
 };
 
 // Polls of a bounded on-chip wait before it gives up (mbarrier try_wait polls).
 constexpr uint32_t kDefaultWaitTries = 1u << 22;
 
-// Polls of the first bounded wait of each prefill kernel (the testing hook
-// kda_testing_set_first_wait_tries; the default otherwise).
-uint32_t prefill_first_wait_tries();
+// Polls of the first bounded wait of the intra-chunk kernel (which = 0) or
+// of the state kernel (which = 1): the testing hook
+// kda_testing_set_first_wait_tries, the default otherwise.
+uint32_t prefill_first_wait_tries(int which);
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device), so
 // later calls (including those made during stream capture) skip the

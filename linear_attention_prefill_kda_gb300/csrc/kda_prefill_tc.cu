@@ -49,10 +49,17 @@ constexpr uint32_t WS_KLT = 32768;    // fp16 MN-major [M=c 128 x K=j 64] (K str
 constexpr uint32_t WS_U0 = 49152;     // fp16 [v/8][64 rows][8]: byte (v/8)*1024 + r*16 + (v%8)*2
 constexpr uint32_t WS_AQK = 65536;    // fp16 K-major [64 x 64] (SBO 1024)
 constexpr uint32_t WS_DECAY = 73728;  // fp32 [128]
-constexpr uint32_t WS_GW = 74240;     // fp16 [v/8][64 rows][8]: w * act(gate) (when gated)
-constexpr uint32_t WS_BYTES = 90624;
+constexpr uint32_t WS_TAG = 74240;    // int32: BLOCK_OK once the block is complete, BLOCK_FAILED
+                                      // after a timed-out wait (16 bytes reserved)
+constexpr uint32_t WS_GW = 74256;     // fp16 [v/8][64 rows][8]: w * act(gate) (when gated)
+constexpr uint32_t WS_BYTES = 90640;
 constexpr uint32_t WS_COPY0 = 65536;  // PA | KLT | U0
-constexpr uint32_t WS_COPY1 = 8704;   // AQK | DECAY
+constexpr uint32_t WS_COPY1 = 8720;   // AQK | DECAY | TAG
+// Block tags.  Every block the state kernel reads is written by one intra
+// CTA of the same call, which stamps it last: a block the intra CTA could not
+// finish is stamped failed, so the chain that reads it stores nothing
+// instead of carrying stale data into the pool.
+constexpr int BLOCK_OK = 1, BLOCK_FAILED = 2;
 
 __host__ __device__ inline int64_t num_slots_bound(int64_t T, int N) { return T / C + N; }
 
@@ -374,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   };
   // ---- G = L g : inclusive in-chunk cumulative sum, rows duplicated in both lane halves ----
   bool ok_l = true;
-  if (tid == 0) ok_l = tc::mbar_wait(&bar_l, 0, p.first_wait_tries);  // the L operand has landed
+  if (tid == 0) ok_l = tc::mbar_wait(&bar_l, 0, p.intra_first_wait_tries);  // the L operand has landed
   if (tid == 0 && ok_l) {
     constexpr uint32_t idG = tc::idesc_f16(128, 128, true, false, true);
     const uint32_t la = tc::smem_u32(sm + S_LOP), gb = tc::smem_u32(sm + S_GOP);
@@ -405,7 +412,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   }
   __syncthreads();
   if (!ok) {
-    if (tid == 0) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
+    if (tid == 0) {
+      latch_status(p.dev_status, KDA_DEV_TIMEOUT);
+      *reinterpret_cast<int*>(ws + WS_TAG) = BLOCK_FAILED;
+    }
     drain(!ok_l);
     tc::fence_before_sync();
     __syncthreads();
@@ -570,7 +580,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   tc::fence_before_sync();
   __syncthreads();  // region reads done; phase-3 buffers may be written
   if (!ok) {
-    if (tid == 0) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
+    if (tid == 0) {
+      latch_status(p.dev_status, KDA_DEV_TIMEOUT);
+      *reinterpret_cast<int*>(ws + WS_TAG) = BLOCK_FAILED;
+    }
     drain(false);
     tc::fence_before_sync();
     __syncthreads();
@@ -803,6 +816,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     if (tid == 0) latch_status(p.dev_status, KDA_DEV_TIMEOUT);
     drain(false);
   }
+  if (tid == 0) *reinterpret_cast<int*>(ws + WS_TAG) = ok ? BLOCK_OK : BLOCK_FAILED;
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, 256);
@@ -813,11 +827,11 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
 // =====================================================================
 namespace state {
 // A stage holds one chunk's operands: PA|KLT|U0 (65536, the main copy) and
-// AQK|DECAY (8704, the tail copy).  The output product reads the 8 KB before
+// AQK|DECAY|TAG (8720, the tail copy).  The output product reads the 8 KB before
 // AQK (the end of U0) as rows 0-63 of its A operand; those products land in
 // TMEM lanes 0-63, whose W S values have been consumed by then.
-constexpr uint32_t STAGE = 74240;
-constexpr uint32_t ST_PA = 0, ST_KLT = 32768, ST_U0 = 49152, ST_AQK = 65536, ST_DECAY = 73728;
+constexpr uint32_t STAGE = 74256;
+constexpr uint32_t ST_PA = 0, ST_KLT = 32768, ST_U0 = 49152, ST_AQK = 65536, ST_DECAY = 73728, ST_TAG = 74240;
 constexpr uint32_t S_SOP = 2 * STAGE;    // fp16 MN-major [K=c 128 x N=v 128] (K stride 2048)
 constexpr uint32_t S_UOP = S_SOP + 32768;  // fp16 MN-major [K=j 64 x N=v 128]
 constexpr uint32_t S_NW = S_UOP + 16384;   // fp32 [128]
@@ -1045,8 +1059,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     const uint32_t tP = tmem + 128 * (k & 1);
     tc::fence_proxy_async();
     tc::fence_before_sync();
-    ok = cta_wait(&bar_ld[k & 1], (k >> 1) & 1, k == 0 ? p.first_wait_tries : kDefaultWaitTries);
+    ok = cta_wait(&bar_ld[k & 1], (k >> 1) & 1, k == 0 ? p.state_first_wait_tries : kDefaultWaitTries);
     if (!ok) break;
+    // a block its intra CTA could not finish ends the chain (every thread
+    // reads the same stamp after the barrier)
+    ok = *reinterpret_cast<const int*>(st + ST_TAG) == BLOCK_OK;
+    if (!ok) {
+      last_landed = k;
+      break;
+    }
     last_landed = k;
     tc::fence_after_sync();
     if (k + 1 < nchunks) last_issued = k + 1;

@@ -1,12 +1,19 @@
-"""A bounded on-chip wait that runs out: with the testing hook set to zero
-polls, the first wait of each tensor-core prefill kernel gives up at once.  The
-call must still return, the kernels must report KDA_DEV_TIMEOUT (3) instead of
-hanging or trapping, and nothing may be written to the pool; after the hook is
-reset, the next call on the same stream must match the oracle.
+"""A bounded on-chip wait that runs out.  With the testing hook set to zero
+polls, the first wait of the selected tensor-core prefill kernel gives up at
+once.  The call must still return and report KDA_DEV_TIMEOUT (3) instead of
+hanging or trapping, and nothing may be written to the pool:
+  * intra-chunk kernel: every CTA gives up and stamps its workspace block
+    failed; the state kernel, whose own waits succeed, must see the stamps
+    and store nothing (no stale workspace data carried into the pool);
+  * state kernel: every chain gives up on its first operand copy and drains
+    the copies and products still in flight before it exits;
+  * both.
+After the hook is reset, the next call on the same stream must match the
+oracle.
 
 Nothing here makes the GPU fault: a wait gives up on its own count, and the
-kernels' clean-up lets every bulk copy and tensor-core product in flight finish
-before their shared and tensor memory is released."""
+kernels' clean-up lets every bulk copy and tensor-core product in flight
+finish before their shared and tensor memory are released."""
 import pytest
 import torch
 
@@ -18,17 +25,18 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
 
-def test_first_wait_timeout_reports_and_recovers(kda_gpu):
+@pytest.mark.parametrize("kernels", [1, 2, 3], ids=["intra", "state", "both"])
+def test_first_wait_timeout_reports_and_recovers(kda_gpu, kernels):
     kda = kda_gpu
     w = W.SCHED.replace(seqlens=(150, 64, 1), H=4, num_slots=8, slot_range=None,
                         checkpoint_every=64, seed=808)
     d = W.make_prefill(w)
     pool0 = d["pool"].clone()
     try:
-        kda.kda_testing_set_first_wait_tries(0)
+        kda.kda_testing_set_first_wait_tries(0, kernels)
         out, pool, ck, offs, status = run_prefill(kda, d, w, DEV)
         assert int(status.item()) == 3, kda.DEV_STATUS.get(int(status.item()))
-        # every state chain gave up before its first product: no slot written
+        # every state chain stopped before its first product: no slot written
         assert torch.equal(pool.cpu(), pool0)
     finally:
         kda.kda_testing_set_first_wait_tries(-1)
