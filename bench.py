@@ -12,6 +12,8 @@ Workloads (seeded synthetic inputs, no dataset):
            step's q, k, v projections (12288 channels), with its cache pool.
   long     one 32768-token prompt as 8 calls of 4096 tokens carrying a bf16
            state through the pool, bf16 checkpoints every 256 tokens, no gate.
+  varlen   4 sequences {37, 128, 200, 512}, H=8, d=64, bf16 inputs, fp32
+           pool of 16, checkpoints every 64 (a latency-bound correctness case).
 A step is one prefill call, one decode step, one verify + commit, one
 convolution call and the 8 long-prompt calls; each is timed in its own loop
 with CUDA events on the launching stream, the L2 flushed (a 256 MiB write)
@@ -335,6 +337,26 @@ def run_gpu(args):
                                 checkpoint_every=lw.checkpoint_every, workspace=lws,
                                 dev_status=status, stream=stream)
 
+    # ---------------- varlen: 4 sequences {37, 128, 200, 512}, H=8, d=64, bf16,
+    # fp32 pool of 16, checkpoints every 64 (the d=64 tensor-core kernels)
+    with_varlen = args.workload in ("both", "varlen")
+    vw = W.VARLEN
+    if with_varlen:
+        vd = W.make_prefill(vw)
+        vt = {k: (x.to(dev) if isinstance(x, torch.Tensor) else x) for k, x in vd.items()}
+        vout = torch.empty(vw.T, vw.H, vw.dv, device=dev, dtype=vw.in_dtype)
+        vck = torch.empty(vw.T // vw.checkpoint_every, vw.H, vw.dk, vw.dv, device=dev,
+                          dtype=vw.state_dtype)
+        vwsb = kda.kda_prefill_workspace_bytes(vw.N, vw.T, vw.H, vw.dk, vw.dv, vw.chunk)
+        vws = torch.empty(vwsb, dtype=torch.uint8, device=dev) if vwsb else None
+
+    def varlen_call():
+        kda.kda_prefill_chunked(vt["q"], vt["k"], vt["v"], vt["g"], vt["beta"], vt["cu_seqlens"],
+                                vt["state_indices"], vt["pool"], vout, chunk=vw.chunk,
+                                checkpoints=vck, checkpoint_every=vw.checkpoint_every,
+                                scale=vd["scale"], workspace=vws, dev_status=status,
+                                stream=stream)
+
     def conv_call():
         if not with_conv:
             return
@@ -381,6 +403,8 @@ def run_gpu(args):
             lpool.copy_(lpool0)
             for c in range(lw.T // LSEG):
                 long_call(c)
+        if with_varlen:
+            varlen_call()
     barrier()
 
     def gpu_lead():
@@ -453,6 +477,20 @@ def run_gpu(args):
         barrier()
         long_ms = (sum(a.elapsed_time(b) for a, b in zip(lstarts, lends)) / (args.steps * ncall)
                    if with_long else float("nan"))
+        # varlen (a latency-bound correctness workload): each call timed with
+        # the L2 flushed before it
+        vstarts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        vends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier()
+        for i in range(args.steps if with_varlen else 0):
+            flush.fill_(float(i))
+            gpu_lead()
+            vstarts[i].record(stream)
+            varlen_call()
+            vends[i].record(stream)
+        barrier()
+        var_ms = (sum(a.elapsed_time(b) for a, b in zip(vstarts, vends)) / args.steps
+                  if with_varlen else float("nan"))
     clocks = clk.summary()
     st = int(status.item())
     if st != 0:
@@ -461,8 +499,8 @@ def run_gpu(args):
     pre_ms_mean = sum(pre_ms) / len(pre_ms)
     dec_ms = dec_ms_total / args.steps
     spec_ms = spec_ms_total / args.steps if with_spec else float("nan")
-    pre_ms_mean, dec_ms, spec_ms, conv_ms, long_ms = max_over_ranks(
-        [pre_ms_mean, dec_ms, spec_ms, conv_ms, long_ms], dev)
+    pre_ms_mean, dec_ms, spec_ms, conv_ms, long_ms, var_ms = max_over_ranks(
+        [pre_ms_mean, dec_ms, spec_ms, conv_ms, long_ms, var_ms], dev)
 
     # ---------------- e2e through the public API with host buffers
     # Every step copies its inputs in from pinned host memory and its output
@@ -602,13 +640,17 @@ def run_gpu(args):
                                     "algorithmic_bytes": long_bytes,
                                     "algorithmic_flops": long_flops,
                                     "achieved_tflops": round(rate(long_flops, long_ms) / 1e12, 2)}},
+        "varlen": {"workload": vw.name, "value": round(replica_rate(vw.T, ws, var_ms), 1),
+                   "unit": "tokens/s", "ms_per_call": round(var_ms, 4),
+                   "path": kda.kda_prefill_path(vw.dk, vw.dv, vw.chunk, vw.in_dtype)},
         "e2e": {"value": round(replica_rate(T, ws, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipelined": "step i+1's inputs copied in while step i computes and its output "
                              "is copied out (two copy streams, double-buffered staging)"},
         "gpu_launches": args.steps * (prefill_launches(kda, w) * with_prefill + with_decode
                                       + 2 * with_spec + with_conv
-                                      + (lw.T // LSEG) * prefill_launches(kda, lw) * with_long),
+                                      + (lw.T // LSEG) * prefill_launches(kda, lw) * with_long
+                                      + prefill_launches(kda, vw) * with_varlen),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -733,7 +775,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["both", "prefill", "decode", "spec", "conv",
-                                           "longprompt"],
+                                           "longprompt", "varlen"],
                     default="both",
                     help="time every part (default) or one of them (for profiling runs)")
     raw = list(sys.argv[1:] if argv is None else argv)

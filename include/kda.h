@@ -135,8 +135,9 @@ KDA_API size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int 
  * State is carried in fp32 inside a call and rounded (to nearest even) to
  * state_dtype only when stored: at checkpoints and at the final write-back.
  *
- * Numerics.  The tensor-core path (bf16 inputs, dk = dv = 128, chunk 64)
- * forms the in-chunk products A_kk, A_qk from split bf16 operands (fp32
+ * Numerics.  The tensor-core path (bf16 inputs, dk = dv in {64, 128}, chunk
+ * 64; kda_prefill_path says which path a shape takes) forms the in-chunk
+ * products A_kk, A_qk from split bf16 operands (fp32
  * accuracy) and the state-coupled products from fp16 operands, all with fp32
  * accumulation.  That relies on the method's regime: q and k rows of unit L2
  * norm and beta in [0, 1], where I - beta k k^T is a contraction and the
@@ -326,6 +327,18 @@ KDA_API kda_status kda_prefill_chunked_static_scratch(
  * any other part of the GPU.  Not for production use.
  */
 KDA_API void kda_testing_set_first_wait_tries(int32_t tries, int32_t kernels);
+
+/*
+ * Which kernels kda_prefill_chunked runs for this shape: KDA_PATH_TENSOR_CORES
+ * (an intra-chunk and a state kernel on tcgen05/TMEM; bf16 inputs, dk = dv in
+ * {64, 128}, chunk 64), KDA_PATH_CUDA_CORES (one CUDA-core kernel per
+ * (sequence, head, 64-column slab), plus a norm-gate pass when gated), or
+ * KDA_PATH_UNSUPPORTED.  A host-side query; no device work.
+ */
+#define KDA_PATH_UNSUPPORTED 0
+#define KDA_PATH_CUDA_CORES 1
+#define KDA_PATH_TENSOR_CORES 2
+KDA_API int kda_prefill_path(int dk, int dv, int chunk, kda_dtype in_dtype);
 
 /* A static, human-readable name for a kda_status value. */
 KDA_API const char* kda_status_string(kda_status status);

@@ -20,7 +20,7 @@ __all__ = [
     "kda_status_string", "kda_version", "DEV_STATUS", "prefill_launches",
     "kda_prefill_chunked_static_scratch", "STATIC_SCRATCH_BYTES", "kda_decode_multi",
     "kda_commit_accepted", "kda_norm_gate_ex", "KDA_F16", "kda_causal_conv1d_prefill",
-    "kda_causal_conv1d_decode", "kda_testing_set_first_wait_tries",
+    "kda_causal_conv1d_decode", "kda_testing_set_first_wait_tries", "kda_prefill_path",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -69,6 +69,7 @@ _SIGNATURES = {
         ctypes.c_int, ctypes.c_int, _F32, _P, _P]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kda_testing_set_first_wait_tries": (None, [_I32, _I32]),
+    "kda_prefill_path": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "kda_version": (ctypes.c_int, []),
 }
 
@@ -205,11 +206,25 @@ def kda_prefill_workspace_bytes(N: int, T: int, H: int, dk: int, dv: int, chunk:
     return int(load().kda_prefill_workspace_bytes(N, T, H, dk, dv, chunk))
 
 
+PREFILL_PATHS = {0: "unsupported", 1: "cuda cores", 2: "tensor cores"}
+
+
+def kda_prefill_path(dk: int, dv: int, chunk: int, in_dtype) -> str:
+    """Which kernels kda_prefill_chunked runs for this shape (the library's
+    own answer): 'tensor cores', 'cuda cores' or 'unsupported'."""
+    code = load().kda_prefill_path(int(dk), int(dv), int(chunk), _dtype_of(in_dtype))
+    return PREFILL_PATHS[int(code)]
+
+
+def _dtype_of(dt) -> int:
+    return {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16, torch.float16: KDA_F16}[dt]
+
+
 def prefill_launches(dk: int, dv: int, chunk: int, in_dtype, gate: bool) -> int:
     """Kernel launches one kda_prefill_chunked call makes: the tensor-core path
-    (dk = dv = 128, chunk 64, bf16) runs an intra-chunk and a state kernel; the
-    CUDA-core path runs one kernel plus a norm-gate pass when gated."""
-    if dk == 128 and dv == 128 and chunk == 64 and in_dtype == torch.bfloat16:
+    runs an intra-chunk and a state kernel; the CUDA-core path runs one kernel
+    plus a norm-gate pass when gated."""
+    if kda_prefill_path(dk, dv, chunk, in_dtype) == "tensor cores":
         return 2
     return 2 if gate else 1
 

@@ -39,6 +39,13 @@ extern "C" {
 
 int kda_version(void) { return 105; }
 
+int kda_prefill_path(int dk, int dv, int chunk, kda_dtype in_dtype) {
+  if (!dim_ok(dk) || dv != dk || (chunk != 16 && chunk != 64) || !dtype_ok(in_dtype)) return KDA_PATH_UNSUPPORTED;
+  kda::PrefillParams q{};
+  q.dk = dk; q.dv = dv; q.chunk = chunk; q.in_dtype = in_dtype;
+  return kda::prefill_uses_tensor_cores(q) ? KDA_PATH_TENSOR_CORES : KDA_PATH_CUDA_CORES;
+}
+
 void kda_testing_set_first_wait_tries(int32_t tries, int32_t kernels) {
   for (int which = 0; which < 2; ++which)
     if (tries < 0 || (kernels >> which) & 1)

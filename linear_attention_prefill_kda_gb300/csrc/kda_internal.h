@@ -128,6 +128,8 @@ cudaError_t launch_norm_gate_ex(const NormGateExParams& p, cudaStream_t stream);
 cudaError_t launch_conv_prefill(const ConvParams& p, cudaStream_t stream);
 cudaError_t launch_conv_decode(const ConvParams& p, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
+// Whether launch_prefill takes the tensor-core kernels for this shape.
+bool prefill_uses_tensor_cores(const PrefillParams& p);
 // Upper bound over every option (what kda_prefill_workspace_bytes reports).
 size_t prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk);
 // What one call with these options actually uses (<= the bound).

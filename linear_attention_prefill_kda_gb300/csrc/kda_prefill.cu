@@ -63,6 +63,8 @@ size_t prefill_workspace_needed(int N, int64_t T, int H, int dk, int dv, int chu
   return ((size_t)T * (size_t)H * (size_t)dv * sizeof(float) + 255) & ~(size_t)255;
 }
 
+bool prefill_uses_tensor_cores(const PrefillParams& p) { return prefill_tc_supported(p); }
+
 cudaError_t launch_prefill(const PrefillParams& p_in, cudaStream_t stream) {
   if (prefill_tc_supported(p_in)) return launch_prefill_tc(p_in, stream);
   PrefillParams p = p_in;

@@ -1,5 +1,11 @@
 // Chunked KDA prefill on the Blackwell tensor cores (tcgen05 + TMEM), for
-// dk = dv = 128, chunk 64, bf16 inputs (fp32 or bf16 state).
+// dk = dv = DI in {64, 128}, chunk 64, bf16 inputs (fp32 or bf16 state).
+//
+// Every tile is 128 channels wide.  With DI = 64 the loads zero-fill channels
+// 64-127 of k, q, g and v, and the state, output and checkpoint stores cover
+// the first 64 rows and columns only: zero channels add nothing to A, W, U0
+// or the state, their decay is e^0 = 1, and the RMS of the norm-gate divides
+// by DI.
 //
 // Method ("[Feature][KDA] Add Kimi K3 KDA execution", section "KDA
 // execution", step 3).  For a chunk of rows r = 0..63 of one sequence and
@@ -189,20 +195,22 @@ __device__ void intra_exact_A(const bf16* fk, const bf16* fq, const float* fg, i
 
 // w * act(gate) for row r, channels [c0, c0 + 32) of a chunk -> fp16 in the
 // workspace (the output epilogue of the state kernel then needs two multiplies).
+template <int DI>
 __device__ __forceinline__ void gated_weight_rows(const PrefillParams& p, uint8_t* ws, int64_t tb, int head,
                                                   int n, int r, int c0) {
-  const bf16* gg = reinterpret_cast<const bf16*>(p.gate) + ((tb + r) * p.H + head) * D + c0;
-  const bf16* gw = reinterpret_cast<const bf16*>(p.norm_w) + c0;
+  const bool live = c0 < DI;  // channels past the head width weigh zero
+  const bf16* gg = reinterpret_cast<const bf16*>(p.gate) + ((tb + r) * p.H + head) * DI + (live ? c0 : 0);
+  const bf16* gw = reinterpret_cast<const bf16*>(p.norm_w) + (live ? c0 : 0);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     float x[8], w8[8];
-    if (r < n) {
+    if (r < n && live) {
       unpack_bf8(__ldg(reinterpret_cast<const uint4*>(gg) + i), x);
+      unpack_bf8(__ldg(reinterpret_cast<const uint4*>(gw) + i), w8);
     } else {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) x[u] = 0.f;
+      for (int u = 0; u < 8; ++u) x[u] = w8[u] = 0.f;
     }
-    unpack_bf8(__ldg(reinterpret_cast<const uint4*>(gw) + i), w8);
 #pragma unroll
     for (int u = 0; u < 8; ++u) x[u] = w8[u] * gate_actf(x[u], p.gate_act);
     *reinterpret_cast<uint4*>(ws + WS_GW + ((c0 + 8 * i) >> 3) * 1024 + r * 16) = pack_half8(x);
@@ -228,6 +236,7 @@ constexpr LTable make_ltable() {
 }
 __device__ __align__(16) const LTable g_ltable = make_ltable();
 
+template <int DI>
 __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p) {
   using namespace intra;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -322,23 +331,24 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     const int idx = tid + kThreads * s;
     const int t = idx >> 10, j = (idx >> 4) & (C - 1), piece = idx & 15;
     const bf16* base = reinterpret_cast<const bf16*>(t == 0 ? p.k : t == 1 ? p.q : p.g);
-    const bool has = j < n;
+    const bool has = j < n && piece * 8 < DI;  // zero rows past the chunk, zero channels past DI
     tc::cp_async16(sm + S_RAWK + t * RAW_BYTES + j * RAW_STRIDE + piece * 16,
-                   base + ((tb + (has ? j : 0)) * H + head) * (int64_t)D + piece * 8, has);
+                   base + ((tb + (has ? j : 0)) * H + head) * (int64_t)DI + (has ? piece * 8 : 0), has);
   }
   tc::cp_async_commit();
   if (warp >= 1 && warp <= 4) {
     const int s = tid - 32, t = s / C, j = s % C;  // t = 0: v, 1: gate
     if (j < n && (t == 0 || p.gate)) {
       const bf16* base = reinterpret_cast<const bf16*>(t == 0 ? p.v : p.gate);
-      tc::prefetch_l2(base + ((tb + j) * H + head) * (int64_t)D, 256);
+      tc::prefetch_l2(base + ((tb + j) * H + head) * (int64_t)DI, DI * 2);
     }
   }
   tc::cp_async_wait_all();
   __syncthreads();
   const bool valid = r < n;
-  const int64_t rowoff = ((tb + r) * H + head) * (int64_t)D + cb;
-  const int64_t row0off = (tb * H + head) * (int64_t)D + cb;  // a row that exists (for zero-filled copies)
+  const bool vlive = valid && cb < DI;  // this thread's v channels exist
+  const int64_t rowoff = ((tb + r) * H + head) * (int64_t)DI + cb;
+  const int64_t row0off = (tb * H + head) * (int64_t)DI;  // a row that exists (for zero-filled copies)
   uint4 kr[4], qr[4];  // k and q of row r, channels [cb, cb + 32) (zero rows past the chunk's end)
   {
     const uint8_t* rk = sm + S_RAWK + r * RAW_STRIDE + cb * 2;
@@ -497,9 +507,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
       }
       tc::mma_commit(&bar);
     }
-    if (p.gate) gated_weight_rows(p, ws, tb, head, n, r, cb);
+    if (p.gate) gated_weight_rows<DI>(p, ws, tb, head, n, r, cb);
   } else {
-    if (p.gate) gated_weight_rows(p, ws, tb, head, n, r, cb);
+    if (p.gate) gated_weight_rows<DI>(p, ws, tb, head, n, r, cb);
     // exact element-wise path: stage k, q, G for every row, write the
     // global-only operands with direct exponentials
     bf16* fk = reinterpret_cast<bf16*>(sm + S_FK);
@@ -530,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   }
   // V -> U0 operand (bf16 MN-major [K=j 64 x N=v 128]) by asynchronous 16-byte
   // copies, once the operand buffer it lands in is no longer read
-  const bf16* gv = reinterpret_cast<const bf16*>(p.v) + (valid ? rowoff : row0off);
+  const bf16* gv = reinterpret_cast<const bf16*>(p.v) + (vlive ? rowoff : row0off);
   float a32[32];
   uint4 kw[4];  // K e^G for row r, channels [cb, cb + 32) (bf16)
   if (!exact) {
@@ -539,7 +549,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     tc::fence_after_sync();
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      tc::cp_async16(sm + S_VB + mnmaj(cb + 8 * i, r, 2048), reinterpret_cast<const uint4*>(gv) + i, valid);
+      tc::cp_async16(sm + S_VB + mnmaj(cb + 8 * i, r, 2048), reinterpret_cast<const uint4*>(gv) + (vlive ? i : 0),
+                     vlive);
     tc::cp_async_commit();
     if (ok) {
       tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, 128 + hh * 32), a32);
@@ -593,7 +604,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   if (exact) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      tc::cp_async16(sm + S_VB + mnmaj(cb + 8 * i, r, 2048), reinterpret_cast<const uint4*>(gv) + i, valid);
+      tc::cp_async16(sm + S_VB + mnmaj(cb + 8 * i, r, 2048), reinterpret_cast<const uint4*>(gv) + (vlive ? i : 0),
+                     vlive);
     tc::cp_async_commit();
   }
   float* s_akk = reinterpret_cast<float*>(sm + S_AKK);
@@ -868,14 +880,18 @@ __device__ __forceinline__ void transpose8x8(V4 (&v)[8], int lane) {
 // through transpose8x8 so that each memory instruction of a warp covers four
 // whole 128-byte (fp32) row segments instead of 32 scattered 16-byte pieces.
 // Warp-collective: every lane must take part.
-template <typename TS>
+// With DI < 128 the block is DI x DI and the rows and columns past DI read as
+// zero and are not stored.
+template <int DI, typename TS>
 __device__ __forceinline__ void load_state_block(const TS* blk, float* s, int quad, int lane, int hh) {
   const int rbase = 32 * quad + 8 * (lane >> 3), j = lane & 7;
 #pragma unroll
   for (int h2 = 0; h2 < 2; ++h2) {
     float4 v[8];
+    const int col = hh * 64 + 32 * h2 + 4 * j;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) v[c] = load4(blk + (rbase + c) * D + hh * 64 + 32 * h2 + 4 * j);
+    for (int c = 0; c < 8; ++c)
+      v[c] = (rbase + c < DI && col < DI) ? load4(blk + (rbase + c) * DI + col) : make_float4(0.f, 0.f, 0.f, 0.f);
     transpose8x8(v, lane);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -884,7 +900,7 @@ __device__ __forceinline__ void load_state_block(const TS* blk, float* s, int qu
     }
   }
 }
-template <typename TS>
+template <int DI, typename TS>
 __device__ __forceinline__ void store_state_block(TS* blk, const float* s, int quad, int lane, int hh) {
   const int rbase = 32 * quad + 8 * (lane >> 3), j = lane & 7;
 #pragma unroll
@@ -894,12 +910,14 @@ __device__ __forceinline__ void store_state_block(TS* blk, const float* s, int q
     for (int c = 0; c < 8; ++c)
       v[c] = make_float4(s[32 * h2 + 4 * c], s[32 * h2 + 4 * c + 1], s[32 * h2 + 4 * c + 2], s[32 * h2 + 4 * c + 3]);
     transpose8x8(v, lane);
+    const int col = hh * 64 + 32 * h2 + 4 * j;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) store4(blk + (rbase + c) * D + hh * 64 + 32 * h2 + 4 * j, v[c]);
+    for (int c = 0; c < 8; ++c)
+      if (rbase + c < DI && col < DI) store4(blk + (rbase + c) * DI + col, v[c]);
   }
 }
 
-template <typename TS>
+template <typename TS, int DI>
 __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p) {
   using namespace state;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -917,7 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
 
   SeqInfo si;
   if (!seq_prologue(p, seq, head, true, si)) {
-    if (si.zero_rows) zero_out_rows<bf16>(p, si.t0, si.t1, head, 0, D, D);
+    if (si.zero_rows) zero_out_rows<bf16>(p, si.t0, si.t1, head, 0, DI, DI);
     return;
   }
   const int64_t t0 = si.t0;
@@ -939,10 +957,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   }
   float* s_ss = reinterpret_cast<float*>(sm + S_SS);
   // state row lrow, columns [64 hh, 64 hh + 64), fp32 in registers for the whole call
-  TS* slot_state = reinterpret_cast<TS*>(p.state_pool) + ((int64_t)si.slot * H + head) * (D * D);
+  TS* slot_state = reinterpret_cast<TS*>(p.state_pool) + ((int64_t)si.slot * H + head) * (DI * DI);
   float S[64];
   if (si.init) {
-    load_state_block(slot_state, S, quad, lane, hh);
+    load_state_block<DI>(slot_state, S, quad, lane, hh);
   } else {
 #pragma unroll
     for (int i = 0; i < 64; ++i) S[i] = 0.f;
@@ -1019,11 +1037,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
       ssb[hh * 64 + orow] = ss;
       asm volatile("bar.sync 1, 128;" ::: "memory");
     }
-    if (ok_o && (staged || orow < n)) {
+    if (ok_o && (staged || (orow < n && hh * 64 < DI))) {
       uint4* dst = staged ? reinterpret_cast<uint4*>(sm + S_OSTG + orow * OSTG_ROW + hh * 128)
-                          : reinterpret_cast<uint4*>(gout + ((t0 + c0 + orow) * H + head) * D + hh * 64);
+                          : reinterpret_cast<uint4*>(gout + ((t0 + c0 + orow) * H + head) * DI + hh * 64);
       float inv = 1.f;
-      if (p.gate) inv = rsqrtf((ssb[orow] + ssb[64 + orow]) * (1.f / (float)D) + p.eps);
+      if (p.gate) inv = rsqrtf((ssb[orow] + ssb[64 + orow]) * (1.f / (float)DI) + p.eps);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float y[8];
@@ -1044,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
   int64_t pending_ck = -1;  // checkpoint entry whose store is still to be issued
   auto store_pending_ck = [&]() {
     if (pending_ck >= 0) {
-      store_state_block(reinterpret_cast<TS*>(p.checkpoints) + (pending_ck * H + head) * (int64_t)(D * D), S, quad,
+      store_state_block<DI>(reinterpret_cast<TS*>(p.checkpoints) + (pending_ck * H + head) * (int64_t)(DI * DI), S, quad,
                         lane, hh);
       pending_ck = -1;
     }
@@ -1149,8 +1167,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int row = 16 * kw + 2 * i + (lane >> 4), ch = lane & 15;
-        if (row < np)
-          reinterpret_cast<uint4*>(gout + ((t0 + (int64_t)(k - 1) * C + row) * H + head) * D)[ch] =
+        if (row < np && ch * 8 < DI)
+          reinterpret_cast<uint4*>(gout + ((t0 + (int64_t)(k - 1) * C + row) * H + head) * DI)[ch] =
               *reinterpret_cast<const uint4*>(sm + S_OSTG + row * OSTG_ROW + ch * 16);
       }
     }
@@ -1194,7 +1212,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     }
   } else {
     store_pending_ck();
-    store_state_block(slot_state, S, quad, lane, hh);
+    store_state_block<DI>(slot_state, S, quad, lane, hh);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1204,25 +1222,26 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
 }  // namespace tcp
 
 bool prefill_tc_supported(const PrefillParams& p) {
-  return p.dk == tcp::D && p.dv == tcp::D && p.chunk == tcp::C && p.in_dtype == KDA_BF16;
+  return p.dk == p.dv && (p.dk == tcp::D || p.dk == 64) && p.chunk == tcp::C && p.in_dtype == KDA_BF16;
 }
 
 size_t prefill_tc_workspace_bytes(int N, int64_t T, int H) {
   return (size_t)tcp::num_slots_bound(T, N) * (size_t)H * tcp::WS_BYTES;
 }
 
-cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(tcp::kda_intra_kernel), (int)tcp::intra::SMEM_BYTES);
+template <int DI>
+static cudaError_t launch_prefill_tc_d(const PrefillParams& p, cudaStream_t stream) {
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(tcp::kda_intra_kernel<DI>), (int)tcp::intra::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const void* sk = p.state_dtype == KDA_F32 ? reinterpret_cast<const void*>(tcp::kda_state_kernel<float>)
-                                            : reinterpret_cast<const void*>(tcp::kda_state_kernel<bf16>);
+  const void* sk = p.state_dtype == KDA_F32 ? reinterpret_cast<const void*>(tcp::kda_state_kernel<float, DI>)
+                                            : reinterpret_cast<const void*>(tcp::kda_state_kernel<bf16, DI>);
   e = set_smem_once(sk, (int)tcp::state::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int64_t slots = tcp::num_slots_bound(p.T, p.N);
   const bool intra = p.T > 0 && slots > 0;
   if (intra) {
     dim3 g1((unsigned)(slots * p.H));
-    tcp::kda_intra_kernel<<<g1, tcp::kThreads, tcp::intra::SMEM_BYTES, stream>>>(p);
+    tcp::kda_intra_kernel<DI><<<g1, tcp::kThreads, tcp::intra::SMEM_BYTES, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1239,8 +1258,12 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = intra ? 1 : 0;
-  if (p.state_dtype == KDA_F32) return cudaLaunchKernelEx(&cfg, tcp::kda_state_kernel<float>, p);
-  return cudaLaunchKernelEx(&cfg, tcp::kda_state_kernel<bf16>, p);
+  if (p.state_dtype == KDA_F32) return cudaLaunchKernelEx(&cfg, tcp::kda_state_kernel<float, DI>, p);
+  return cudaLaunchKernelEx(&cfg, tcp::kda_state_kernel<bf16, DI>, p);
+}
+
+cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
+  return p.dk == 64 ? launch_prefill_tc_d<64>(p, stream) : launch_prefill_tc_d<tcp::D>(p, stream);
 }
 
 }  // namespace kda

@@ -292,3 +292,18 @@ def test_binding_rejects_tensors_on_two_devices():
     for call in calls:
         with pytest.raises(ValueError, match="one CUDA device"):
             call()
+
+
+def test_prefill_path_query(lib):
+    """The library's own answer to which kernels a prefill shape takes: the
+    tensor-core kernels for bf16 inputs, dk = dv in {64, 128}, chunk 64; the
+    CUDA-core kernel otherwise; unsupported shapes say so."""
+    assert kda.kda_prefill_path(128, 128, 64, torch.bfloat16) == "tensor cores"
+    assert kda.kda_prefill_path(64, 64, 64, torch.bfloat16) == "tensor cores"
+    assert kda.kda_prefill_path(16, 16, 16, torch.float32) == "cuda cores"
+    assert kda.kda_prefill_path(16, 16, 64, torch.bfloat16) == "cuda cores"
+    assert kda.kda_prefill_path(128, 128, 16, torch.bfloat16) == "cuda cores"
+    assert kda.kda_prefill_path(128, 128, 64, torch.float32) == "cuda cores"
+    assert kda.kda_prefill_path(96, 96, 64, torch.bfloat16) == "unsupported"
+    assert kda.kda_prefill_path(64, 128, 64, torch.bfloat16) == "unsupported"
+    assert kda.prefill_launches(64, 64, 64, torch.bfloat16, gate=False) == 2

@@ -59,7 +59,20 @@ def test_prefill_tiny(kda_gpu):
 
 
 def test_prefill_varlen(kda_gpu):
+    # d = 64, bf16, chunk 64: the tensor-core kernels (tiles zero-padded to 128 channels)
+    assert kda_gpu.kda_prefill_path(64, 64, 64, torch.bfloat16) == "tensor cores"
     _check_prefill(kda_gpu, W.VARLEN, W.make_prefill(W.VARLEN), label=W.VARLEN.name)
+
+
+def test_prefill_d64_tensor_cores_gate_and_bf16_state(kda_gpu):
+    """The d = 64 tensor-core path with the fused norm-gate (mean over 64
+    columns), bf16 state and checkpoints, lengths around the chunk edges and a
+    padding sequence."""
+    w = W.SCHED.replace(seqlens=(1, 63, 64, 65, 0, 200, 130), H=6, dk=64, dv=64, num_slots=12,
+                        slot_range=None, state_dtype=torch.bfloat16, checkpoint_every=64, seed=264)
+    d = W.make_prefill(w)
+    d["state_indices"][4] = -1
+    _check_prefill(kda_gpu, w, d)
 
 
 def test_prefill_sched_full(kda_gpu):
