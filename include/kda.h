@@ -75,6 +75,7 @@ typedef enum { KDA_GATE_SIGMOID = 0, KDA_GATE_SILU = 1 } kda_gate_act;
 #define KDA_DEV_BAD_SEQLENS 2     /* cu_seqlens not non-decreasing within [0, T] */
 #define KDA_DEV_TIMEOUT 3         /* a bounded on-chip wait gave up */
 #define KDA_DEV_CKPT_OVERFLOW 4   /* checkpoints would exceed checkpoint_capacity */
+#define KDA_DEV_DUP_INDEX 5       /* one state slot named by two sequences of a call */
 
 /*
  * Bytes of caller-owned scratch that always suffice for kda_prefill_chunked
@@ -106,7 +107,9 @@ KDA_API size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int 
  *               state_pool[state_indices[i]] and its final state is written
  *               back to that slot in place.  -1 marks a padding sequence: its
  *               output rows are zeroed and the pool is untouched.  Indices
- *               must be distinct within a call.
+ *               must be distinct within a call: a repeated index latches
+ *               KDA_DEV_DUP_INDEX, and the results of the sequences that
+ *               share the slot are undefined.
  *  has_initial_state int32 [N], device, or NULL (every sequence has state).
  *               0 marks a sequence without initial state -- a new prompt
  *               ("[Feature][KDA] ...", section "Metadata construction": a

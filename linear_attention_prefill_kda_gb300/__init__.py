@@ -31,7 +31,7 @@ KDA_OK, KDA_F32, KDA_BF16, KDA_F16 = 0, 0, 1, 2
 GATE_ACT = {"sigmoid": 0, "silu": 1}  # kda_gate_act
 STATIC_SCRATCH_BYTES = 128 << 20  # KDA_STATIC_SCRATCH_BYTES in include/kda.h
 DEV_STATUS = {0: "ok", 1: "bad state index", 2: "bad cu_seqlens", 3: "on-chip wait timeout",
-              4: "checkpoint capacity exceeded"}
+              4: "checkpoint capacity exceeded", 5: "state slot named twice in one call"}
 
 _P = ctypes.c_void_p
 _I32, _I64, _F32, _SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t

@@ -87,6 +87,24 @@ __device__ __forceinline__ void latch_status(int32_t* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// A state slot that an earlier sequence of the same call also names: the two
+// sequences would read and write one state concurrently.  Run by the threads
+// of one CTA per sequence (no barrier); `live(j)` says whether sequence j
+// uses its slot at all.
+template <typename Live>
+__device__ __forceinline__ void check_duplicate_slot(const int32_t* idx, int seq, int32_t slot, int32_t* status,
+                                                     Live live) {
+  if (slot < 0) return;
+  for (int j = threadIdx.x; j < seq; j += blockDim.x)
+    if (idx[j] == slot && live(j)) {
+      latch_status(status, KDA_DEV_DUP_INDEX);
+      break;
+    }
+}
+__device__ __forceinline__ void check_duplicate_slot(const int32_t* idx, int seq, int32_t slot, int32_t* status) {
+  check_duplicate_slot(idx, seq, slot, status, [](int) { return true; });
+}
+
 __device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 // Gate activation of the RMSNorm-gate: sigmoid (act 0) or SiLU x*sigmoid(x) (act 1).

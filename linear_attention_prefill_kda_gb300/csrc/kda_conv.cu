@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 4) conv_prefill_kernel(ConvPa
     }
     return;
   }
+  if (k == 0 && blockIdx.x == 0) check_duplicate_slot(p.state_indices, seq, sidx, p.dev_status);
   T* cache = reinterpret_cast<T*>(p.pool) + (int64_t)sidx * WM * C;
   const bool init = s_init != 0;
   // Stage each sub-block as its own group of 16-byte asynchronous copies: row
@@ -333,6 +334,14 @@ __global__ void __launch_bounds__(kThreads) conv_decode_kernel(ConvParams p) {
     const float z[kVec] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     store8(y, z);
     return;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    // one thread per sequence scans the earlier sequences' cache slots
+    for (int j = 0; j < seq; ++j)
+      if (p.state_indices[j] == sidx) {
+        latch_status(p.dev_status, KDA_DEV_DUP_INDEX);
+        break;
+      }
   }
   T* cache = reinterpret_cast<T*>(p.pool) + (int64_t)sidx * WM * C + c0;
   float win[WM][kVec], xv[kVec], bs[kVec], acc[kVec];

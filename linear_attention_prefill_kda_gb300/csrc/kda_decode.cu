@@ -55,6 +55,7 @@ decode_kernel(DecodeParams p) {
     for (int j = tid; j < DV; j += blockDim.x) out[j] = from_f32<TI>(0.f);
     return;
   }
+  if (head == 0) check_duplicate_slot(p.state_indices, seq, slot, p.dev_status);
   TS* S = reinterpret_cast<TS*>(p.state_pool) + ((int64_t)slot * p.H + head) * (DK * DV);
 
   // Issue the state loads first: they are the whole cost of the step.

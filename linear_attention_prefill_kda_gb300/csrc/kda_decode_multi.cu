@@ -58,6 +58,7 @@ decode_multi_kernel(DecodeMultiParams p) {
     }
     return;
   }
+  if (head == 0) check_duplicate_slot(p.state_indices, seq, slot, p.dev_status);
   TS* S = reinterpret_cast<TS*>(p.state_pool) + ((int64_t)slot * H + head) * (DK * DV);
   float4 st[RPT];
 #pragma unroll
@@ -167,6 +168,9 @@ __global__ void __launch_bounds__(256) commit_kernel(CommitParams p) {
     if (threadIdx.x == 0) latch_status(p.dev_status, KDA_DEV_BAD_INDEX);
     return;
   }
+  if (head == 0)
+    check_duplicate_slot(p.state_indices, seq, slot, p.dev_status,
+                         [&](int j) { return p.num_accepted[j] > 0; });
   const int64_t elems = (int64_t)p.dk * p.dv;
   const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const TS*>(p.token_states) +
                                                     (((int64_t)seq * p.K + (a - 1)) * p.H + head) * elems);

@@ -65,6 +65,7 @@ __device__ __forceinline__ bool seq_prologue(const PrefillParams& p, int seq, in
     si.zero_rows = true;
     return false;
   }
+  if (first_slab && head == 0) check_duplicate_slot(p.state_indices, seq, si.slot, p.dev_status);
   if (len == 0) return false;
   if (I > 0) {
     si.ckpt_ok = si.ckpt_off + len / I <= p.checkpoint_capacity;

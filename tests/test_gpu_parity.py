@@ -178,6 +178,77 @@ def test_prefill_bad_index_latches_status(kda_gpu):
             assert torch.equal(p[s], pool0[s])
 
 
+@pytest.mark.parametrize("d,in_dtype", [(128, torch.bfloat16), (64, torch.float32)],
+                         ids=["tensor-cores", "cuda-cores"])
+def test_duplicate_slot_latches_status(kda_gpu, d, in_dtype):
+    """Two sequences of one call naming the same state slot (or conv cache
+    slot) would race on it: every kernel family reports KDA_DEV_DUP_INDEX (5).
+    The values of the sequences involved are undefined; the other slots stay
+    untouched."""
+    w = W.SCHED.replace(seqlens=(70, 30, 40), H=2, dk=d, dv=d, in_dtype=in_dtype, num_slots=8,
+                        slot_range=None, checkpoint_every=0, seed=55)
+    dd = W.make_prefill(w)
+    dd["state_indices"] = torch.tensor([3, 5, 3], dtype=torch.int32)
+    pool0 = dd["pool"].clone()
+    out, pool, _, _, status = run_prefill(kda_gpu, dd, w, DEV, ckpt=False)
+    assert int(status.item()) == 5
+    p = pool.cpu()
+    for slot in range(w.num_slots):
+        if slot not in (3, 5):
+            assert torch.equal(p[slot], pool0[slot])
+    # decode, verification + commit, convolution: the same report
+    dw = W.DECODE.replace(N=3, H=2, dk=64, dv=64, num_slots=8)
+    pd = W.make_decode_pool(dw)
+    idx = torch.tensor([6, 1, 6], dtype=torch.int32, device=DEV)
+    for kind in ("decode", "verify", "commit"):
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        dpool = pd["pool"].to(DEV)
+        if kind == "decode":
+            sd = to_dev(W.make_decode_step(dw, 0), DEV)
+            o = torch.empty(dw.N, dw.H, dw.dv, device=DEV, dtype=dw.in_dtype)
+            kda_gpu.kda_decode_step(sd["q"], sd["k"], sd["v"], sd["g"], sd["beta"], idx, dpool, o,
+                                    dev_status=status)
+        else:
+            dr = W.make_decode_draft(dw, 2)
+            dr.pop("num_accepted")
+            t = to_dev(dr, DEV)
+            o = torch.empty(dw.N, 2, dw.H, dw.dv, device=DEV, dtype=dw.in_dtype)
+            ts = torch.empty(dw.N, 2, dw.H, dw.dk, dw.dv, device=DEV, dtype=dw.state_dtype)
+            if kind == "verify":
+                kda_gpu.kda_decode_multi(t["q"], t["k"], t["v"], t["g"], t["beta"], idx, dpool, o, ts,
+                                         dev_status=status)
+            else:
+                kda_gpu.kda_decode_multi(t["q"], t["k"], t["v"], t["g"], t["beta"],
+                                         torch.tensor([6, 1, 2], dtype=torch.int32, device=DEV), dpool,
+                                         o, ts)
+                acc = torch.tensor([1, 0, 2], dtype=torch.int32, device=DEV)
+                kda_gpu.kda_commit_accepted(ts, acc, idx, dpool, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 5, kind
+    # a repeated slot whose second user commits nothing is not a conflict
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda_gpu.kda_commit_accepted(ts, torch.tensor([1, 0, 0], dtype=torch.int32, device=DEV), idx,
+                                dpool, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    cd = W.make_conv((20, 9, 33), 64, 4, torch.bfloat16, num_slots=6, seed=3)
+    cd = to_dev(cd, DEV)
+    cidx = torch.tensor([2, 4, 2], dtype=torch.int32, device=DEV)
+    for prefill in (True, False):
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        if prefill:
+            y = torch.empty_like(cd["x"])
+            kda_gpu.kda_causal_conv1d_prefill(cd["x"], cd["w"], cd["cu_seqlens"], cidx, cd["pool"], y,
+                                              bias=cd["b"], dev_status=status)
+        else:
+            x1 = cd["x"][:3].contiguous()
+            y1 = torch.empty_like(x1)
+            kda_gpu.kda_causal_conv1d_decode(x1, cd["w"], cidx, cd["pool"], y1, bias=cd["b"],
+                                             dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 5, ("conv", prefill)
+
+
 def test_prefill_longprompt_bf16_state(kda_gpu):
     """One 32768-token sequence as 8 calls of 4096 carrying bf16 state through
     the pool, against the one-shot fp64 oracle (every head) and against a
