@@ -274,3 +274,52 @@ def conv_decode(x, w, state_indices, pool, *, bias=None, act="silu"):
     N = x.shape[0]
     cu = np.arange(N + 1, dtype=np.int32)
     return conv_prefill(x, w, cu, state_indices, pool, bias=bias, act=act)
+
+
+def l2_normalize(x, eps=1e-6):
+    """Rows of unit L2 norm over the last axis: x / sqrt(sum(x^2) + eps), in
+    fp64.  The pages apply the short convolution to Q/K/V and then run the
+    chunk prefill ("[Feature][KDA] Add Kimi K3 KDA execution", "KDA
+    execution" steps 2-3); the recurrence's regime is q and k rows of unit
+    norm, so the composed operator normalises q and k per (token, head) in
+    between (the eps keeps a zero row at zero)."""
+    x = _f64(x)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+def _stored(x, dtype):
+    """``x`` as a tensor of ``dtype`` would hold it (round to nearest even),
+    widened back to fp64: the value a stage of the pipeline hands to the next
+    through a tensor of that dtype."""
+    import torch
+    return torch.from_numpy(_f64(x)).to(dtype).double().numpy()
+
+
+def prefill_conv(xq, xk, xv, conv_w, cu_seqlens, state_indices, pool, conv_pool, *, conv_bias=None,
+                 conv_act="silu", has_initial_state=None, dtype=None, l2_eps=1e-6, **prefill_kw):
+    """The convolution, the normalisation and the chunk prefill as the pages'
+    pipeline runs them, each stage reading the previous one's output tensor:
+
+      q, k, v = act(conv(x)) over the packed channels [q | k | v] of each
+                token, with the convolution cache of state_indices[i]
+                (conv_prefill), stored in ``dtype``;
+      q, k    = l2_normalize per (token, head), stored in ``dtype``;
+      the chunked prefill (prefill) on q, k, v and the caller's g, beta.
+
+    xq, xk, xv [T, H, d]; conv_w [3*H*d, W] (channels q, then k, then v, head
+    by head); conv_pool [slots, W-1, 3*H*d].  ``dtype`` (a torch dtype, or None
+    for no rounding) is the activation dtype.  Returns ``(out, pool_after,
+    checkpoints, ckpt_offsets, conv_pool_after)``."""
+    xq, xk, xv = _f64(xq), _f64(xk), _f64(xv)
+    T, H, d = xq.shape
+    x = np.concatenate([xq.reshape(T, H * d), xk.reshape(T, H * d), xv.reshape(T, H * d)], axis=1)
+    y, conv_after = conv_prefill(x, conv_w, cu_seqlens, state_indices, conv_pool, bias=conv_bias,
+                                 has_initial_state=has_initial_state, act=conv_act)
+    rnd = (lambda a: a) if dtype is None else (lambda a: _stored(a, dtype))
+    y = rnd(y)
+    q, k, v = (y[:, i * H * d:(i + 1) * H * d].reshape(T, H, d) for i in range(3))
+    q, k = rnd(l2_normalize(q, l2_eps)), rnd(l2_normalize(k, l2_eps))
+    out, pool_after, ck, offs = prefill(q, k, v, prefill_kw.pop("g"), prefill_kw.pop("beta"), cu_seqlens,
+                                        state_indices, pool, has_initial_state=has_initial_state,
+                                        **prefill_kw)
+    return out, pool_after, ck, offs, conv_after

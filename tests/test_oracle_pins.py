@@ -552,3 +552,72 @@ def test_conv_split_decode_and_flags():
     assert np.all(yp == 0) and np.array_equal(pp, pool)
     ya, _ = oracle.conv_prefill(x, w, cu, idx, pool, bias=b, act="none")
     np.testing.assert_allclose(y, ya / (1 + np.exp(-ya)), atol=1e-14)
+
+
+def test_l2_normalize_hand_worked_and_invariants():
+    """x / sqrt(sum x^2 + eps): [3, 4] -> [0.6, 0.8] (eps = 0), a zero row
+    stays zero, and rows of any scale come out with norm sqrt(s / (s + eps))."""
+    np.testing.assert_allclose(oracle.l2_normalize(np.array([[3.0, 4.0]]), eps=0.0), [[0.6, 0.8]],
+                               rtol=0, atol=1e-15)
+    assert not np.any(oracle.l2_normalize(np.zeros((2, 5))))
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((7, 3, 16)) * rng.uniform(1e-2, 1e2, (7, 3, 1))
+    y = oracle.l2_normalize(x, eps=1e-6)
+    s = np.sum(x * x, axis=-1)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.sqrt(s / (s + 1e-6)), rtol=1e-13)
+    # direction unchanged: y is a positive multiple of x
+    np.testing.assert_allclose(y * np.linalg.norm(x, axis=-1, keepdims=True),
+                               x * np.linalg.norm(y, axis=-1, keepdims=True), rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_conv_with_identity_taps_is_the_plain_prefill():
+    """A convolution whose only tap is the current token (taps [0, 0, 0, 1], no
+    bias, no activation) passes x through, so on q, k rows that already have
+    unit norm the composed operator is the plain prefill; v is passed through
+    unnormalised; the cache afterwards holds each sequence's last 3 inputs."""
+    rng = np.random.default_rng(21)
+    T, H, dd = 16, 2, 8
+    q, k, v, g, beta = _rand_inputs(rng, T, H, dd, dd)
+    cu = np.array([0, 5, 16], np.int32)
+    idx = np.array([3, 1], np.int32)
+    pool = rng.standard_normal((4, H, dd, dd)) * 0.1
+    C = 3 * H * dd
+    taps = np.zeros((C, 4))
+    taps[:, 3] = 1.0
+    conv_pool = rng.standard_normal((4, 3, C))
+    out_c, pool_c, _, _, conv_after = oracle.prefill_conv(
+        q, k, v, taps, cu, idx, pool, conv_pool, conv_act="none", l2_eps=0.0, g=g, beta=beta)
+    out_p, pool_p, _, _ = oracle.prefill(q, k, v, g, beta, cu, idx, pool)
+    np.testing.assert_allclose(out_c, out_p, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(pool_c, pool_p, rtol=0, atol=1e-12)
+    x = np.concatenate([a.reshape(T, H * dd) for a in (q, k, v)], axis=1)
+    for i, slot in enumerate(idx.tolist()):
+        np.testing.assert_array_equal(conv_after[slot], x[cu[i + 1] - 3:cu[i + 1]])
+
+
+def test_prefill_conv_order_of_stages():
+    """Swapping the q and k channel blocks, or normalising v as well, changes
+    the result: the composition reads the blocks in the order q, k, v and
+    normalises q and k only."""
+    rng = np.random.default_rng(33)
+    _, _, _, g, beta = _rand_inputs(rng, 9, 1, 4, 4)
+    cu, idx = _one_seq(9)
+    pool = rng.standard_normal((1, 1, 4, 4)) * 0.1
+    C = 12
+    taps = rng.standard_normal((C, 4)) * 0.5
+    conv_pool = rng.standard_normal((1, 3, C))
+    xq, xk, xv = (rng.standard_normal((9, 1, 4)) for _ in range(3))
+    kw = dict(conv_act="silu", g=g, beta=beta)
+    ref = oracle.prefill_conv(xq, xk, xv, taps, cu, idx, pool, conv_pool, **kw)[0]
+    perm = [*range(4, 8), *range(4), *range(8, 12)]
+    swapped = oracle.prefill_conv(xk, xq, xv, taps[perm], cu, idx, pool, conv_pool[:, :, perm], **kw)[0]
+    assert np.max(np.abs(ref - swapped)) > 1e-3
+    y, _ = oracle.conv_prefill(np.concatenate([xq[:, 0], xk[:, 0], xv[:, 0]], axis=1), taps, cu, idx,
+                               conv_pool, act="silu")
+    q, k, v = (y[:, 4 * i:4 * i + 4].reshape(9, 1, 4) for i in range(3))
+    # v normalised as well (a plausible mistake) gives another answer
+    wrong = oracle.prefill(oracle.l2_normalize(q), oracle.l2_normalize(k), oracle.l2_normalize(v), g,
+                           beta, cu, idx, pool)[0]
+    assert np.max(np.abs(ref - wrong)) > 1e-3
+    right = oracle.prefill(oracle.l2_normalize(q), oracle.l2_normalize(k), v, g, beta, cu, idx, pool)[0]
+    np.testing.assert_allclose(ref, right, rtol=0, atol=1e-12)
