@@ -291,6 +291,48 @@ KDA_API kda_status kda_causal_conv1d_decode(const void* x, const void* weight, c
                                     int32_t* dev_status, void* stream);
 
 /*
+ * The short convolution, the L2 normalisation of q and k and the chunked
+ * prefill in one pass ("[Feature][KDA] Add Kimi K3 KDA execution", section
+ * "KDA execution", steps 2-3: the causal convolution with its cache update,
+ * then the chunk prefill on its output).  Per token and head, with the
+ * convolution and cache of kda_causal_conv1d_prefill over the packed channels
+ * [q | k | v] (channels = 3 H d, head by head within each block):
+ *     y        = act(conv(x)) rounded to bf16
+ *     q, k     = y_q / sqrt(|y_q|^2 + KDA_CONV_L2_EPS), y_k / ..., rounded to bf16
+ *     v        = y_v
+ * then everything kda_prefill_chunked does with those q, k, v and the given
+ * g, beta (state pool, checkpoints, fused norm-gate).  The results equal
+ * kda_causal_conv1d_prefill, a per-(token, head) L2 normalisation stored in
+ * bf16, and kda_prefill_chunked, run in sequence -- without the intermediate
+ * tensors (q, k, v are never written to memory).
+ *  x_q, x_k, x_v  [T, H, d] bf16 rows of x_row_stride elements (a multiple of
+ *                 8, at least H d): for a packed projection output [T, 3 H d]
+ *                 pass its base, base + H d, base + 2 H d and 3 H d.
+ *  conv_w         [3 H d, W] bf16; conv_b [3 H d] bf16 or NULL; W in {2, 3, 4}.
+ *  conv_state_pool [conv_num_slots, W-1, 3 H d] bf16, indexed by the same
+ *                 state_indices as the state pool and read as initial context
+ *                 under the same has_initial_state flag; rewritten with each
+ *                 sequence's last W-1 extended inputs (an empty sequence or a
+ *                 padding index leaves its slot alone).
+ * Other arguments as for kda_prefill_chunked (same workspace size).  Supported
+ * only where kda_prefill_path reports KDA_PATH_TENSOR_CORES (bf16 inputs,
+ * dk = dv in {64, 128}, chunk 64); otherwise KDA_ERR_UNSUPPORTED, as for W
+ * outside {2, 3, 4}.  KDA_ERR_INVALID_ARG for an unknown act, a bad row
+ * stride, conv_num_slots <= 0 or a NULL/misaligned convolution pointer.  An
+ * index at or above conv_num_slots latches KDA_DEV_BAD_INDEX like one at or
+ * above num_slots.
+ */
+#define KDA_CONV_L2_EPS 1e-6f
+KDA_API kda_status kda_prefill_chunked_conv(
+    const void* x_q, const void* x_k, const void* x_v, int64_t x_row_stride, const void* conv_w,
+    const void* conv_b, int conv_width, kda_conv_act conv_act, void* conv_state_pool, int64_t conv_num_slots,
+    const void* g, const void* beta, kda_dtype in_dtype, const int32_t* cu_seqlens, int N, int64_t T,
+    const int32_t* state_indices, const int32_t* has_initial_state, void* state_pool, int64_t num_slots,
+    kda_dtype state_dtype, void* out, void* checkpoints, int32_t checkpoint_every, int64_t checkpoint_capacity,
+    int32_t* ckpt_offsets, const void* gate, const void* norm_w, float eps, kda_gate_act gate_act, int H, int dk,
+    int dv, int chunk, float scale, void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
  * Chunked prefill without caller scratch.  The pages have no counterpart of
  * this entry point; it serves callers that cannot allocate device memory where
  * they run the prefill (for example code running under strict-mode stream

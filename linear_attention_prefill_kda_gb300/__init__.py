@@ -21,6 +21,7 @@ __all__ = [
     "kda_prefill_chunked_static_scratch", "STATIC_SCRATCH_BYTES", "kda_decode_multi",
     "kda_commit_accepted", "kda_norm_gate_ex", "KDA_F16", "kda_causal_conv1d_prefill",
     "kda_causal_conv1d_decode", "kda_testing_set_first_wait_tries", "kda_prefill_path",
+    "kda_prefill_chunked_conv",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -67,6 +68,11 @@ _SIGNATURES = {
         _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_int, _I64, _P, _P, _P, _I64, ctypes.c_int,
         _P, _P, _I32, _I64, _P, _P, _P, _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_int, _F32, _P, _P]),
+    "kda_prefill_chunked_conv": (ctypes.c_int, [
+        _P, _P, _P, _I64, _P, _P, ctypes.c_int, ctypes.c_int, _P, _I64,
+        _P, _P, ctypes.c_int, _P, ctypes.c_int, _I64, _P, _P, _P, _I64, ctypes.c_int,
+        _P, _P, _I32, _I64, _P, _P, _P, _F32, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, _F32, _P, _SZ, _P, _P]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kda_testing_set_first_wait_tries": (None, [_I32, _I32]),
     "kda_prefill_path": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
@@ -143,15 +149,27 @@ def _need_prefill(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, 
                   ckpt_offsets, gate, norm_w, has_initial_state, dev_status):
     T, H, dk = q.shape
     dv = v.shape[-1]
-    N = state_indices.shape[0]
     dev = q.device
     _one_device(dev, k=k, v=v, g=g, beta=beta, cu_seqlens=cu_seqlens, state_indices=state_indices,
                 state_pool=state_pool, out=out, checkpoints=checkpoints, ckpt_offsets=ckpt_offsets,
                 gate=gate, norm_w=norm_w, has_initial_state=has_initial_state, dev_status=dev_status)
-    for name, t, shape in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("g", g, (T, H, dk)),
-                           ("v", v, (T, H, dv)), ("beta", beta, (T, H)), ("out", out, (T, H, dv)),
-                           ("gate", gate, (T, H, dv)), ("norm_w", norm_w, (dv,))):
+    for name, t, shape in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("v", v, (T, H, dv))):
         _need(t, name, shape, q.dtype, dev)
+    _need_prefill_rest(T, H, dk, dv, q.dtype, dev, g, beta, cu_seqlens, state_indices, state_pool, out,
+                       checkpoints, ckpt_offsets, gate, norm_w, has_initial_state, dev_status)
+    return dev
+
+
+def _need_prefill_rest(T, H, dk, dv, dtype, dev, g, beta, cu_seqlens, state_indices, state_pool, out,
+                       checkpoints, ckpt_offsets, gate, norm_w, has_initial_state, dev_status):
+    """The prefill's checks of every tensor but q, k and v."""
+    N = state_indices.shape[0]
+    _one_device(dev, g=g, beta=beta, cu_seqlens=cu_seqlens, state_indices=state_indices,
+                state_pool=state_pool, out=out, checkpoints=checkpoints, ckpt_offsets=ckpt_offsets,
+                gate=gate, norm_w=norm_w, has_initial_state=has_initial_state, dev_status=dev_status)
+    for name, t, shape in (("g", g, (T, H, dk)), ("beta", beta, (T, H)), ("out", out, (T, H, dv)),
+                           ("gate", gate, (T, H, dv)), ("norm_w", norm_w, (dv,))):
+        _need(t, name, shape, dtype, dev)
     _need(cu_seqlens, "cu_seqlens", (N + 1,), torch.int32, dev)
     _need(state_indices, "state_indices", (N,), torch.int32, dev)
     _need(has_initial_state, "has_initial_state", (N,), torch.int32, dev)
@@ -159,7 +177,6 @@ def _need_prefill(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, 
     _need(state_pool, "state_pool", (None, H, dk, dv), None, dev)
     _need(checkpoints, "checkpoints", (None, H, dk, dv), state_pool.dtype, dev)
     _need(dev_status, "dev_status", None, torch.int32, dev)
-    return dev
 
 
 def _dtype(t: torch.Tensor) -> int:
@@ -253,6 +270,51 @@ def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_indices, state_pool,
             _ptr(ckpt_offsets), _ptr(gate), _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk, dv,
             int(chunk), float(scale), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream, dev))
     _check(st, "kda_prefill_chunked")
+
+
+def kda_prefill_chunked_conv(x, conv_w, conv_state_pool, g, beta, cu_seqlens, state_indices, state_pool,
+                             out, *, conv_b=None, conv_act: str = "silu", chunk: int = 64,
+                             checkpoints=None, checkpoint_every: int = 0, ckpt_offsets=None, gate=None,
+                             norm_w=None, eps: float = 1e-6, gate_act: str = "sigmoid",
+                             has_initial_state=None, scale: float = 0.0, workspace=None,
+                             dev_status=None, stream=None):
+    """Short convolution, L2 normalisation of q and k, and the chunked prefill
+    in one pass (see ``include/kda.h``).  ``x`` is the packed projection
+    output [T, 3*H*d] (channels q, then k, then v); conv_w [3*H*d, W];
+    conv_state_pool [slots, W-1, 3*H*d] is updated in place like state_pool.
+    The shapes H, d come from ``g`` [T, H, d]."""
+    T, H, dk = g.shape
+    dev = g.device
+    C3 = 3 * H * dk
+    Wd = conv_w.shape[-1] if conv_w.dim() == 2 else 0
+    _one_device(dev, x=x, conv_w=conv_w, conv_b=conv_b, conv_state_pool=conv_state_pool, beta=beta,
+                cu_seqlens=cu_seqlens, state_indices=state_indices, state_pool=state_pool, out=out,
+                checkpoints=checkpoints, ckpt_offsets=ckpt_offsets, gate=gate, norm_w=norm_w,
+                has_initial_state=has_initial_state, dev_status=dev_status, workspace=workspace)
+    for name, t, shape in (("x", x, (T, C3)), ("conv_w", conv_w, (C3, Wd)), ("conv_b", conv_b, (C3,)),
+                           ("conv_state_pool", conv_state_pool, (None, Wd - 1, C3))):
+        _need(t, name, shape, g.dtype, dev)
+    _need_prefill_rest(T, H, dk, dk, g.dtype, dev, g, beta, cu_seqlens, state_indices, state_pool, out,
+                       checkpoints, ckpt_offsets, gate, norm_w, has_initial_state, dev_status)
+    _need(workspace, "workspace", None, None, dev)
+    N = state_indices.shape[0]
+    cap = checkpoints.shape[0] if checkpoints is not None else 0
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if not x.is_contiguous():
+        raise ValueError("libkda takes contiguous tensors")
+    base = x.data_ptr() if x.numel() > 0 else None
+    part = H * dk * x.element_size()
+    xq, xk, xv = ((None, None, None) if base is None else
+                  (ctypes.c_void_p(base), ctypes.c_void_p(base + part), ctypes.c_void_p(base + 2 * part)))
+    with torch.cuda.device(dev):
+        st = load().kda_prefill_chunked_conv(
+            xq, xk, xv, C3, _ptr(conv_w), _ptr(conv_b), Wd, CONV_ACT[conv_act], _ptr(conv_state_pool),
+            conv_state_pool.shape[0], _ptr(g), _ptr(beta), _dtype(g), _ptr(cu_seqlens), N, T,
+            _ptr(state_indices), _ptr(has_initial_state), _ptr(state_pool), state_pool.shape[0],
+            _dtype(state_pool), _ptr(out), _ptr(checkpoints), int(checkpoint_every), cap,
+            _ptr(ckpt_offsets), _ptr(gate), _ptr(norm_w), float(eps), GATE_ACT[gate_act], H, dk, dk,
+            int(chunk), float(scale), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream, dev))
+    _check(st, "kda_prefill_chunked_conv")
 
 
 def kda_prefill_chunked_static_scratch(q, k, v, g, beta, cu_seqlens, state_indices, state_pool,

@@ -68,17 +68,20 @@ size_t kda_prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int 
   return kda::prefill_workspace_bytes(N, T, H, dk, dv, chunk);
 }
 
-kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, const void* g,
-                               const void* beta, kda_dtype in_dtype, const int32_t* cu_seqlens,
-                               int N, int64_t T, const int32_t* state_indices,
-                               const int32_t* has_initial_state, void* state_pool,
-                               int64_t num_slots, kda_dtype state_dtype, void* out,
-                               void* checkpoints, int32_t checkpoint_every,
-                               int64_t checkpoint_capacity, int32_t* ckpt_offsets,
-                               const void* gate, const void* norm_w, float eps,
-                               kda_gate_act gate_act, int H, int dk, int dv, int chunk,
-                               float scale, void* workspace, size_t workspace_bytes,
-                               int32_t* dev_status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Host-side checks shared by the prefill entry points; on success fills *pp.
+// q, k, v may be NULL here when the caller supplies them another way.
+kda_status prefill_params(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                          kda_dtype in_dtype, const int32_t* cu_seqlens, int N, int64_t T,
+                          const int32_t* state_indices, const int32_t* has_initial_state, void* state_pool,
+                          int64_t num_slots, kda_dtype state_dtype, void* out, void* checkpoints,
+                          int32_t checkpoint_every, int64_t checkpoint_capacity, int32_t* ckpt_offsets,
+                          const void* gate, const void* norm_w, float eps, kda_gate_act gate_act, int H, int dk,
+                          int dv, int chunk, float scale, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, kda::PrefillParams* pp) {
   if (N < 0 || T < 0 || T > INT32_MAX || H <= 0 || H > 65535 || num_slots <= 0) return KDA_ERR_INVALID_ARG;
   if ((int64_t)N * H > INT32_MAX || (T / 16 + N) * (int64_t)H > INT32_MAX) return KDA_ERR_INVALID_ARG;
   if (!dtype_ok(in_dtype) || !dtype_ok(state_dtype)) return KDA_ERR_UNSUPPORTED;
@@ -103,12 +106,8 @@ kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, cons
   }
   const size_t need = kda::prefill_workspace_needed(N, T, H, dk, dv, chunk, in_dtype, gate != nullptr);
   if (need > 0 && (workspace_bytes < need || !ptr_ok(workspace, true))) return KDA_ERR_WORKSPACE;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (N == 0) {
-    if (ckpt_offsets) return from_cuda(cudaMemsetAsync(ckpt_offsets, 0, sizeof(int32_t), st));
-    return KDA_OK;
-  }
-  kda::PrefillParams p{};
+  kda::PrefillParams& p = *pp;
+  p = kda::PrefillParams{};
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
   p.cu_seqlens = cu_seqlens;
   p.state_indices = state_indices;
@@ -129,7 +128,79 @@ kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, cons
   p.gate_act = gate_act;
   p.intra_first_wait_tries = kda::prefill_first_wait_tries(0);
   p.state_first_wait_tries = kda::prefill_first_wait_tries(1);
+  return KDA_OK;
+}
+
+// An empty batch only writes the checkpoint offsets' single entry.
+kda_status launch_or_empty(const kda::PrefillParams& p, int32_t* ckpt_offsets, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.N == 0) {
+    if (ckpt_offsets) return from_cuda(cudaMemsetAsync(ckpt_offsets, 0, sizeof(int32_t), st));
+    return KDA_OK;
+  }
   return from_cuda(kda::launch_prefill(p, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill_chunked(const void* q, const void* k, const void* v, const void* g,
+                               const void* beta, kda_dtype in_dtype, const int32_t* cu_seqlens,
+                               int N, int64_t T, const int32_t* state_indices,
+                               const int32_t* has_initial_state, void* state_pool,
+                               int64_t num_slots, kda_dtype state_dtype, void* out,
+                               void* checkpoints, int32_t checkpoint_every,
+                               int64_t checkpoint_capacity, int32_t* ckpt_offsets,
+                               const void* gate, const void* norm_w, float eps,
+                               kda_gate_act gate_act, int H, int dk, int dv, int chunk,
+                               float scale, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream) {
+  kda::PrefillParams p;
+  const kda_status s = prefill_params(q, k, v, g, beta, in_dtype, cu_seqlens, N, T, state_indices,
+                                      has_initial_state, state_pool, num_slots, state_dtype, out, checkpoints,
+                                      checkpoint_every, checkpoint_capacity, ckpt_offsets, gate, norm_w, eps,
+                                      gate_act, H, dk, dv, chunk, scale, workspace, workspace_bytes, dev_status,
+                                      &p);
+  if (s != KDA_OK) return s;
+  return launch_or_empty(p, ckpt_offsets, stream);
+}
+
+kda_status kda_prefill_chunked_conv(const void* x_q, const void* x_k, const void* x_v, int64_t x_row_stride,
+                                    const void* conv_w, const void* conv_b, int conv_width,
+                                    kda_conv_act conv_act, void* conv_state_pool, int64_t conv_num_slots,
+                                    const void* g, const void* beta, kda_dtype in_dtype,
+                                    const int32_t* cu_seqlens, int N, int64_t T,
+                                    const int32_t* state_indices, const int32_t* has_initial_state,
+                                    void* state_pool, int64_t num_slots, kda_dtype state_dtype, void* out,
+                                    void* checkpoints, int32_t checkpoint_every, int64_t checkpoint_capacity,
+                                    int32_t* ckpt_offsets, const void* gate, const void* norm_w, float eps,
+                                    kda_gate_act gate_act, int H, int dk, int dv, int chunk, float scale,
+                                    void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                    void* stream) {
+  kda::PrefillParams p;
+  const kda_status s = prefill_params(x_q, x_k, x_v, g, beta, in_dtype, cu_seqlens, N, T, state_indices,
+                                      has_initial_state, state_pool, num_slots, state_dtype, out, checkpoints,
+                                      checkpoint_every, checkpoint_capacity, ckpt_offsets, gate, norm_w, eps,
+                                      gate_act, H, dk, dv, chunk, scale, workspace, workspace_bytes, dev_status,
+                                      &p);
+  if (s != KDA_OK) return s;
+  if (kda_prefill_path(dk, dv, chunk, in_dtype) != KDA_PATH_TENSOR_CORES) return KDA_ERR_UNSUPPORTED;
+  if (conv_width < 2 || conv_width > 4) return KDA_ERR_UNSUPPORTED;
+  if (conv_act != KDA_CONV_IDENTITY && conv_act != KDA_CONV_SILU) return KDA_ERR_INVALID_ARG;
+  // rows of the projections start on 16-byte boundaries
+  if (x_row_stride < (int64_t)H * dk || x_row_stride % 8 != 0) return KDA_ERR_INVALID_ARG;
+  if (!ptr_ok(conv_w, true) || !ptr_ok(conv_b, false) || !ptr_ok(conv_state_pool, true) || conv_num_slots <= 0)
+    return KDA_ERR_INVALID_ARG;
+  p.conv = true;
+  p.x_row_stride = x_row_stride;
+  p.conv_w = conv_w;
+  p.conv_b = conv_b;
+  p.conv_pool = conv_state_pool;
+  p.conv_num_slots = conv_num_slots;
+  p.conv_width = conv_width;
+  p.conv_act = conv_act;
+  return launch_or_empty(p, ckpt_offsets, stream);
 }
 
 kda_status kda_decode_step(const void* q, const void* k, const void* v, const void* g,

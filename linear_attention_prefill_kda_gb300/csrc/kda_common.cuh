@@ -120,4 +120,8 @@ __device__ __forceinline__ float gate_actf(float x, int act) {
 // exponent instead of swallowing the small decays that follow a huge one.
 constexpr float kLogDecayFloor = -30.0f;
 
+// eps of the L2 normalisation of q and k in the prefill with the convolution
+// fused in: q <- q / sqrt(|q|^2 + eps).
+constexpr float kConvL2Eps = KDA_CONV_L2_EPS;
+
 }  // namespace kda

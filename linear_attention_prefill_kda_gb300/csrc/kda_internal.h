@@ -105,6 +105,16 @@ struct PrefillParams {
   int gate_act;  // kda_gate_act
   // polls of the first bounded wait of the intra-chunk and of the state kernel
   uint32_t intra_first_wait_tries, state_first_wait_tries;
+  // The short convolution folded into the prefill (kda_prefill_chunked_conv):
+  // q, k, v then point at the projections before the convolution, rows
+  // x_row_stride elements apart; the convolution's taps, bias and cache pool
+  // cover the channels [q | k | v] (3 H d of them).
+  bool conv;
+  int64_t x_row_stride;
+  const void *conv_w, *conv_b;
+  void* conv_pool;
+  int64_t conv_num_slots;
+  int conv_width, conv_act;
 };
 
 // Polls of a bounded on-chip wait before it gives up (mbarrier try_wait polls).

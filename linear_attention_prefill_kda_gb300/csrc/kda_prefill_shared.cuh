@@ -60,7 +60,7 @@ __device__ __forceinline__ bool seq_prologue(const PrefillParams& p, int seq, in
     return false;
   }
   si.slot = p.state_indices[seq];
-  if (si.slot < 0 || si.slot >= p.num_slots) {
+  if (si.slot < 0 || si.slot >= p.num_slots || (p.conv && si.slot >= p.conv_num_slots)) {
     if (si.slot != -1 && threadIdx.x == 0) latch_status(p.dev_status, KDA_DEV_BAD_INDEX);
     si.zero_rows = true;
     return false;

@@ -164,6 +164,18 @@ constexpr uint32_t S_TP = 81920;        // bf16 K-major [128 x 64] (SBO 1024): T
 constexpr uint32_t S_FK = 0, S_FQ = 16384, S_FG = 32768, S_FAKK = 65536, S_FAQK = 81920;
 static_assert(S_MB + (2 * 16 * 17 + 32 * 33) * 4 <= S_KW, "solve scratch overlaps the W operand");
 static_assert(S_RAWK >= S_LOP + 16384 && S_RAWK + 3 * RAW_BYTES <= S_REGION, "raw rows overlap phase-1 operands");
+//  phase 1 with the short convolution fused in: the raw projections x of q,
+//  k and v, each with HALO rows ahead of the chunk (its left context), the
+//  row norms of the convolved q and k, and the taps and bias as fp32
+constexpr int HALO = 3;                 // widest left context (convolution width 4)
+constexpr uint32_t RAWC_ROWS = C + HALO;
+constexpr uint32_t RAWC_BYTES = RAWC_ROWS * RAW_STRIDE;
+constexpr uint32_t S_RAWC = 32768;      // x_k rows -HALO..63; x_q at + RAWC_BYTES, x_v at + 2 RAWC_BYTES
+constexpr uint32_t S_NRM = S_RAWC + 3 * RAWC_BYTES;  // fp32 [2 (k, q)][64 rows][4 column quarters]
+constexpr uint32_t S_TAPS = S_NRM + 2048;            // fp32 [3 (k, q, v)][4 taps][128 channels]
+constexpr uint32_t S_CBIAS = S_TAPS + 3 * 4 * 128 * 4;  // fp32 [3][128]
+static_assert(S_RAWC >= S_LOP + 16384 && S_CBIAS + 3 * 128 * 4 <= S_REGION,
+              "convolution staging overlaps phase-1 operands");
 // per-chunk scalars after the region
 constexpr uint32_t S_BETA = S_REGION;          // fp32 [64]
 constexpr uint32_t S_GM = S_BETA + 256;        // fp32 [128] G at the middle row m
@@ -236,7 +248,7 @@ constexpr LTable make_ltable() {
 }
 __device__ __align__(16) const LTable g_ltable = make_ltable();
 
-template <int DI>
+template <int DI, bool CONV>
 __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p) {
   using namespace intra;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -293,11 +305,14 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
         const int64_t t0 = p.cu_seqlens[i], t1 = p.cu_seqlens[i + 1];
         const int64_t kk = slot - (t0 / C + i);
         const int64_t len = t1 - t0;
-        if (t0 >= 0 && len > 0 && t1 <= p.T && kk * C < len && p.state_indices[i] >= 0 &&
-            p.state_indices[i] < p.num_slots) {
+        const int32_t si = p.state_indices[i];
+        if (t0 >= 0 && len > 0 && t1 <= p.T && kk * C < len && si >= 0 && si < p.num_slots &&
+            (!CONV || si < p.conv_num_slots)) {
           s_misc[0] = i;
           s_misc[1] = (int)kk;
           s_misc[2] = (int)(len - kk * C < C ? len - kk * C : C);
+          s_misc[4] = si;
+          s_misc[5] = p.has_initial_state == nullptr || p.has_initial_state[i] != 0;
         }
       }
       if (who) break;
@@ -311,9 +326,6 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   const int64_t tb = (int64_t)p.cu_seqlens[seq] + (int64_t)s_misc[1] * C;
   uint8_t* ws = reinterpret_cast<uint8_t*>(p.workspace) + (slot * H + head) * (int64_t)WS_BYTES;
 
-  // k, q, g rows of the chunk arrive by coalesced 16-byte asynchronous copies
-  // (a warp moves two whole rows per instruction); v and gate rows, read
-  // later, are prefetched into L2 meanwhile.
   if (warp == 0) {
     tc::tmem_alloc(&s_tmem, 256);
     tc::fence_before_sync();
@@ -326,39 +338,167 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     tc::mbar_arrive_expect_tx(&bar_l, sizeof(LTable));
     tc::bulk_g2s(sm + S_LOP, &g_ltable, sizeof(LTable), &bar_l);
   }
-#pragma unroll
-  for (int s = 0; s < 3 * C * 16 / kThreads; ++s) {
-    const int idx = tid + kThreads * s;
-    const int t = idx >> 10, j = (idx >> 4) & (C - 1), piece = idx & 15;
-    const bf16* base = reinterpret_cast<const bf16*>(t == 0 ? p.k : t == 1 ? p.q : p.g);
-    const bool has = j < n && piece * 8 < DI;  // zero rows past the chunk, zero channels past DI
-    tc::cp_async16(sm + S_RAWK + t * RAW_BYTES + j * RAW_STRIDE + piece * 16,
-                   base + ((tb + (has ? j : 0)) * H + head) * (int64_t)DI + (has ? piece * 8 : 0), has);
-  }
-  tc::cp_async_commit();
-  if (warp >= 1 && warp <= 4) {
-    const int s = tid - 32, t = s / C, j = s % C;  // t = 0: v, 1: gate
-    if (j < n && (t == 0 || p.gate)) {
-      const bf16* base = reinterpret_cast<const bf16*>(t == 0 ? p.v : p.gate);
-      tc::prefetch_l2(base + ((tb + j) * H + head) * (int64_t)DI, DI * 2);
-    }
-  }
-  tc::cp_async_wait_all();
-  __syncthreads();
   const bool valid = r < n;
   const bool vlive = valid && cb < DI;  // this thread's v channels exist
   const int64_t rowoff = ((tb + r) * H + head) * (int64_t)DI + cb;
   const int64_t row0off = (tb * H + head) * (int64_t)DI;  // a row that exists (for zero-filled copies)
-  uint4 kr[4], qr[4];  // k and q of row r, channels [cb, cb + 32) (zero rows past the chunk's end)
-  {
+  // k, q and raw g of row r, channels [cb, cb + 32) (zero rows past the chunk's end)
+  uint4 kr[4], qr[4], gr[4];
+  if constexpr (!CONV) {
+    // k, q, g rows of the chunk arrive by coalesced 16-byte asynchronous
+    // copies (a warp moves two whole rows per instruction); v and gate rows,
+    // read later, are prefetched into L2 meanwhile.
+#pragma unroll
+    for (int s = 0; s < 3 * C * 16 / kThreads; ++s) {
+      const int idx = tid + kThreads * s;
+      const int t = idx >> 10, j = (idx >> 4) & (C - 1), piece = idx & 15;
+      const bf16* base = reinterpret_cast<const bf16*>(t == 0 ? p.k : t == 1 ? p.q : p.g);
+      const bool has = j < n && piece * 8 < DI;  // zero rows past the chunk, zero channels past DI
+      tc::cp_async16(sm + S_RAWK + t * RAW_BYTES + j * RAW_STRIDE + piece * 16,
+                     base + ((tb + (has ? j : 0)) * H + head) * (int64_t)DI + (has ? piece * 8 : 0), has);
+    }
+    tc::cp_async_commit();
+    if (warp >= 1 && warp <= 4) {
+      const int s = tid - 32, t = s / C, j = s % C;  // t = 0: v, 1: gate
+      if (j < n && (t == 0 || p.gate)) {
+        const bf16* base = reinterpret_cast<const bf16*>(t == 0 ? p.v : p.gate);
+        tc::prefetch_l2(base + ((tb + j) * H + head) * (int64_t)DI, DI * 2);
+      }
+    }
+    tc::cp_async_wait_all();
+    __syncthreads();
     const uint8_t* rk = sm + S_RAWK + r * RAW_STRIDE + cb * 2;
-    uint4 gr[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       kr[i] = *reinterpret_cast<const uint4*>(rk + 16 * i);
       qr[i] = *reinterpret_cast<const uint4*>(rk + RAW_BYTES + 16 * i);
       gr[i] = *reinterpret_cast<const uint4*>(rk + 2 * RAW_BYTES + 16 * i);
     }
+  } else {
+    // The short causal convolution ahead of the recurrence ("[Feature][KDA]
+    // Add Kimi K3 KDA execution", "KDA execution" step 2) and the L2
+    // normalisation of q and k per (token, head), in the chunk's prologue:
+    //   y[t, c] = act(bias[c] + sum_{i<W} w[c, i] x[t - (W-1) + i, c])
+    // rounded to bf16, then q, k <- y / sqrt(|y|^2 + eps) rounded to bf16.
+    // The W-1 inputs ahead of the chunk come from the previous chunk of the
+    // same sequence or, for its first chunk, from the sequence's convolution
+    // cache (zero without initial state); the cache itself is rewritten by
+    // the state kernel, after this grid has completed.
+    const int W = p.conv_width, WM = W - 1;
+    const int kk = s_misc[1];
+    const bool init = s_misc[5] != 0;
+    const int64_t HD = (int64_t)H * DI;
+    // channel block of k, q, v (t = 0, 1, 2) within the packed [q | k | v]
+    auto blk = [](int t) { return t == 0 ? 1 : t == 1 ? 0 : 2; };
+    const bf16* cpool = reinterpret_cast<const bf16*>(p.conv_pool) + (int64_t)s_misc[4] * WM * 3 * HD + head * DI;
+    for (int idx = tid; idx < 3 * (int)RAWC_ROWS * 16; idx += kThreads) {
+      const int t = idx / ((int)RAWC_ROWS * 16), jr = (idx >> 4) % (int)RAWC_ROWS, piece = idx & 15;
+      const int j = jr - HALO;  // chunk row
+      const bf16* x = reinterpret_cast<const bf16*>(t == 0 ? p.k : t == 1 ? p.q : p.v) + head * DI;
+      const bf16* src = x + tb * p.x_row_stride;  // a row that exists (for zero-filled copies)
+      bool has = false;
+      if (piece * 8 < DI && j >= -WM && j < n) {
+        if (j >= 0 || kk > 0) {
+          src = x + (tb + j) * p.x_row_stride + piece * 8;
+          has = true;
+        } else if (init) {
+          src = cpool + (int64_t)(WM + j) * 3 * HD + blk(t) * HD + piece * 8;
+          has = true;
+        }
+      }
+      tc::cp_async16(sm + S_RAWC + t * RAWC_BYTES + jr * RAW_STRIDE + piece * 16, src, has);
+    }
+    tc::cp_async_commit();
+    {
+      // raw g of row r straight into registers; gate rows prefetched into L2
+      const uint4* gp = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(p.g) + (vlive ? rowoff : row0off));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) gr[i] = vlive ? __ldg(gp + i) : make_uint4(0u, 0u, 0u, 0u);
+      if (p.gate && warp >= 1 && warp <= 2 && tid - 32 < n)
+        tc::prefetch_l2(reinterpret_cast<const bf16*>(p.gate) + ((tb + tid - 32) * H + head) * (int64_t)DI, DI * 2);
+    }
+    float* s_taps = reinterpret_cast<float*>(sm + S_TAPS);
+    float* s_cbias = reinterpret_cast<float*>(sm + S_CBIAS);
+    {
+      const bf16* cw = reinterpret_cast<const bf16*>(p.conv_w);
+      for (int e = tid; e < 3 * DI * W; e += kThreads) {
+        const int t = e / (DI * W), rem = e - t * DI * W, c = rem / W, i = rem - c * W;
+        s_taps[(t * 4 + i) * 128 + c] = __bfloat162float(cw[(blk(t) * HD + head * DI) * W + rem]);
+      }
+      const bf16* cbias = reinterpret_cast<const bf16*>(p.conv_b);
+      for (int e = tid; e < 3 * DI; e += kThreads) {
+        const int t = e / DI, c = e - t * DI;
+        s_cbias[t * 128 + c] = cbias ? __bfloat162float(cbias[blk(t) * HD + head * DI + c]) : 0.f;
+      }
+    }
+    tc::cp_async_wait_all();
+    __syncthreads();
+    const bool silu = p.conv_act == KDA_CONV_SILU;
+    // convolved channels [c0, c0 + 8) of tensor t at row r, rounded to bf16
+    auto conv8 = [&](int t, int c0, float* y) {
+      const uint8_t* xr = sm + S_RAWC + t * RAWC_BYTES + (r + HALO - WM) * RAW_STRIDE + c0 * 2;
+      const float* bias = s_cbias + t * 128 + c0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) y[u] = bias[u];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (i < W) {
+          float x8[8];
+          unpack_bf8(*reinterpret_cast<const uint4*>(xr + i * RAW_STRIDE), x8);
+          const float* tp = s_taps + (t * 4 + i) * 128 + c0;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) y[u] = fmaf(tp[u], x8[u], y[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float a = silu ? y[u] / (1.f + __expf(-y[u])) : y[u];
+        y[u] = __bfloat162float(__float2bfloat16_rn(a));
+      }
+    };
+    float ssk = 0.f, ssq = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float y[8];
+      if (vlive) {
+        conv8(0, cb + 8 * i, y);
+        kr[i] = pack_bf8(y);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ssk += y[u] * y[u];
+        conv8(1, cb + 8 * i, y);
+        qr[i] = pack_bf8(y);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ssq += y[u] * y[u];
+        // convolved v waits in this block's U0 area of the workspace (written
+        // with U0 only at the end) until the U0 operand is loaded
+        conv8(2, cb + 8 * i, y);
+        *reinterpret_cast<uint4*>(ws + WS_U0 + ((cb + 8 * i) >> 3) * 1024 + r * 16) = pack_bf8(y);
+      } else {
+        kr[i] = qr[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    float* nrm = reinterpret_cast<float*>(sm + S_NRM);
+    nrm[r * 4 + (cb >> 5)] = ssk;
+    nrm[(C + r) * 4 + (cb >> 5)] = ssq;
+    __syncthreads();
+    const float4 nk = *reinterpret_cast<const float4*>(nrm + r * 4);
+    const float4 nq = *reinterpret_cast<const float4*>(nrm + (C + r) * 4);
+    const float ik = 1.f / sqrtf(nk.x + nk.y + nk.z + nk.w + kConvL2Eps);
+    const float iq = 1.f / sqrtf(nq.x + nq.y + nq.z + nq.w + kConvL2Eps);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float y[8];
+      unpack_bf8(kr[i], y);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) y[u] *= ik;
+      kr[i] = pack_bf8(y);
+      unpack_bf8(qr[i], y);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) y[u] *= iq;
+      qr[i] = pack_bf8(y);
+    }
+  }
+  {
     // raw g (floored) -> B operand of the cumulative-sum product
     const __nv_bfloat162 floor2 = __float2bfloat162_rn(kLogDecayFloor);
 #pragma unroll
@@ -539,19 +679,29 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     intra_exact_A(fk, fq, fg, n, reinterpret_cast<float*>(sm + S_FAKK), reinterpret_cast<float*>(sm + S_FAQK));
   }
   // V -> U0 operand (bf16 MN-major [K=j 64 x N=v 128]) by asynchronous 16-byte
-  // copies, once the operand buffer it lands in is no longer read
-  const bf16* gv = reinterpret_cast<const bf16*>(p.v) + (vlive ? rowoff : row0off);
+  // copies, once the operand buffer it lands in is no longer read (with the
+  // convolution fused in, each thread fetches back the convolved v it left in
+  // the workspace)
+  auto load_v = [&]() {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const void* src;
+      if constexpr (CONV)
+        src = ws + WS_U0 + (vlive ? ((cb + 8 * i) >> 3) * 1024 + r * 16 : 0);
+      else
+        src = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(p.v) + (vlive ? rowoff : row0off)) +
+              (vlive ? i : 0);
+      tc::cp_async16(sm + S_VB + mnmaj(cb + 8 * i, r, 2048), src, vlive);
+    }
+    tc::cp_async_commit();
+  };
   float a32[32];
   uint4 kw[4];  // K e^G for row r, channels [cb, cb + 32) (bf16)
   if (!exact) {
     ok = cta_wait(&bar, phase);
     phase ^= 1;
     tc::fence_after_sync();
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      tc::cp_async16(sm + S_VB + mnmaj(cb + 8 * i, r, 2048), reinterpret_cast<const uint4*>(gv) + (vlive ? i : 0),
-                     vlive);
-    tc::cp_async_commit();
+    load_v();
     if (ok) {
       tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, 128 + hh * 32), a32);
       // K e^G = (K e^(G - G_m)) e^(G_m), from the hi + lo operand still in place
@@ -601,13 +751,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
     return;
   }
-  if (exact) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      tc::cp_async16(sm + S_VB + mnmaj(cb + 8 * i, r, 2048), reinterpret_cast<const uint4*>(gv) + (vlive ? i : 0),
-                     vlive);
-    tc::cp_async_commit();
-  }
+  if (exact) load_v();
   float* s_akk = reinterpret_cast<float*>(sm + S_AKK);
   float* s_tf = reinterpret_cast<float*>(sm + S_TF);
   if (side == 0) {
@@ -917,6 +1061,40 @@ __device__ __forceinline__ void store_state_block(TS* blk, const float* s, int q
   }
 }
 
+// The convolution cache of a sequence after the call, for this head's
+// channels of q, k and v: the last W-1 inputs of the extended sequence
+// xe = [old cache rows (W-1, oldest first; zero without initial state); x rows],
+// i.e. xe[len .. len + W-1).  Every read precedes the barrier and every write
+// follows it, so a sequence shorter than W-1 that keeps some of its old rows
+// moves them in place safely.  Called after the intra grid -- the only other
+// reader of the old rows -- has completed.
+template <int DI>
+__device__ void conv_cache_update(const PrefillParams& p, const SeqInfo& si, int head) {
+  constexpr int P = DI / 8;  // 16-byte pieces per head row
+  const int WM = p.conv_width - 1;
+  const int len = (int)(si.t1 - si.t0);
+  const int64_t HD = (int64_t)p.H * DI;
+  const int t = threadIdx.x;
+  const bool mine = t < 3 * WM * P;
+  bf16* slot = reinterpret_cast<bf16*>(p.conv_pool) + (int64_t)si.slot * WM * 3 * HD + head * DI;
+  int b = 0, j = 0, piece = 0;  // block of [q | k | v], cache row, piece of the head row
+  uint4 val = make_uint4(0u, 0u, 0u, 0u);
+  if (mine) {
+    b = t / (WM * P);
+    j = (t / P) % WM;
+    piece = t % P;
+    const int m = len + j;  // position in xe
+    if (m >= WM) {
+      const bf16* x = reinterpret_cast<const bf16*>(b == 0 ? p.q : b == 1 ? p.k : p.v);
+      val = *reinterpret_cast<const uint4*>(x + (si.t0 + m - WM) * p.x_row_stride + head * DI + piece * 8);
+    } else if (si.init) {
+      val = *reinterpret_cast<const uint4*>(slot + (int64_t)m * 3 * HD + b * HD + piece * 8);
+    }
+  }
+  __syncthreads();
+  if (mine) *reinterpret_cast<uint4*>(slot + (int64_t)j * 3 * HD + b * HD + piece * 8) = val;
+}
+
 template <typename TS, int DI>
 __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p) {
   using namespace state;
@@ -993,6 +1171,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     issue_load_main(0);
     issue_load_tail(0);
   }
+  if (p.conv) conv_cache_update<DI>(p, si, head);
   int last_issued = 0, last_landed = -1;  // bulk copies in flight: (last_landed, last_issued]
 
   auto write_sop = [&]() {
@@ -1231,7 +1410,9 @@ size_t prefill_tc_workspace_bytes(int N, int64_t T, int H) {
 
 template <int DI>
 static cudaError_t launch_prefill_tc_d(const PrefillParams& p, cudaStream_t stream) {
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(tcp::kda_intra_kernel<DI>), (int)tcp::intra::SMEM_BYTES);
+  void (*const intra_kernel)(PrefillParams) =
+      p.conv ? tcp::kda_intra_kernel<DI, true> : tcp::kda_intra_kernel<DI, false>;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(intra_kernel), (int)tcp::intra::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const void* sk = p.state_dtype == KDA_F32 ? reinterpret_cast<const void*>(tcp::kda_state_kernel<float, DI>)
                                             : reinterpret_cast<const void*>(tcp::kda_state_kernel<bf16, DI>);
@@ -1241,7 +1422,7 @@ static cudaError_t launch_prefill_tc_d(const PrefillParams& p, cudaStream_t stre
   const bool intra = p.T > 0 && slots > 0;
   if (intra) {
     dim3 g1((unsigned)(slots * p.H));
-    tcp::kda_intra_kernel<DI><<<g1, tcp::kThreads, tcp::intra::SMEM_BYTES, stream>>>(p);
+    intra_kernel<<<g1, tcp::kThreads, tcp::intra::SMEM_BYTES, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

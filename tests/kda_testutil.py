@@ -104,3 +104,45 @@ def oracle_prefill(oracle, d, w, *, ckpt=True, heads=None):
                           eps=d.get("eps", 1e-6), scale=d["scale"],
                           gate_act=d.get("gate_act", "sigmoid"),
                           has_initial_state=d.get("has_initial_state"))
+
+
+def run_prefill_conv(kda, d, w, dev, *, conv_act="silu", ckpt=True):
+    """Run kda_prefill_chunked_conv on inputs ``d`` (CPU tensors, from
+    make_prefill_conv); returns the device tensors (out, pool, checkpoints,
+    offsets, status, conv_pool)."""
+    t = to_dev(d, dev)
+    T = t["x"].shape[0]
+    N = t["state_indices"].shape[0]
+    I = w.checkpoint_every if ckpt else 0
+    cap = max(T // I, 1) if I else 0
+    ck = torch.full((cap, w.H, w.dk, w.dv), float("nan"), device=dev,
+                    dtype=w.state_dtype) if I else None
+    offs = torch.full((N + 1,), -7, dtype=torch.int32, device=dev)
+    out = torch.full((T, w.H, w.dv), float("nan"), device=dev, dtype=w.in_dtype)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_bytes = kda.kda_prefill_workspace_bytes(N, T, w.H, w.dk, w.dv, w.chunk)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if ws_bytes else None
+    kda.kda_prefill_chunked_conv(t["x"], t["conv_w"], t["conv_pool"], t["g"], t["beta"], t["cu_seqlens"],
+                                 t["state_indices"], t["pool"], out, conv_b=t.get("conv_b"),
+                                 conv_act=conv_act, chunk=w.chunk, checkpoints=ck, checkpoint_every=I,
+                                 ckpt_offsets=offs, gate=t.get("gate"), norm_w=t.get("norm_w"),
+                                 eps=d.get("eps", 1e-6), scale=d["scale"],
+                                 gate_act=d.get("gate_act", "sigmoid"),
+                                 has_initial_state=t.get("has_initial_state"), workspace=ws,
+                                 dev_status=status)
+    torch.cuda.synchronize()
+    return out, t["pool"], ck, offs, status, t["conv_pool"]
+
+
+def oracle_prefill_conv(oracle, d, w, *, conv_act="silu", ckpt=True):
+    """oracle.prefill_conv on the same inputs, with every stage's result
+    stored in the inputs' dtype."""
+    T = d["x"].shape[0]
+    x = d["x"].reshape(T, 3, w.H, w.dk)
+    return oracle.prefill_conv(x[:, 0], x[:, 1], x[:, 2], d["conv_w"], d["cu_seqlens"], d["state_indices"],
+                               d["pool"], d["conv_pool"], conv_bias=d.get("conv_b"), conv_act=conv_act,
+                               has_initial_state=d.get("has_initial_state"), dtype=w.in_dtype,
+                               g=d["g"], beta=d["beta"],
+                               checkpoint_every=w.checkpoint_every if ckpt else 0, gate=d.get("gate"),
+                               norm_w=d.get("norm_w"), eps=d.get("eps", 1e-6), scale=d["scale"],
+                               gate_act=d.get("gate_act", "sigmoid"))

@@ -233,6 +233,23 @@ def test_static_scratch_entry_rejects_oversize_on_host(lib):
         None, None, None, 1e-6, 0, 2, 96, 96, 64, 0.0, None, None) == -2
 
 
+def test_prefill_conv_host_checks(lib):
+    """The fused convolution + prefill refuses before touching the device: a
+    width outside 2-4, a shape off the tensor-core path (d = 16, fp32 inputs)
+    as unsupported; a row stride shorter than a head block or not a multiple
+    of 8 elements, an unknown activation, a missing convolution pool or an
+    empty one as invalid."""
+    def call(width=4, act=1, stride=768, dk=128, in_dtype=1, cpool=FAKE, cslots=4):
+        return lib.kda_prefill_chunked_conv(
+            FAKE, FAKE, FAKE, stride, FAKE, None, width, act, cpool, cslots, FAKE, FAKE, in_dtype, FAKE, 1,
+            64, FAKE, None, FAKE, 4, 0, FAKE, None, 0, 0, None, None, None, 1e-6, 0, 2, dk, dk, 64, 0.0,
+            FAKE, 1 << 40, None, None)
+    assert call(width=5) == -2 and call(width=1) == -2
+    assert call(dk=16, stride=96) == -2 and call(in_dtype=0) == -2
+    assert call(stride=100) == -1 and call(stride=260) == -1
+    assert call(act=2) == -1 and call(cpool=None) == -1 and call(cslots=0) == -1
+
+
 def test_binding_rejects_host_tensors_before_any_call():
     """The binding hands bare device pointers to the ABI: host tensors are
     refused with ValueError before the library is called."""
@@ -255,6 +272,10 @@ def test_binding_rejects_host_tensors_before_any_call():
                                              q[None, :1, 0], q[:1, 0]),
         lambda: kda.kda_norm_gate(q, q, q[0, 0], q),
         lambda: kda.kda_norm_gate_ex(q, q, q),
+        lambda: kda.kda_prefill_chunked_conv(torch.zeros(8, 96, dtype=torch.bfloat16),
+                                             torch.zeros(96, 4, dtype=torch.bfloat16),
+                                             torch.zeros(2, 3, 96, dtype=torch.bfloat16), q, b, cu, idx,
+                                             pool, q),
     ]
     for call in calls:
         with _pt.raises(ValueError, match="CUDA tensor"):
@@ -288,6 +309,10 @@ def test_binding_rejects_tensors_on_two_devices():
                                              q[None, :1, 0].to("meta"), q[:1, 0]),
         lambda: kda.kda_norm_gate(q, qm, q[0, 0], q),
         lambda: kda.kda_norm_gate_ex(q, q, qm),
+        lambda: kda.kda_prefill_chunked_conv(torch.zeros(8, 96, dtype=torch.bfloat16),
+                                             torch.zeros(96, 4, dtype=torch.bfloat16),
+                                             torch.zeros(2, 3, 96, dtype=torch.bfloat16), q, b, cu, idx,
+                                             pool, qm),
     ]
     for call in calls:
         with pytest.raises(ValueError, match="one CUDA device"):

@@ -7,8 +7,8 @@ import torch
 
 import oracle
 import workloads as W
-from kda_testutil import (excess_error, max_abs, oracle_prefill, record, run_prefill, to_dev,
-                          tol_for)
+from kda_testutil import (excess_error, max_abs, oracle_prefill, oracle_prefill_conv, record, run_prefill,
+                          run_prefill_conv, to_dev, tol_for)
 
 W_ = W  # the workloads module, for tests whose parameter W is a convolution width
 
@@ -564,6 +564,115 @@ def test_conv_prefill_many_items_per_cta(kda_gpu, dtype, W):
     tol = 1e-5 if dtype == torch.float32 else 1e-3
     assert excess_error(y, y_ref) <= tol
     assert excess_error(t["pool"], p_ref) <= (1e-6 if dtype == torch.float32 else 0.0)
+
+
+def _check_prefill_conv(kda, w, d, conv_act, *, label=None):
+    """The fused convolution + normalisation + prefill against the oracle's
+    pipeline: outputs, states and checkpoints within the tolerance rule, the
+    convolution cache bit-exact (its rows are copies of inputs), checkpoint
+    offsets exact, untouched slots of both pools unchanged."""
+    pool0, cpool0 = d["pool"].clone(), d["conv_pool"].clone()
+    out, pool, ck, offs, status, cpool = run_prefill_conv(kda, d, w, DEV, conv_act=conv_act)
+    assert int(status.item()) == 0, kda.DEV_STATUS[int(status.item())]
+    o_ref, p_ref, ck_ref, offs_ref, c_ref = oracle_prefill_conv(oracle, d, w, conv_act=conv_act)
+    tol = tol_for(w.state_dtype)
+    if label:
+        record(label, "out", out, o_ref)
+    assert excess_error(out, o_ref) <= tol
+    idx = d["state_indices"].tolist()
+    lens = (d["cu_seqlens"][1:] - d["cu_seqlens"][:-1]).tolist()
+    touched = [s for s, L in zip(idx, lens) if s >= 0 and L > 0]
+    pool_cpu, cpool_cpu = pool.cpu(), cpool.cpu()
+    for s in range(w.num_slots):
+        if s in touched:
+            if label:
+                record(label, "final_state", pool_cpu[s], p_ref[s])
+            assert excess_error(pool_cpu[s], p_ref[s]) <= tol, s
+            assert np.array_equal(cpool_cpu[s].double().numpy(), c_ref[s]), f"conv cache of slot {s}"
+        else:
+            assert torch.equal(pool_cpu[s], pool0[s]), f"slot {s} modified"
+            assert torch.equal(cpool_cpu[s], cpool0[s]), f"conv cache of slot {s} modified"
+    if w.checkpoint_every:
+        assert offs.cpu().numpy().tolist() == offs_ref.tolist()
+        real = []
+        for i, s in enumerate(idx):
+            if s >= 0:
+                real.extend(range(int(offs_ref[i]), int(offs_ref[i + 1])))
+        if real:
+            assert excess_error(ck[real], ck_ref[real]) <= tol
+    for i, s in enumerate(idx):
+        if s < 0:  # padding rows exactly zero
+            t0, t1 = int(d["cu_seqlens"][i]), int(d["cu_seqlens"][i + 1])
+            assert torch.count_nonzero(out[t0:t1].float()).item() == 0
+    return out
+
+
+@pytest.mark.parametrize("d,cw,act,state_dtype", [(128, 4, "silu", torch.float32),
+                                                  (128, 3, "none", torch.bfloat16),
+                                                  (64, 2, "silu", torch.float32),
+                                                  (64, 4, "silu", torch.bfloat16)])
+def test_prefill_conv_fused(kda_gpu, d, cw, act, state_dtype):
+    """Convolution widths 2-4 and both activations in front of the tensor-core
+    prefill: lengths shorter than the convolution's context (the cache keeps
+    old rows), chunk edges, an empty and a padding sequence, a mix of
+    initial-state flags (the flag governs both the state and the convolution
+    cache), gate, checkpoints every 64 tokens."""
+    lens = (1, 2, 3, 63, 64, 65, 0, 200, 130, 5)
+    w = W.SCHED.replace(seqlens=lens, H=4, dk=d, dv=d, num_slots=14, slot_range=None,
+                        state_dtype=state_dtype, checkpoint_every=64, seed=900 + d + cw)
+    inp = W.make_prefill_conv(w, cw)
+    inp["state_indices"][8] = -1
+    inp["has_initial_state"] = torch.tensor([1, 0, 1, 1, 0, 1, 1, 1, 0, 1], dtype=torch.int32)
+    _check_prefill_conv(kda_gpu, w, inp, act)
+
+
+def test_prefill_conv_fused_sched_workload(kda_gpu):
+    """The 4096-token scheduler mix at its full width (32 heads of 128) with a
+    width-4 SiLU convolution in front."""
+    w = W.SCHED
+    _check_prefill_conv(kda_gpu, w, W.make_prefill_conv(w, 4), "silu", label=w.name + "_conv4")
+
+
+def test_prefill_conv_fused_equals_the_separate_calls(kda_gpu):
+    """The fused call against the three library calls it replaces, run one
+    after another on the same inputs (convolution, L2 normalisation in torch
+    on the device with bf16 rounding, prefill): the convolution caches agree
+    bit for bit and the outputs within the tolerance."""
+    w = W.VARLEN.replace(dk=128, dv=128, H=4, seqlens=(3, 100, 64, 129), num_slots=8, seed=931)
+    d = W.make_prefill_conv(w, 4)
+    out_f, pool_f, _, _, status, cpool_f = run_prefill_conv(kda_gpu, d, w, DEV, ckpt=False)
+    assert int(status.item()) == 0
+    t = to_dev(d, DEV)
+    T = t["x"].shape[0]
+    y = torch.empty_like(t["x"])
+    kda_gpu.kda_causal_conv1d_prefill(t["x"], t["conv_w"], t["cu_seqlens"], t["state_indices"], t["conv_pool"],
+                                      y, bias=t["conv_b"], act="silu")
+    yq, yk, yv = (y.reshape(T, 3, w.H, w.dk)[:, i].float() for i in range(3))
+    nq = (yq / torch.sqrt((yq * yq).sum(-1, keepdim=True) + 1e-6)).to(w.in_dtype).contiguous()
+    nk = (yk / torch.sqrt((yk * yk).sum(-1, keepdim=True) + 1e-6)).to(w.in_dtype).contiguous()
+    sep = dict(d, q=nq, k=nk, v=yv.to(w.in_dtype).contiguous())
+    sep = {k: v for k, v in sep.items() if k not in ("x", "conv_w", "conv_b", "conv_pool")}
+    sep["pool"] = d["pool"].clone()
+    out_s, pool_s, _, _, status = run_prefill(kda_gpu, sep, w, DEV, ckpt=False)
+    assert int(status.item()) == 0
+    assert torch.equal(cpool_f, t["conv_pool"])
+    assert (out_f.float() - out_s.float()).abs().max().item() <= 0.01
+    assert (pool_f - pool_s).abs().max().item() <= 0.01
+
+
+def test_prefill_conv_bad_conv_slot_latches_status(kda_gpu):
+    """An index inside the state pool but past the convolution pool latches
+    the bad-index status; that sequence's rows are zero and no slot changes."""
+    w = W.VARLEN.replace(dk=64, dv=64, H=2, seqlens=(70, 30), num_slots=6, seed=937)
+    d = W.make_prefill_conv(w, 3)
+    d["conv_pool"] = d["conv_pool"][:4].contiguous()
+    d["state_indices"] = torch.tensor([1, 5], dtype=torch.int32)
+    pool0, cpool0 = d["pool"].clone(), d["conv_pool"].clone()
+    out, pool, _, _, status, cpool = run_prefill_conv(kda_gpu, d, w, DEV, ckpt=False)
+    assert int(status.item()) == 1
+    assert torch.count_nonzero(out[70:].float()).item() == 0
+    assert torch.equal(pool[5].cpu(), pool0[5])
+    assert torch.equal(cpool.cpu()[[0, 2, 3]], cpool0[[0, 2, 3]])
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])

@@ -27,6 +27,7 @@ import torch
 __all__ = [
     "PrefillWorkload", "DecodeWorkload", "TINY", "VARLEN", "SCHED", "LONGPROMPT", "DECODE",
     "make_prefill", "make_decode_pool", "make_decode_step", "sched_lengths", "cu_from_lengths",
+    "make_prefill_conv",
 ]
 
 
@@ -167,6 +168,28 @@ def make_prefill(w: PrefillWorkload, *, lengths: Optional[Sequence[int]] = None,
     d["cu_seqlens"] = cu_from_lengths(lengths)
     d["eps"] = 1e-6
     d["scale"] = 1.0 / math.sqrt(w.dk)
+    return d
+
+
+def make_prefill_conv(w: PrefillWorkload, conv_width: int, *, lengths: Optional[Sequence[int]] = None,
+                      seed=None):
+    """Inputs of the prefill with the short convolution in front: those of
+    make_prefill without q, k, v (the convolution makes them), plus the packed
+    projection x [T, 3*H*dk] ~ N(0, 1) (channels q, then k, then v), taps
+    conv_w [3*H*dk, W] ~ N(0, 0.5^2), bias conv_b [3*H*dk] ~ N(0, 0.1^2) and a
+    convolution cache pool conv_pool [num_slots, W-1, 3*H*dk] ~ N(0, 1), all
+    in ``w.in_dtype``."""
+    d = make_prefill(w, lengths=lengths, seed=seed)
+    for key in ("q", "k", "v"):
+        d.pop(key)
+    gen = torch.Generator().manual_seed(int(w.seed if seed is None else seed) + 7919)
+    C3 = 3 * w.H * w.dk
+    T = int(d["cu_seqlens"][-1])
+    d["x"] = torch.randn(T, C3, generator=gen, dtype=torch.float32).to(w.in_dtype)
+    d["conv_w"] = (0.5 * torch.randn(C3, conv_width, generator=gen, dtype=torch.float32)).to(w.in_dtype)
+    d["conv_b"] = (0.1 * torch.randn(C3, generator=gen, dtype=torch.float32)).to(w.in_dtype)
+    d["conv_pool"] = torch.randn(w.num_slots, conv_width - 1, C3, generator=gen,
+                                 dtype=torch.float32).to(w.in_dtype)
     return d
 
 
