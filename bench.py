@@ -249,6 +249,20 @@ def conv_algorithmic(w, C, Wd):
     return int(2 * w.T * C * 2 + C * (Wd + 1) * 2 + 2 * n_seq * (Wd - 1) * C * 2)
 
 
+def prefill_conv_algorithmic(w, d, Wd):
+    """Bytes and FLOPs of one prefill call with the short convolution fused in:
+    the prefill's (its q, k, v reads are the reads of the packed projection
+    x), plus taps and bias, each sequence's convolution cache read and
+    written, and the convolution's multiply-adds."""
+    b, fl = prefill_algorithmic(w, d)
+    C3 = 3 * w.H * w.dk
+    lens = [int(x) for x in (d["cu_seqlens"][1:] - d["cu_seqlens"][:-1]).tolist()]
+    n_seq = sum(1 for L in lens if L > 0)
+    b += C3 * (Wd + 1) * 2 + 2 * n_seq * (Wd - 1) * C3 * 2
+    fl += 2.0 * w.T * C3 * Wd
+    return int(b), float(fl)
+
+
 # ----------------------------------------------------------------- GPU arm
 def run_gpu(args):
     import linear_attention_prefill_kda_gb300 as kda
@@ -357,6 +371,23 @@ def run_gpu(args):
                                 scale=vd["scale"], workspace=vws, dev_status=status,
                                 stream=stream)
 
+    # ---------------- the scheduler step with a width-4 SiLU convolution and the
+    # q/k normalisation fused into the prefill (packed projection x in, no q/k/v
+    # tensors in between)
+    with_fused = args.workload in ("both", "convfused")
+    if with_fused:
+        fd = W.make_prefill_conv(w, CONV_W)
+        ft = {k: (x.to(dev) if isinstance(x, torch.Tensor) else x) for k, x in fd.items()}
+
+    def fused_call():
+        kda.kda_prefill_chunked_conv(ft["x"], ft["conv_w"], ft["conv_pool"], ft["g"], ft["beta"],
+                                     ft["cu_seqlens"], ft["state_indices"], ft["pool"], out,
+                                     conv_b=ft["conv_b"], conv_act="silu", chunk=w.chunk,
+                                     checkpoints=ck, checkpoint_every=w.checkpoint_every,
+                                     ckpt_offsets=offs, gate=ft["gate"], norm_w=ft["norm_w"],
+                                     eps=fd["eps"], scale=fd["scale"], workspace=wspace,
+                                     dev_status=status, stream=stream)
+
     def conv_call():
         if not with_conv:
             return
@@ -405,6 +436,8 @@ def run_gpu(args):
                 long_call(c)
         if with_varlen:
             varlen_call()
+        if with_fused:
+            fused_call()
     barrier()
 
     def gpu_lead():
@@ -491,6 +524,19 @@ def run_gpu(args):
         barrier()
         var_ms = (sum(a.elapsed_time(b) for a, b in zip(vstarts, vends)) / args.steps
                   if with_varlen else float("nan"))
+        # fused convolution + prefill, each call timed with the L2 flushed before it
+        fstarts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        fends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier()
+        for i in range(args.steps if with_fused else 0):
+            flush.fill_(float(i))
+            gpu_lead()
+            fstarts[i].record(stream)
+            fused_call()
+            fends[i].record(stream)
+        barrier()
+        fused_ms = (sum(a.elapsed_time(b) for a, b in zip(fstarts, fends)) / args.steps
+                    if with_fused else float("nan"))
     clocks = clk.summary()
     st = int(status.item())
     if st != 0:
@@ -499,8 +545,8 @@ def run_gpu(args):
     pre_ms_mean = sum(pre_ms) / len(pre_ms)
     dec_ms = dec_ms_total / args.steps
     spec_ms = spec_ms_total / args.steps if with_spec else float("nan")
-    pre_ms_mean, dec_ms, spec_ms, conv_ms, long_ms, var_ms = max_over_ranks(
-        [pre_ms_mean, dec_ms, spec_ms, conv_ms, long_ms, var_ms], dev)
+    pre_ms_mean, dec_ms, spec_ms, conv_ms, long_ms, var_ms, fused_ms = max_over_ranks(
+        [pre_ms_mean, dec_ms, spec_ms, conv_ms, long_ms, var_ms, fused_ms], dev)
 
     # ---------------- e2e through the public API with host buffers
     # Every step copies its inputs in from pinned host memory and its output
@@ -577,6 +623,8 @@ def run_gpu(args):
     long_bytes, long_flops = prefill_algorithmic(lw_seg, {"cu_seqlens": W.cu_from_lengths([LSEG])})
     long_gbs = rate(long_bytes, long_ms) / 1e9
     conv_gbs = rate(conv_bytes, conv_ms) / 1e9
+    fused_bytes, fused_flops = prefill_conv_algorithmic(w, d, CONV_W)
+    fused_gbs = rate(fused_bytes, fused_ms) / 1e9
     tokens_s = replica_rate(T, ws, pre_ms_mean)
     seqsteps_s = replica_rate(dw.N, ws, dec_ms)
     result = {
@@ -643,6 +691,17 @@ def run_gpu(args):
         "varlen": {"workload": vw.name, "value": round(replica_rate(vw.T, ws, var_ms), 1),
                    "unit": "tokens/s", "ms_per_call": round(var_ms, 4),
                    "path": kda.kda_prefill_path(vw.dk, vw.dv, vw.chunk, vw.in_dtype)},
+        "conv_fused_prefill": {
+            "workload": w.name + "_conv4_silu", "value": round(replica_rate(T, ws, fused_ms), 1),
+            "unit": "tokens/s", "ms_per_call": round(fused_ms, 4),
+            "separate_ms": round(conv_ms + pre_ms_mean, 4),
+            "separate": "the convolution kernel and the prefill timed above, one after the other "
+                        "(the q/k normalisation between them, which the library has no separate "
+                        "kernel for, is not counted)",
+            "roofline": {"bound": "hbm", "achieved": round(fused_gbs, 1), "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": round(fused_gbs / pk["hbm"], 4),
+                         "traffic": recorded_traffic("prefill", "conv_fused_call_dram_bytes"),
+                         "algorithmic_bytes": fused_bytes, "algorithmic_flops": fused_flops}},
         "e2e": {"value": round(replica_rate(T, ws, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipelined": "step i+1's inputs copied in while step i computes and its output "
@@ -650,7 +709,8 @@ def run_gpu(args):
         "gpu_launches": args.steps * (prefill_launches(kda, w) * with_prefill + with_decode
                                       + 2 * with_spec + with_conv
                                       + (lw.T // LSEG) * prefill_launches(kda, lw) * with_long
-                                      + prefill_launches(kda, vw) * with_varlen),
+                                      + prefill_launches(kda, vw) * with_varlen
+                                      + 2 * with_fused),
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -775,7 +835,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["both", "prefill", "decode", "spec", "conv",
-                                           "longprompt", "varlen"],
+                                           "longprompt", "varlen", "convfused"],
                     default="both",
                     help="time every part (default) or one of them (for profiling runs)")
     raw = list(sys.argv[1:] if argv is None else argv)

@@ -120,6 +120,56 @@ __device__ __forceinline__ float gate_actf(float x, int act) {
 // exponent instead of swallowing the small decays that follow a huge one.
 constexpr float kLogDecayFloor = -30.0f;
 
+// SiLU a * sigmoid(a) = a / (1 + 2^(-a log2 e)), from the approximate base-2
+// exponential and reciprocal instructions (each within a few fp32 ulps; the
+// limits come out exactly: 0 for a -> -inf through 1/inf, a for a -> +inf)
+__device__ __forceinline__ float silu_approx(float a) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(a * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return a * r;
+}
+
+// Packed fp32 pair arithmetic (two IEEE round-to-nearest operations in one
+// instruction, sm_100 family): the same results as the scalar forms, half
+// the instructions.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// silu_approx on a pair, with the multiplications and the addition packed.
+__device__ __forceinline__ float2 silu_approx2(float2 a) {
+  const float2 m = fmul2(a, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+  float2 e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.x) : "f"(m.x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.y) : "f"(m.y));
+  const float2 den = fadd2(e, make_float2(1.f, 1.f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.x) : "f"(den.x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.y) : "f"(den.y));
+  return fmul2(a, r);
+}
+
 // eps of the L2 normalisation of q and k in the prefill with the convolution
 // fused in: q <- q / sqrt(|q|^2 + eps).
 constexpr float kConvL2Eps = KDA_CONV_L2_EPS;

@@ -59,67 +59,15 @@ constexpr int kPrefillThreads = 256;  // 8 warps x 8 tokens = one 64-token tile
 constexpr int kCh = 128;              // channels of a prefill CTA
 constexpr int kPV = 4;                // channels per lane (32 lanes x 4)
 
-// SiLU a * sigmoid(a) = a / (1 + 2^(-a log2 e)), from the approximate base-2
-// exponential and reciprocal instructions (each within a few fp32 ulps; the
-// limits come out exactly: 0 for a -> -inf through 1/inf, a for a -> +inf)
-__device__ __forceinline__ float silu_approx(float a) {
-  float e, r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(a * -1.4426950408889634f));
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
-  return a * r;
-}
-
-// Packed fp32 pair arithmetic (two IEEE round-to-nearest operations in one
-// instruction, sm_100 family): the same results as the scalar forms, half
-// the instructions.
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-      " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-
-// The activation on a pair of channels (SiLU as in silu_approx, with the
-// multiplications and the addition packed).
+// The activation on a pair of channels (identity, or SiLU as silu_approx2).
 template <int ACT>
 __device__ __forceinline__ float2 conv_act2(float2 a) {
-  if (ACT != 1) return a;
-  const float2 m = fmul2(a, make_float2(-1.4426950408889634f, -1.4426950408889634f));
-  float2 e, r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.x) : "f"(m.x));
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.y) : "f"(m.y));
-  const float2 den = fadd2(e, make_float2(1.f, 1.f));
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.x) : "f"(den.x));
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.y) : "f"(den.y));
-  return fmul2(a, r);
+  return ACT == 1 ? silu_approx2(a) : a;
 }
 
 template <typename T>
 __device__ __forceinline__ void unpack4(float4 f, float* o) {
   o[0] = f.x; o[1] = f.y; o[2] = f.z; o[3] = f.w;
-}
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Sub-blocks of 128 channels per prefill CTA: two for 16-bit inputs (one
@@ -256,9 +204,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 4) conv_prefill_kernel(ConvPa
 #pragma unroll
   for (int sb = 0; sb < kSplit; ++sb) {
     if (sb == 0)
-      cp_async_wait_group<kSplit - 1>();
+      tc::cp_async_wait_group<kSplit - 1>();
     else
-      cp_async_wait_group<0>();
+      tc::cp_async_wait_group<0>();
     __syncthreads();
     const T* buf = s_buf + sb * kBlk;
     const int c0 = cbase + sb * kCh + lane * kPV;

@@ -117,6 +117,20 @@ __device__ __forceinline__ void unpack_bf8(uint4 u, float* x) {
     x[2 * i + 1] = f.y;
   }
 }
+__device__ __forceinline__ void unpack_bf4(uint2 u, float* x) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+  const float2 a = __bfloat1622float2(p[0]), b = __bfloat1622float2(p[1]);
+  x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+__device__ __forceinline__ uint2 pack_bf4(const float* x) {
+  uint2 u;
+  __nv_bfloat162 h0 = __floats2bfloat162_rn(x[0], x[1]), h1 = __floats2bfloat162_rn(x[2], x[3]);
+  u.x = *reinterpret_cast<uint32_t*>(&h0);
+  u.y = *reinterpret_cast<uint32_t*>(&h1);
+  return u;
+}
+// x <- bf16(x), element-wise (round to nearest even)
+__device__ __forceinline__ void round_bf4(float* x) { unpack_bf4(pack_bf4(x), x); }
 __device__ __forceinline__ void unpack_half8(uint4 u, float* x) {
   const __half2* p = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
@@ -132,6 +146,33 @@ __device__ __forceinline__ void unpack_half8(uint4 u, float* x) {
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, uint32_t tries = kDefaultWaitTries) {
   const bool ok = tc::mbar_wait(bar, parity, tries);
   return __syncthreads_and(ok) != 0;
+}
+
+// For 8 values per lane: inv[j] = 1 / sqrt(sum over the warp's 32 lanes of
+// v[j] + eps), in every lane.  A reduce-scatter (lanes split the 8 sums by
+// halves over lane bits 4, 3, 2, then reduce over bits 1, 0) leaves lane l
+// with the total of row R(l) = 4 b4 + 2 b3 + b2 (b = bits of l); each row's
+// result is then read from the first lane that holds it: 17 shuffles in all.
+__device__ __forceinline__ void warp_rsqrt_sum8(const float (&v)[8], float eps, float (&inv)[8]) {
+  const int lane = threadIdx.x & 31;
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float a4[4], a2[2];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float send = b4 ? v[k] : v[k + 4];
+    a4[k] = (b4 ? v[k + 4] : v[k]) + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float send = b3 ? a4[k] : a4[k + 2];
+    a2[k] = (b3 ? a4[k + 2] : a4[k]) + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  float a1 = (b2 ? a2[1] : a2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? a2[0] : a2[1], 4);
+  a1 += __shfl_xor_sync(0xffffffffu, a1, 2);
+  a1 += __shfl_xor_sync(0xffffffffu, a1, 1);
+  const float mine = rsqrtf(a1 + eps);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) inv[j] = __shfl_sync(0xffffffffu, mine, ((j >> 2) & 1) * 16 + ((j >> 1) & 1) * 8 + (j & 1) * 4);
 }
 
 // =====================================================================
@@ -171,10 +212,8 @@ constexpr int HALO = 3;                 // widest left context (convolution widt
 constexpr uint32_t RAWC_ROWS = C + HALO;
 constexpr uint32_t RAWC_BYTES = RAWC_ROWS * RAW_STRIDE;
 constexpr uint32_t S_RAWC = 32768;      // x_k rows -HALO..63; x_q at + RAWC_BYTES, x_v at + 2 RAWC_BYTES
-constexpr uint32_t S_NRM = S_RAWC + 3 * RAWC_BYTES;  // fp32 [2 (k, q)][64 rows][4 column quarters]
-constexpr uint32_t S_TAPS = S_NRM + 2048;            // fp32 [3 (k, q, v)][4 taps][128 channels]
-constexpr uint32_t S_CBIAS = S_TAPS + 3 * 4 * 128 * 4;  // fp32 [3][128]
-static_assert(S_RAWC >= S_LOP + 16384 && S_CBIAS + 3 * 128 * 4 <= S_REGION,
+                                        // (each row then overwritten by its convolved, normalised value)
+static_assert(S_RAWC >= S_LOP + 16384 && S_RAWC + 3 * RAWC_BYTES <= S_REGION,
               "convolution staging overlaps phase-1 operands");
 // per-chunk scalars after the region
 constexpr uint32_t S_BETA = S_REGION;          // fp32 [64]
@@ -248,8 +287,9 @@ constexpr LTable make_ltable() {
 }
 __device__ __align__(16) const LTable g_ltable = make_ltable();
 
-template <int DI, bool CONV>
+template <int DI, int CW>
 __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p) {
+  constexpr bool CONV = CW > 0;  // short convolution of width CW fused into the prologue
   using namespace intra;
   extern __shared__ __align__(1024) uint8_t sm[];
   float* s_beta = reinterpret_cast<float*>(sm + S_BETA);
@@ -344,6 +384,11 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   const int64_t row0off = (tb * H + head) * (int64_t)DI;  // a row that exists (for zero-filled copies)
   // k, q and raw g of row r, channels [cb, cb + 32) (zero rows past the chunk's end)
   uint4 kr[4], qr[4], gr[4];
+  // with the convolution: its left context, the packed channel count, and
+  // the channel block of k, q, v (t = 0, 1, 2) within the packed [q | k | v]
+  constexpr int WM = CONV ? CW - 1 : 0;
+  const int64_t HD = (int64_t)H * DI;
+  auto blk = [](int t) { return t == 0 ? 1 : t == 1 ? 0 : 2; };
   if constexpr (!CONV) {
     // k, q, g rows of the chunk arrive by coalesced 16-byte asynchronous
     // copies (a warp moves two whole rows per instruction); v and gate rows,
@@ -384,31 +429,39 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     // same sequence or, for its first chunk, from the sequence's convolution
     // cache (zero without initial state); the cache itself is rewritten by
     // the state kernel, after this grid has completed.
-    const int W = p.conv_width, WM = W - 1;
     const int kk = s_misc[1];
     const bool init = s_misc[5] != 0;
-    const int64_t HD = (int64_t)H * DI;
-    // channel block of k, q, v (t = 0, 1, 2) within the packed [q | k | v]
-    auto blk = [](int t) { return t == 0 ? 1 : t == 1 ? 0 : 2; };
     const bf16* cpool = reinterpret_cast<const bf16*>(p.conv_pool) + (int64_t)s_misc[4] * WM * 3 * HD + head * DI;
-    for (int idx = tid; idx < 3 * (int)RAWC_ROWS * 16; idx += kThreads) {
-      const int t = idx / ((int)RAWC_ROWS * 16), jr = (idx >> 4) % (int)RAWC_ROWS, piece = idx & 15;
-      const int j = jr - HALO;  // chunk row
-      const bf16* x = reinterpret_cast<const bf16*>(t == 0 ? p.k : t == 1 ? p.q : p.v) + head * DI;
-      const bf16* src = x + tb * p.x_row_stride;  // a row that exists (for zero-filled copies)
-      bool has = false;
-      if (piece * 8 < DI && j >= -WM && j < n) {
-        if (j >= 0 || kk > 0) {
-          src = x + (tb + j) * p.x_row_stride + piece * 8;
-          has = true;
-        } else if (init) {
-          src = cpool + (int64_t)(WM + j) * 3 * HD + blk(t) * HD + piece * 8;
-          has = true;
+    // a warp copies two rows of 16 pieces per step: rows 2 w + lane/16 + 16 s
+    // of each tensor (67 rows: 5 steps, the last partial)
+    const int piece = lane & 15;
+    const bool plive = piece * 8 < DI;
+#pragma unroll 1
+    for (int t = 0; t < 3; ++t) {
+      const bf16* x = reinterpret_cast<const bf16*>(t == 0 ? p.k : t == 1 ? p.q : p.v) + head * DI + piece * 8;
+      const bf16* cp = cpool + blk(t) * HD + piece * 8;
+      uint8_t* dst = sm + S_RAWC + t * RAWC_BYTES + piece * 16;
+#pragma unroll
+      for (int s8 = 0; s8 < ((int)RAWC_ROWS + 15) / 16; ++s8) {
+        const int jr = 2 * warp + (lane >> 4) + 16 * s8;
+        const int j = jr - HALO;  // chunk row
+        if (jr < (int)RAWC_ROWS) {
+          const bf16* src = x + tb * p.x_row_stride;  // a row that exists (for zero-filled copies)
+          bool has = false;
+          if (plive && j >= -WM && j < n) {
+            if (j >= 0 || kk > 0) {
+              src = x + (tb + j) * p.x_row_stride;
+              has = true;
+            } else if (init) {
+              src = cp + (int64_t)(WM + j) * 3 * HD;
+              has = true;
+            }
+          }
+          tc::cp_async16(dst + jr * RAW_STRIDE, src, has);
         }
       }
-      tc::cp_async16(sm + S_RAWC + t * RAWC_BYTES + jr * RAW_STRIDE + piece * 16, src, has);
+      tc::cp_async_commit();  // one group per tensor: the convolution of k starts while q and v land
     }
-    tc::cp_async_commit();
     {
       // raw g of row r straight into registers; gate rows prefetched into L2
       const uint4* gp = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(p.g) + (vlive ? rowoff : row0off));
@@ -416,86 +469,6 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
       for (int i = 0; i < 4; ++i) gr[i] = vlive ? __ldg(gp + i) : make_uint4(0u, 0u, 0u, 0u);
       if (p.gate && warp >= 1 && warp <= 2 && tid - 32 < n)
         tc::prefetch_l2(reinterpret_cast<const bf16*>(p.gate) + ((tb + tid - 32) * H + head) * (int64_t)DI, DI * 2);
-    }
-    float* s_taps = reinterpret_cast<float*>(sm + S_TAPS);
-    float* s_cbias = reinterpret_cast<float*>(sm + S_CBIAS);
-    {
-      const bf16* cw = reinterpret_cast<const bf16*>(p.conv_w);
-      for (int e = tid; e < 3 * DI * W; e += kThreads) {
-        const int t = e / (DI * W), rem = e - t * DI * W, c = rem / W, i = rem - c * W;
-        s_taps[(t * 4 + i) * 128 + c] = __bfloat162float(cw[(blk(t) * HD + head * DI) * W + rem]);
-      }
-      const bf16* cbias = reinterpret_cast<const bf16*>(p.conv_b);
-      for (int e = tid; e < 3 * DI; e += kThreads) {
-        const int t = e / DI, c = e - t * DI;
-        s_cbias[t * 128 + c] = cbias ? __bfloat162float(cbias[blk(t) * HD + head * DI + c]) : 0.f;
-      }
-    }
-    tc::cp_async_wait_all();
-    __syncthreads();
-    const bool silu = p.conv_act == KDA_CONV_SILU;
-    // convolved channels [c0, c0 + 8) of tensor t at row r, rounded to bf16
-    auto conv8 = [&](int t, int c0, float* y) {
-      const uint8_t* xr = sm + S_RAWC + t * RAWC_BYTES + (r + HALO - WM) * RAW_STRIDE + c0 * 2;
-      const float* bias = s_cbias + t * 128 + c0;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) y[u] = bias[u];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (i < W) {
-          float x8[8];
-          unpack_bf8(*reinterpret_cast<const uint4*>(xr + i * RAW_STRIDE), x8);
-          const float* tp = s_taps + (t * 4 + i) * 128 + c0;
-#pragma unroll
-          for (int u = 0; u < 8; ++u) y[u] = fmaf(tp[u], x8[u], y[u]);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float a = silu ? y[u] / (1.f + __expf(-y[u])) : y[u];
-        y[u] = __bfloat162float(__float2bfloat16_rn(a));
-      }
-    };
-    float ssk = 0.f, ssq = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float y[8];
-      if (vlive) {
-        conv8(0, cb + 8 * i, y);
-        kr[i] = pack_bf8(y);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) ssk += y[u] * y[u];
-        conv8(1, cb + 8 * i, y);
-        qr[i] = pack_bf8(y);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) ssq += y[u] * y[u];
-        // convolved v waits in this block's U0 area of the workspace (written
-        // with U0 only at the end) until the U0 operand is loaded
-        conv8(2, cb + 8 * i, y);
-        *reinterpret_cast<uint4*>(ws + WS_U0 + ((cb + 8 * i) >> 3) * 1024 + r * 16) = pack_bf8(y);
-      } else {
-        kr[i] = qr[i] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    float* nrm = reinterpret_cast<float*>(sm + S_NRM);
-    nrm[r * 4 + (cb >> 5)] = ssk;
-    nrm[(C + r) * 4 + (cb >> 5)] = ssq;
-    __syncthreads();
-    const float4 nk = *reinterpret_cast<const float4*>(nrm + r * 4);
-    const float4 nq = *reinterpret_cast<const float4*>(nrm + (C + r) * 4);
-    const float ik = 1.f / sqrtf(nk.x + nk.y + nk.z + nk.w + kConvL2Eps);
-    const float iq = 1.f / sqrtf(nq.x + nq.y + nq.z + nq.w + kConvL2Eps);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float y[8];
-      unpack_bf8(kr[i], y);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) y[u] *= ik;
-      kr[i] = pack_bf8(y);
-      unpack_bf8(qr[i], y);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) y[u] *= iq;
-      qr[i] = pack_bf8(y);
     }
   }
   {
@@ -542,6 +515,106 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   }
   uint32_t phase = 0;
   ok_l = __syncthreads_and(ok_l) != 0;  // without the L operand no product was issued
+  if constexpr (CONV) {
+    // Convolution, one tensor at a time (k, q, v), while the cumulative-sum
+    // product runs: warp w takes chunk rows 8w .. 8w+7, each lane 4
+    // channels, with the W-1 rows before them in a sliding window; k and q
+    // rows are normalised by a warp reduction over the head's channels.  Each
+    // warp first holds all its input rows in registers; after a barrier the
+    // outputs overwrite the inputs in place.
+    const int c4 = 4 * lane;
+    const bool clive = c4 < DI;  // channels past the head width stay zero
+    const int row0 = 8 * warp;
+    const bool silu = p.conv_act == KDA_CONV_SILU;
+    const bf16* cw = reinterpret_cast<const bf16*>(p.conv_w);
+    const bf16* cbias = reinterpret_cast<const bf16*>(p.conv_b);
+#pragma unroll 1
+    for (int t = 0; t < 3; ++t) {
+      if (t == 0)
+        tc::cp_async_wait_group<2>();
+      else if (t == 1)
+        tc::cp_async_wait_group<1>();
+      else
+        tc::cp_async_wait_group<0>();
+      const int64_t ch = blk(t) * HD + head * DI + (clive ? c4 : 0);  // first channel of this lane
+      // taps w[ch + u][i] as channel pairs (u = 0, 1 and 2, 3): 4 CW
+      // contiguous elements, read as CW 8-byte pieces
+      float2 tp[2][CW], bs[2];
+      {
+        float e[4 * CW];
+#pragma unroll
+        for (int q8 = 0; q8 < CW; ++q8) unpack_bf4(__ldg(reinterpret_cast<const uint2*>(cw + ch * CW) + q8), e + 4 * q8);
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+          tp[0][i] = make_float2(e[0 * CW + i], e[1 * CW + i]);
+          tp[1][i] = make_float2(e[2 * CW + i], e[3 * CW + i]);
+        }
+        float b4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (cbias) unpack_bf4(__ldg(reinterpret_cast<const uint2*>(cbias + ch)), b4);
+        bs[0] = make_float2(b4[0], b4[1]);
+        bs[1] = make_float2(b4[2], b4[3]);
+      }
+      __syncthreads();  // every thread's copies of this tensor have landed
+      uint8_t* xb = sm + S_RAWC + t * RAWC_BYTES + c4 * 2;
+      uint2 xr[8 + WM];  // chunk rows row0 - WM .. row0 + 7 of this lane's channels
+#pragma unroll
+      for (int j = 0; j < 8 + WM; ++j)
+        xr[j] = *reinterpret_cast<const uint2*>(xb + (row0 - WM + j + HALO) * RAW_STRIDE);
+      __syncthreads();  // every warp holds its inputs: outputs may overwrite them
+      float2 win[CW][2];
+      auto unpack_pairs = [](uint2 u, float2* w2) {
+        w2[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        w2[1] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+      };
+#pragma unroll
+      for (int j = 0; j < WM; ++j) unpack_pairs(xr[j], win[j + 1]);
+      float y[8][4], ss[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int i = 0; i + 1 < CW; ++i) {
+          win[i][0] = win[i + 1][0];
+          win[i][1] = win[i + 1][1];
+        }
+        unpack_pairs(xr[j + WM], win[CW - 1]);
+        const bool live = clive && row0 + j < n;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float2 a = bs[h];
+#pragma unroll
+          for (int i = 0; i < CW; ++i) a = ffma2(tp[h][i], win[i][h], a);
+          if (silu) a = silu_approx2(a);
+          y[j][2 * h] = live ? a.x : 0.f;
+          y[j][2 * h + 1] = live ? a.y : 0.f;
+        }
+        round_bf4(y[j]);
+        ss[j] = y[j][0] * y[j][0] + y[j][1] * y[j][1] + y[j][2] * y[j][2] + y[j][3] * y[j][3];
+      }
+      if (t < 2) {
+        // q, k <- y / sqrt(|y|^2 + eps) over the head's channels
+        float inv[8];
+        warp_rsqrt_sum8(ss, kConvL2Eps, inv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) y[j][u] *= inv[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(xb + (row0 + j + HALO) * RAW_STRIDE) = pack_bf4(y[j]);
+    }
+    __syncthreads();
+    // this thread's rows of k and q; its v waits in the block's U0 area of the
+    // workspace (written with U0 only at the end) until the U0 operand is loaded
+    const uint8_t* rk = sm + S_RAWC + (r + HALO) * RAW_STRIDE + cb * 2;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      kr[i] = *reinterpret_cast<const uint4*>(rk + 16 * i);
+      qr[i] = *reinterpret_cast<const uint4*>(rk + RAWC_BYTES + 16 * i);
+      if (vlive)
+        *reinterpret_cast<uint4*>(ws + WS_U0 + ((cb + 8 * i) >> 3) * 1024 + r * 16) =
+            *reinterpret_cast<const uint4*>(rk + 2 * RAWC_BYTES + 16 * i);
+    }
+  }
   bool ok = ok_l && cta_wait(&bar, phase);
   phase ^= 1;
   tc::fence_after_sync();
@@ -1410,8 +1483,10 @@ size_t prefill_tc_workspace_bytes(int N, int64_t T, int H) {
 
 template <int DI>
 static cudaError_t launch_prefill_tc_d(const PrefillParams& p, cudaStream_t stream) {
-  void (*const intra_kernel)(PrefillParams) =
-      p.conv ? tcp::kda_intra_kernel<DI, true> : tcp::kda_intra_kernel<DI, false>;
+  void (*const intra_kernel)(PrefillParams) = !p.conv ? tcp::kda_intra_kernel<DI, 0>
+                                               : p.conv_width == 2 ? tcp::kda_intra_kernel<DI, 2>
+                                               : p.conv_width == 3 ? tcp::kda_intra_kernel<DI, 3>
+                                                                   : tcp::kda_intra_kernel<DI, 4>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(intra_kernel), (int)tcp::intra::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const void* sk = p.state_dtype == KDA_F32 ? reinterpret_cast<const void*>(tcp::kda_state_kernel<float, DI>)
