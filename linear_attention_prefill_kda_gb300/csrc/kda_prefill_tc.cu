@@ -40,7 +40,9 @@
 #include "kda_prefill_shared.cuh"
 #include "kda_tc.cuh"
 
+#include <cuda.h>
 #include <cuda_fp16.h>
+#include <string.h>
 
 namespace kda {
 namespace tcp {
@@ -186,8 +188,11 @@ constexpr uint32_t S_LOP = 16384;       // bf16 K-major [128 x 64] (SBO 1024): L
 //  phase 1 also: raw k, q, g rows of the chunk (rows padded to 272 bytes so
 //  that row-per-lane reads spread over the banks; rows past the end zero)
 constexpr uint32_t RAW_STRIDE = 272;
-constexpr uint32_t RAW_BYTES = 64 * RAW_STRIDE;
-constexpr uint32_t S_RAWK = 32768;      // k rows; q at + RAW_BYTES, g at + 2 RAW_BYTES
+//  phase 1: raw k, q, g rows of the chunk as tensor-map boxes: [k, q, g][channel
+//  half][64 rows][128 bytes], each 128-byte row swizzled (16-byte piece c of a row
+//  at address A sits at piece c ^ ((A >> 7) & 7)); rows past T zero
+constexpr uint32_t S_RAWT = 32768;
+constexpr uint32_t BOX_BYTES = 64 * 128;
 //  phase 2 (decay-weighted K K^T and Q K^T):
 constexpr uint32_t S_AROW_HI = 0;       // bf16 K-major [128 x 128] (SBO 2048): K e^(G-Gm) ; Q e^(G-Gm)
 constexpr uint32_t S_AROW_LO = 32768;
@@ -204,7 +209,8 @@ constexpr uint32_t S_TP = 81920;        // bf16 K-major [128 x 64] (SBO 1024): T
 //  exact path (extreme decay) instead of phase 2:
 constexpr uint32_t S_FK = 0, S_FQ = 16384, S_FG = 32768, S_FAKK = 65536, S_FAQK = 81920;
 static_assert(S_MB + (2 * 16 * 17 + 32 * 33) * 4 <= S_KW, "solve scratch overlaps the W operand");
-static_assert(S_RAWK >= S_LOP + 16384 && S_RAWK + 3 * RAW_BYTES <= S_REGION, "raw rows overlap phase-1 operands");
+static_assert(S_RAWT % 1024 == 0 && S_RAWT >= S_LOP + 16384 && S_RAWT + 6 * BOX_BYTES <= S_REGION,
+              "raw rows overlap phase-1 operands");
 //  phase 1 with the short convolution fused in: the raw projections x of q,
 //  k and v, each with HALO rows ahead of the chunk (its left context), the
 //  row norms of the convolved q and k, and the taps and bias as fp32
@@ -224,6 +230,12 @@ constexpr uint32_t S_EGLM = S_EGM + 512;       // fp32 [128] e^(G_last - G_m)
 constexpr uint32_t S_MISC = S_EGLM + 512;      // int [4]
 constexpr uint32_t SMEM_BYTES = S_MISC + 64;
 }  // namespace intra
+
+// Tensor maps of the k, q and g inputs [T, H, DI] (bf16), each read as boxes
+// of 64 tokens x 1 head x 64 channels with 128-byte swizzle.
+struct RowMaps {
+  CUtensorMap k, q, g;
+};
 
 // Element-wise exact A for chunks with extreme decay (rare): no factorisation.
 // fk, fq: k and q rows (bf16, exact copies); fg: cumulative gate (fp32).
@@ -288,7 +300,7 @@ constexpr LTable make_ltable() {
 __device__ __align__(16) const LTable g_ltable = make_ltable();
 
 template <int DI, int CW>
-__global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p, const __grid_constant__ RowMaps maps) {
   constexpr bool CONV = CW > 0;  // short convolution of width CW fused into the prologue
   using namespace intra;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -298,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   float* s_egm = reinterpret_cast<float*>(sm + S_EGM);
   float* s_eglm = reinterpret_cast<float*>(sm + S_EGLM);
   int* s_misc = reinterpret_cast<int*>(sm + S_MISC);
-  __shared__ __align__(8) uint64_t bar, bar_l, bar_fin;
+  __shared__ __align__(8) uint64_t bar, bar_l, bar_fin, bar_x;
   __shared__ uint32_t s_tmem;
 
   // Thread roles.  A warp may only touch the TMEM lane quarter of its SM
@@ -374,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
     tc::mbar_init(&bar, 1);
     tc::mbar_init(&bar_l, 1);
     tc::mbar_init(&bar_fin, 1);
+    tc::mbar_init(&bar_x, 1);
     tc::mbar_fence_init();
     tc::mbar_arrive_expect_tx(&bar_l, sizeof(LTable));
     tc::bulk_g2s(sm + S_LOP, &g_ltable, sizeof(LTable), &bar_l);
@@ -390,19 +403,19 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
   const int64_t HD = (int64_t)H * DI;
   auto blk = [](int t) { return t == 0 ? 1 : t == 1 ? 0 : 2; };
   if constexpr (!CONV) {
-    // k, q, g rows of the chunk arrive by coalesced 16-byte asynchronous
-    // copies (a warp moves two whole rows per instruction); v and gate rows,
-    // read later, are prefetched into L2 meanwhile.
+    // k, q, g rows of the chunk: one tensor-map box per tensor and 64-channel
+    // half, issued by one thread; v and gate rows, read later, are prefetched
+    // into L2 meanwhile.  Rows of the box past the chunk's end (the next
+    // sequence's tokens) and channels past DI are replaced by zeros when read.
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(&bar_x, 3 * (DI / 64) * BOX_BYTES);
 #pragma unroll
-    for (int s = 0; s < 3 * C * 16 / kThreads; ++s) {
-      const int idx = tid + kThreads * s;
-      const int t = idx >> 10, j = (idx >> 4) & (C - 1), piece = idx & 15;
-      const bf16* base = reinterpret_cast<const bf16*>(t == 0 ? p.k : t == 1 ? p.q : p.g);
-      const bool has = j < n && piece * 8 < DI;  // zero rows past the chunk, zero channels past DI
-      tc::cp_async16(sm + S_RAWK + t * RAW_BYTES + j * RAW_STRIDE + piece * 16,
-                     base + ((tb + (has ? j : 0)) * H + head) * (int64_t)DI + (has ? piece * 8 : 0), has);
+      for (int t = 0; t < 3; ++t)
+#pragma unroll
+        for (int hx = 0; hx < DI / 64; ++hx)
+          tc::tma_load_3d(sm + S_RAWT + (2 * t + hx) * BOX_BYTES, t == 0 ? &maps.k : t == 1 ? &maps.q : &maps.g,
+                          64 * hx, head, (int)tb, &bar_x);
     }
-    tc::cp_async_commit();
     if (warp >= 1 && warp <= 4) {
       const int s = tid - 32, t = s / C, j = s % C;  // t = 0: v, 1: gate
       if (j < n && (t == 0 || p.gate)) {
@@ -410,14 +423,33 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p)
         tc::prefetch_l2(base + ((tb + j) * H + head) * (int64_t)DI, DI * 2);
       }
     }
-    tc::cp_async_wait_all();
-    __syncthreads();
-    const uint8_t* rk = sm + S_RAWK + r * RAW_STRIDE + cb * 2;
+    __syncthreads();  // the barriers are initialised
+    if (!cta_wait(&bar_x, 0, p.intra_first_wait_tries)) {
+      // timed out before any product was issued: let the box and L-operand
+      // copies land (bounded) before the shared memory and TMEM are released
+      if (tid == 0) {
+        latch_status(p.dev_status, KDA_DEV_TIMEOUT);
+        *reinterpret_cast<int*>(ws + WS_TAG) = BLOCK_FAILED;
+        tc::mbar_wait(&bar_x, 0);
+        tc::mbar_wait(&bar_l, 0);
+      }
+      tc::fence_before_sync();
+      __syncthreads();
+      if (warp == 0) tc::tmem_dealloc(s_tmem, 256);
+      return;
+    }
+    const int hx = cb >> 6;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      kr[i] = *reinterpret_cast<const uint4*>(rk + 16 * i);
-      qr[i] = *reinterpret_cast<const uint4*>(rk + RAW_BYTES + 16 * i);
-      gr[i] = *reinterpret_cast<const uint4*>(rk + 2 * RAW_BYTES + 16 * i);
+    for (int t = 0; t < 3; ++t) {
+      const uint32_t row = S_RAWT + (2 * t + hx) * BOX_BYTES + r * 128;
+      const uint32_t sw = ((tc::smem_u32(sm) + row) >> 7) & 7;
+      uint4* dst = t == 0 ? kr : t == 1 ? qr : gr;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t piece = (uint32_t)(((cb & 63) >> 3) + i) ^ sw;
+        const uint4 v = *reinterpret_cast<const uint4*>(sm + row + piece * 16);
+        dst[i] = vlive ? v : make_uint4(0u, 0u, 0u, 0u);
+      }
     }
   } else {
     // The short causal convolution ahead of the recurrence ("[Feature][KDA]
@@ -1481,9 +1513,47 @@ size_t prefill_tc_workspace_bytes(int N, int64_t T, int H) {
   return (size_t)tcp::num_slots_bound(T, N) * (size_t)H * tcp::WS_BYTES;
 }
 
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (no
+// link-time dependence on the driver library).
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// [T, H, DI] bf16 as boxes of 64 channels x 1 head x 64 tokens, 128-byte
+// swizzle, zeros outside the tensor.  The base is 16-byte aligned and the
+// row strides (DI and H*DI elements) are multiples of 16 bytes.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t T, int H, int DI) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)DI, (cuuint64_t)H, (cuuint64_t)T};
+  const cuuint64_t strides[2] = {(cuuint64_t)DI * 2, (cuuint64_t)H * DI * 2};
+  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 template <int DI>
 static cudaError_t launch_prefill_tc_d(const PrefillParams& p, cudaStream_t stream) {
-  void (*const intra_kernel)(PrefillParams) = !p.conv ? tcp::kda_intra_kernel<DI, 0>
+  void (*const intra_kernel)(PrefillParams, tcp::RowMaps) = !p.conv ? tcp::kda_intra_kernel<DI, 0>
                                                : p.conv_width == 2 ? tcp::kda_intra_kernel<DI, 2>
                                                : p.conv_width == 3 ? tcp::kda_intra_kernel<DI, 3>
                                                                    : tcp::kda_intra_kernel<DI, 4>;
@@ -1496,8 +1566,13 @@ static cudaError_t launch_prefill_tc_d(const PrefillParams& p, cudaStream_t stre
   const int64_t slots = tcp::num_slots_bound(p.T, p.N);
   const bool intra = p.T > 0 && slots > 0;
   if (intra) {
+    tcp::RowMaps maps;
+    memset(&maps, 0, sizeof(maps));  // unused with the convolution fused in
+    if (!p.conv && !(encode_rows(&maps.k, p.k, p.T, p.H, DI) && encode_rows(&maps.q, p.q, p.T, p.H, DI) &&
+                     encode_rows(&maps.g, p.g, p.T, p.H, DI)))
+      return cudaErrorInvalidValue;
     dim3 g1((unsigned)(slots * p.H));
-    intra_kernel<<<g1, tcp::kThreads, tcp::intra::SMEM_BYTES, stream>>>(p);
+    intra_kernel<<<g1, tcp::kThreads, tcp::intra::SMEM_BYTES, stream>>>(p, maps);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -132,6 +132,19 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32
       : "memory");
 }
 
+// Tiled tensor copy global -> shared (TMA) of one box of a 3-D tensor map at
+// coordinates (x, y, z), innermost first; completion counted in bytes on the
+// mbarrier.  The map must live in kernel-parameter, constant or global
+// memory; x times the element size must be a multiple of 16 bytes.  Elements
+// outside the tensor are filled with zeros.
+__device__ __forceinline__ void tma_load_3d(void* dst_smem, const void* tmap, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(dst_smem)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
