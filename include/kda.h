@@ -377,7 +377,8 @@ KDA_API void kda_testing_set_first_wait_tries(int32_t tries, int32_t kernels);
  * Which kernels kda_prefill_chunked runs for this shape: KDA_PATH_TENSOR_CORES
  * (an intra-chunk and a state kernel on tcgen05/TMEM; bf16 inputs, dk = dv in
  * {64, 128}, chunk 64), KDA_PATH_CUDA_CORES (one CUDA-core kernel per
- * (sequence, head, 64-column slab), plus a norm-gate pass when gated), or
+ * (sequence, head, 64-column slab), with the norm-gate fused when dv <= 64
+ * and as a second pass when gated with dv = 128), or
  * KDA_PATH_UNSUPPORTED.  A host-side query; no device work.
  */
 #define KDA_PATH_UNSUPPORTED 0

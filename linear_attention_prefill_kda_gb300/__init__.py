@@ -239,11 +239,12 @@ def _dtype_of(dt) -> int:
 
 def prefill_launches(dk: int, dv: int, chunk: int, in_dtype, gate: bool) -> int:
     """Kernel launches one kda_prefill_chunked call makes: the tensor-core path
-    runs an intra-chunk and a state kernel; the CUDA-core path runs one kernel
-    plus a norm-gate pass when gated."""
+    runs an intra-chunk and a state kernel; the CUDA-core path runs one kernel,
+    plus a norm-gate pass when gated with dv = 128 (at dv <= 64 the kernel
+    fuses the norm-gate)."""
     if kda_prefill_path(dk, dv, chunk, in_dtype) == "tensor cores":
         return 2
-    return 2 if gate else 1
+    return 2 if gate and dv > 64 else 1
 
 
 def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, state_indices, state_pool, out, *,

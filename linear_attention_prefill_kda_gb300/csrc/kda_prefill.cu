@@ -41,11 +41,13 @@ cudaError_t set_smem_once(const void* kernel, int bytes) {
   return cudaSuccess;
 }
 
-// The CUDA-core kernel splits dv into slabs of 64 columns, so the norm-gate
-// runs as a second pass.  With bf16 inputs the raw output is kept in fp32
-// scratch (T x H x dv floats) for that pass, so that it is not rounded to
-// bf16 before normalisation.
-static bool needs_o_scratch(int dv, kda_dtype in_dtype) { (void)dv; return in_dtype != KDA_F32; }
+// The CUDA-core kernel splits dv into slabs of 64 columns.  With dv <= 64 one
+// slab holds the whole row and the kernel fuses the norm-gate; with dv = 128
+// it runs as a second pass, and with bf16 inputs the raw output is kept in
+// fp32 scratch (T x H x dv floats) for that pass, so that it is not rounded
+// to bf16 before normalisation.
+static bool gate_fused_simt(int dv) { return dv <= 64; }
+static bool needs_o_scratch(int dv, kda_dtype in_dtype) { return !gate_fused_simt(dv) && in_dtype != KDA_F32; }
 
 size_t prefill_workspace_bytes(int N, int64_t T, int H, int dk, int dv, int chunk) {
   size_t bytes = (size_t)T * (size_t)H * (size_t)dv * sizeof(float);  // raw-output scratch
@@ -72,7 +74,7 @@ cudaError_t launch_prefill(const PrefillParams& p_in, cudaStream_t stream) {
   p.o_scratch = scratch ? reinterpret_cast<float*>(p.workspace) : nullptr;
   cudaError_t e = launch_prefill_simt(p, stream);
   if (e != cudaSuccess) return e;
-  if (p.gate && p.T > 0) {
+  if (p.gate && p.T > 0 && !gate_fused_simt(p.dv)) {
     NormGateParams ng{};
     ng.o = scratch ? static_cast<const void*>(p.o_scratch) : p.out;
     ng.o_f32 = scratch;

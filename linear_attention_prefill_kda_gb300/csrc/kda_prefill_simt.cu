@@ -229,14 +229,36 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(PrefillParams p)
 #pragma unroll
       for (int a = 0; a < RM; ++a) {
         const int r = ty + 16 * a;
+        const int64_t off = ((t0 + c0 + r) * H + head) * DV + v0 + tx * RN;
+        float o[RN];
+#pragma unroll
+        for (int b = 0; b < RN; ++b) o[b] = p.scale * acc[a][b];
+        if constexpr (BV == DV) {
+          // One slab holds the whole row: the output norm-gate is fused here.
+          // Row r's DV columns lie on the 16 threads of this ty (lanes of one
+          // half-warp), so its sum of squares is a 16-lane reduction.
+          if (p.gate) {
+            float ss = 0.f;
+#pragma unroll
+            for (int b = 0; b < RN; ++b) ss += o[b] * o[b];
+#pragma unroll
+            for (int m = 8; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+            const float inv = rsqrtf(ss / (float)DV + p.eps);
+            if (r < n) {
+              const TI* gt = reinterpret_cast<const TI*>(p.gate) + off;
+              const TI* wt = reinterpret_cast<const TI*>(p.norm_w) + tx * RN;
+#pragma unroll
+              for (int b = 0; b < RN; ++b) o[b] *= inv * to_f32(wt[b]) * gate_actf(to_f32(gt[b]), p.gate_act);
+            }
+          }
+        }
         if (r < n) {
-          const int64_t off = ((t0 + c0 + r) * H + head) * DV + v0 + tx * RN;
           if (p.o_scratch) {
 #pragma unroll
-            for (int b = 0; b < RN; ++b) p.o_scratch[off + b] = p.scale * acc[a][b];
+            for (int b = 0; b < RN; ++b) p.o_scratch[off + b] = o[b];
           } else {
 #pragma unroll
-            for (int b = 0; b < RN; ++b) gout[off + b] = from_f32<TI>(p.scale * acc[a][b]);
+            for (int b = 0; b < RN; ++b) gout[off + b] = from_f32<TI>(o[b]);
           }
         }
       }

@@ -332,3 +332,8 @@ def test_prefill_path_query(lib):
     assert kda.kda_prefill_path(96, 96, 64, torch.bfloat16) == "unsupported"
     assert kda.kda_prefill_path(64, 128, 64, torch.bfloat16) == "unsupported"
     assert kda.prefill_launches(64, 64, 64, torch.bfloat16, gate=False) == 2
+    # CUDA-core path: the norm-gate is fused up to dv = 64, a second pass at dv = 128
+    assert kda.prefill_launches(16, 16, 16, torch.float32, gate=True) == 1
+    assert kda.prefill_launches(64, 64, 16, torch.bfloat16, gate=True) == 1
+    assert kda.prefill_launches(128, 128, 64, torch.float32, gate=True) == 2
+    assert kda.prefill_launches(128, 128, 64, torch.float32, gate=False) == 1

@@ -143,6 +143,23 @@ def test_prefill_new_prompts_and_silu_gate(kda_gpu, d, in_dtype, state_dtype):
     _check_prefill(kda_gpu, w, dd)
 
 
+@pytest.mark.parametrize("d,chunk,in_dtype,act", [(16, 64, torch.bfloat16, "silu"),
+                                                  (64, 16, torch.bfloat16, "sigmoid"),
+                                                  (128, 64, torch.float32, "silu"),
+                                                  (128, 16, torch.bfloat16, "sigmoid")])
+def test_prefill_cuda_core_norm_gate(kda_gpu, d, chunk, in_dtype, act):
+    """The CUDA-core prefill's output norm-gate: fused into the kernel where one
+    64-column slab holds the whole row (dv <= 64, one launch), a second pass at
+    dv = 128 (through fp32 scratch for bf16 inputs)."""
+    assert kda_gpu.kda_prefill_path(d, d, chunk, in_dtype) == "cuda cores"
+    assert kda_gpu.prefill_launches(d, d, chunk, in_dtype, True) == (1 if d <= 64 else 2)
+    w = W.SCHED.replace(seqlens=(90, 17, 140), H=3, dk=d, dv=d, chunk=chunk, in_dtype=in_dtype,
+                        checkpoint_every=2 * chunk, num_slots=6, slot_range=None, seed=700 + d + chunk)
+    dd = W.make_prefill(w)
+    dd["gate_act"] = act
+    _check_prefill(kda_gpu, w, dd)
+
+
 def test_prefill_gate_fp32_and_chunk16(kda_gpu):
     w = W.SCHED.replace(seqlens=(100, 37, 256), H=4, dk=64, dv=64, chunk=16, checkpoint_every=32,
                         in_dtype=torch.float32, num_slots=8, slot_range=None, seed=77)
