@@ -16,8 +16,10 @@ Workloads (seeded synthetic inputs, no dataset):
            pool of 16, checkpoints every 64 (a latency-bound correctness case).
 A step is one prefill call, one decode step, one verify + commit, one
 convolution call and the 8 long-prompt calls; each is timed in its own loop
-with CUDA events on the launching stream, the L2 flushed (a 256 MiB write)
-before every timed prefill, convolution and long-prompt call (the decode step
+with CUDA events on the launching stream, the L2 flushed before every timed
+prefill, convolution and long-prompt call: a 256 MiB write, then a read of a
+second 256 MiB buffer, so that the flush's own dirty lines are written back
+before the timer starts rather than inside the timed call (the decode step
 streams 1.07 GB, far above L2).  ``value`` is prefill tokens/s of the
 scheduler step; the other figures sit under ``decode``, ``spec_decode``,
 ``conv_prefill`` and ``longprompt``.  ``e2e`` is scheduler-step prefill
@@ -288,6 +290,13 @@ def run_gpu(args):
     wsb = kda.kda_prefill_workspace_bytes(w.N, T, w.H, w.dk, w.dv, w.chunk)
     wspace = torch.empty(wsb, dtype=torch.uint8, device=dev) if wsb else None
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_read = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2(i):
+        # write a buffer larger than L2, then read another one: the timed call
+        # finds none of its inputs in L2 and no dirty lines left to write back
+        flush.fill_(float(i))
+        torch.sum(flush_read)
     stream = torch.cuda.current_stream()
 
     def prefill_call(src=t, o=out):
@@ -452,7 +461,7 @@ def run_gpu(args):
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         barrier()
         for i in range(args.steps if with_prefill else 0):
-            flush.fill_(float(i))
+            flush_l2(i)
             gpu_lead()
             starts[i].record(stream)
             prefill_call()
@@ -485,7 +494,7 @@ def run_gpu(args):
         cends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         barrier()
         for i in range(args.steps if with_conv else 0):
-            flush.fill_(float(i))
+            flush_l2(i)
             gpu_lead()
             cstarts[i].record(stream)
             conv_call()
@@ -502,7 +511,7 @@ def run_gpu(args):
         for i in range(args.steps if with_long else 0):
             lpool.copy_(lpool0)
             for c in range(ncall):
-                flush.fill_(float(i))
+                flush_l2(i)
                 gpu_lead()
                 lstarts[i * ncall + c].record(stream)
                 long_call(c)
@@ -516,7 +525,7 @@ def run_gpu(args):
         vends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         barrier()
         for i in range(args.steps if with_varlen else 0):
-            flush.fill_(float(i))
+            flush_l2(i)
             gpu_lead()
             vstarts[i].record(stream)
             varlen_call()
@@ -529,7 +538,7 @@ def run_gpu(args):
         fends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         barrier()
         for i in range(args.steps if with_fused else 0):
-            flush.fill_(float(i))
+            flush_l2(i)
             gpu_lead()
             fstarts[i].record(stream)
             fused_call()
@@ -644,7 +653,9 @@ def run_gpu(args):
                    "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
                    "checkpoint_every": w.checkpoint_every, "state_dtype": "f32",
                    "fused_norm_gate": True, "decode_workload": dw.name,
-                   "l2": "flushed (256 MiB write) before each timed prefill call; decode "
+                   "l2": "flushed before each timed prefill call (256 MiB write, then a 256 MiB "
+                         "read of another buffer, so no dirty lines are written back in the timed "
+                         "call); decode "
                          "streams 1.07 GB per step (> L2)",
                    "parallelism": f"replicas x{ws}"},
         "prefill_ms": round(pre_ms_mean, 4),
