@@ -645,9 +645,14 @@ def test_prefill_conv_fused(kda_gpu, d, cw, act, state_dtype):
 
 def test_prefill_conv_fused_sched_workload(kda_gpu):
     """The 4096-token scheduler mix at its full width (32 heads of 128) with a
-    width-4 SiLU convolution in front."""
+    width-4 SiLU convolution in front, with the output norm-gate and without
+    it (the ungated output shows the error before the norm's division by
+    rms(o) amplifies the rare bf16 rounding flips of the intermediate q/k/v)."""
     w = W.SCHED
     _check_prefill_conv(kda_gpu, w, W.make_prefill_conv(w, 4), "silu", label=w.name + "_conv4")
+    wu = w.replace(gate=False)
+    out = _check_prefill_conv(kda_gpu, wu, W.make_prefill_conv(wu, 4), "silu", label=w.name + "_conv4_nogate")
+    assert out.shape == (w.T, w.H, w.dv)
 
 
 def test_prefill_conv_fused_equals_the_separate_calls(kda_gpu):
