@@ -1200,6 +1200,23 @@ __device__ void conv_cache_update(const PrefillParams& p, const SeqInfo& si, int
   if (mine) *reinterpret_cast<uint4*>(slot + (int64_t)j * 3 * HD + b * HD + piece * 8) = val;
 }
 
+// Named barriers of the state kernel (0 is the CTA barrier): the query-side
+// epilogue's row sums (1), the key side after U (2), the query side between
+// staging and storing the output rows (3); 128 threads each.
+constexpr int kBarKey = 2, kBarQuery = 3;
+
+// Barrier over the nthreads threads that reach named barrier id; returns the
+// AND of their predicates.
+__device__ __forceinline__ bool named_barrier_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 template <typename TS, int DI>
 __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p) {
   using namespace state;
@@ -1385,7 +1402,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
       if (k + 1 < nchunks) issue_load_main(k + 1);
     }
     store_pending_ck();
-    bool ok_w = true;
+    // The two halves now run apart until the state product completes: the
+    // key side forms U and meets on its own barrier, after which warp 0
+    // issues the state and output products at once; the query side finishes
+    // the previous chunk's output and stores it meanwhile.
+    bool ok_w = true;  // this side's waits succeeded
     if (qside) {
       // while the P product runs: finish the previous chunk's output rows
       if (k > 0) {
@@ -1400,6 +1421,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
           graw[i] = orow < n ? __ldg(reinterpret_cast<const uint4*>(ws_block(k) + WS_GW + (hh * 8 + i) * 1024 +
                                                                     orow * 16))
                              : make_uint4(0, 0, 0, 0);
+      }
+      if (k > 0) {
+        // the staged rows, re-read row-wise after the query side's barrier:
+        // each instruction of a warp writes two whole 256-byte rows
+        ok_w = named_barrier_and(kBarQuery, 128, ok_w);
+        const int np = min(C, len - (k - 1) * C);
+        const int kw = 2 * (warp >> 2) + (warp & 1);  // 0..3 over the query-side warps
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int row = 16 * kw + 2 * i + (lane >> 4), ch = lane & 15;
+          if (ok_w && row < np && ch * 8 < DI)
+            reinterpret_cast<uint4*>(gout + ((t0 + (int64_t)(k - 1) * C + row) * H + head) * DI)[ch] =
+                *reinterpret_cast<const uint4*>(sm + S_OSTG + row * OSTG_ROW + ch * 16);
+        }
       }
     } else {
       // U = U0 - W S (key-side rows 0-63) -> fp16 MN-major B operand
@@ -1420,44 +1455,38 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
           }
         }
       }
-    }
-    tc::fence_proxy_async();
-    tc::fence_before_sync();
-    ok = __syncthreads_and(ok_w) != 0;
-    if (!ok) break;
-    tc::fence_after_sync();
-    if (tid == 0) {
-      constexpr uint32_t idO = tc::idesc_f16(128, 128, false, false, true);
-      constexpr uint32_t idS = tc::idesc_f16(128, 128, false, true, true);
-      const uint32_t z = tc::smem_u32(st + ST_AQK) - 8192, uo = tc::smem_u32(sm + S_UOP),
-                     kl = tc::smem_u32(st + ST_KLT);
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      ok_w = named_barrier_and(kBarKey, 128, ok_w);
+      if (tid == 0) {
+        if (ok_w) {
+          tc::fence_after_sync();
+          constexpr uint32_t idO = tc::idesc_f16(128, 128, false, false, true);
+          constexpr uint32_t idS = tc::idesc_f16(128, 128, false, true, true);
+          const uint32_t z = tc::smem_u32(st + ST_AQK) - 8192, uo = tc::smem_u32(sm + S_UOP),
+                         kl = tc::smem_u32(st + ST_KLT);
 #pragma unroll
-      for (int kk = 0; kk < C / 16; ++kk)
-        tc::mma_f16(tS, tc::sdesc(kl + kk * 4096, 2048, 128), tc::sdesc(uo + kk * 4096, 2048, 128), idS, kk > 0);
-      tc::mma_commit(&bar_s);
+          for (int kk = 0; kk < C / 16; ++kk)
+            tc::mma_f16(tS, tc::sdesc(kl + kk * 4096, 2048, 128), tc::sdesc(uo + kk * 4096, 2048, 128), idS, kk > 0);
+          tc::mma_commit(&bar_s);
 #pragma unroll
-      for (int kk = 0; kk < C / 16; ++kk)
-        tc::mma_f16(tP, tc::sdesc(z + kk * 256, 128, 1024), tc::sdesc(uo + kk * 4096, 2048, 128), idO, true);
-      tc::mma_commit(&bar_o);
-      // every thread passed the barrier above, so the output product of chunk
-      // k-1 (which the query side waited for) no longer reads the other stage
-      if (k + 1 < nchunks) issue_load_tail(k + 1);
-    }
-    if (!qside && k > 0) {
-      // the previous chunk's output rows, staged by the query side before the
-      // barrier: each instruction of a warp writes two whole 256-byte rows
-      const int np = min(C, len - (k - 1) * C);
-      const int kw = 2 * (warp >> 2) + (warp & 1);  // 0..3 over the key-side warps
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int row = 16 * kw + 2 * i + (lane >> 4), ch = lane & 15;
-        if (row < np && ch * 8 < DI)
-          reinterpret_cast<uint4*>(gout + ((t0 + (int64_t)(k - 1) * C + row) * H + head) * DI)[ch] =
-              *reinterpret_cast<const uint4*>(sm + S_OSTG + row * OSTG_ROW + ch * 16);
+          for (int kk = 0; kk < C / 16; ++kk)
+            tc::mma_f16(tP, tc::sdesc(z + kk * 256, 128, 1024), tc::sdesc(uo + kk * 4096, 2048, 128), idO, true);
+          tc::mma_commit(&bar_o);
+          // the tail copy overwrites the stage of chunk k-1, whose output
+          // product is complete: this thread issued it before this chunk's P
+          // product, and the commit this thread's side waited for (bar_p)
+          // tracks every product it issued earlier
+          if (k + 1 < nchunks) issue_load_tail(k + 1);
+        } else {
+          // no state product: complete its phase so that no thread waits it out
+          tc::mbar_arrive(&bar_s);
+        }
       }
     }
     // ---- state carry: S <- Diag(e^G_last) S + (K e^(G_last-G))^T U ----
-    ok = cta_wait(&bar_s, ph);
+    // (both halves meet here; a failure on either side ends the chain)
+    ok = __syncthreads_and(tc::mbar_wait(&bar_s, ph) && ok_w) != 0;
     if (!ok) break;
     tc::fence_after_sync();
     {
