@@ -63,6 +63,7 @@ constexpr uint32_t WS_GW = 74256;     // fp16 [v/8][64 rows][8]: w * act(gate) (
 constexpr uint32_t WS_BYTES = 90640;
 constexpr uint32_t WS_COPY0 = 65536;  // PA | KLT | U0
 constexpr uint32_t WS_COPY1 = 8720;   // AQK | DECAY | TAG
+static_assert(WS_BYTES % 16 == 0 && WS_COPY0 % 16 == 0 && WS_COPY1 % 16 == 0, "bulk sizes are 16-byte multiples");
 // Block tags.  Every block the state kernel reads is written by one intra
 // CTA of the same call, which stamps it last: a block the intra CTA could not
 // finish is stamped failed, so the chain that reads it stores nothing
@@ -1097,9 +1098,12 @@ constexpr uint32_t S_SOP = 2 * STAGE;    // fp16 MN-major [K=c 128 x N=v 128] (K
 constexpr uint32_t S_UOP = S_SOP + 32768;  // fp16 MN-major [K=j 64 x N=v 128]
 constexpr uint32_t S_NW = S_UOP + 16384;   // fp32 [128]
 constexpr uint32_t S_SS = S_NW + 512;      // fp32 [2 chunk parities][2][64]
-constexpr uint32_t OSTG_ROW = 272;         // padded bf16 output row (256 B + 16)
-constexpr uint32_t S_OSTG = S_SS + 1024;   // bf16 [64][OSTG_ROW]: the finished output rows of a chunk
-constexpr uint32_t SMEM_BYTES = S_OSTG + 64 * OSTG_ROW;
+// bf16 [channel half][64 rows][128 B], each row swizzled like the input boxes
+// (16-byte piece c at piece c ^ ((A >> 7) & 7)): the finished output rows of a
+// chunk, written to the output by tensor-map stores
+constexpr uint32_t S_OSTG = (S_SS + 1024 + 1023) / 1024 * 1024;
+constexpr uint32_t OBOX_BYTES = 64 * 128;
+constexpr uint32_t SMEM_BYTES = S_OSTG + 2 * OBOX_BYTES;
 }  // namespace state
 
 // 8x8 transpose of 16-byte chunks within each group of 8 lanes: before, lane
@@ -1204,6 +1208,8 @@ __device__ void conv_cache_update(const PrefillParams& p, const SeqInfo& si, int
 // epilogue's row sums (1), the key side after U (2), the query side between
 // staging and storing the output rows (3); 128 threads each.
 constexpr int kBarKey = 2, kBarQuery = 3;
+// The query-side thread that issues the output rows' tensor-map stores.
+constexpr int kStoreThread = 64;
 
 // Barrier over the nthreads threads that reach named barrier id; returns the
 // AND of their predicates.
@@ -1218,7 +1224,8 @@ __device__ __forceinline__ bool named_barrier_and(int id, int nthreads, bool pre
 }
 
 template <typename TS, int DI>
-__global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p,
+                                                               const __grid_constant__ CUtensorMap out_map) {
   using namespace state;
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ __align__(8) uint64_t bar_ld[2];
@@ -1331,16 +1338,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     // row partial sums by chunk parity: the buffer of chunk kp is next
     // rewritten in chunk kp + 2, after the barrier of chunk kp + 1
     float* ssb = s_ss + 128 * (kp & 1);
+    // the staging buffer is rewritten only once the previous chunk's tensor
+    // store has read it (its thread waits before the query side's barrier)
+    if (staged && tid == kStoreThread) tc::bulk_wait_read();
     if (p.gate) {
       float ss = 0.f;
 #pragma unroll
       for (int u = 0; u < 64; ++u) ss += o[u] * o[u];
       ssb[hh * 64 + orow] = ss;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
     }
+    if (p.gate || staged) asm volatile("bar.sync 1, 128;" ::: "memory");
     if (ok_o && (staged || (orow < n && hh * 64 < DI))) {
-      uint4* dst = staged ? reinterpret_cast<uint4*>(sm + S_OSTG + orow * OSTG_ROW + hh * 128)
-                          : reinterpret_cast<uint4*>(gout + ((t0 + c0 + orow) * H + head) * DI + hh * 64);
+      const uint32_t srow = S_OSTG + hh * OBOX_BYTES + orow * 128;  // this row's staging line
+      const uint32_t sw = ((tc::smem_u32(sm) + srow) >> 7) & 7;
+      uint4* dst = reinterpret_cast<uint4*>(gout + ((t0 + c0 + orow) * H + head) * DI + hh * 64);
       float inv = 1.f;
       if (p.gate) inv = rsqrtf((ssb[orow] + ssb[64 + orow]) * (1.f / (float)DI) + p.eps);
 #pragma unroll
@@ -1355,7 +1366,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
 #pragma unroll
           for (int u = 0; u < 8; ++u) y[u] = o[8 * i + u];
         }
-        dst[i] = pack_bf8(y);
+        if (staged)
+          *reinterpret_cast<uint4*>(sm + srow + ((i ^ sw) << 4)) = pack_bf8(y);
+        else
+          dst[i] = pack_bf8(y);
       }
     }
   };
@@ -1400,6 +1414,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
         tc::mma_f16(tP, tc::sdesc(pa + kk * 256, 128, 2048), tc::sdesc(so + kk * 4096, 2048, 128), idP, kk > 0);
       tc::mma_commit(&bar_p);
       if (k + 1 < nchunks) issue_load_main(k + 1);
+      // the block two chunks ahead is pulled into L2 now, so that its copy
+      // (issued with the next chunk's product) finds it there
+      if (k + 2 < nchunks) tc::prefetch_l2(ws_block(k + 2), p.gate ? WS_BYTES : WS_COPY0 + WS_COPY1);
     }
     store_pending_ck();
     // The two halves now run apart until the state product completes: the
@@ -1423,17 +1440,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
                              : make_uint4(0, 0, 0, 0);
       }
       if (k > 0) {
-        // the staged rows, re-read row-wise after the query side's barrier:
-        // each instruction of a warp writes two whole 256-byte rows
+        // the staged rows (a full chunk: only the last chunk of a sequence is
+        // partial, and it is stored directly) leave by one tensor-map store
+        // per 64-channel half, issued by one thread once every row is staged
+        tc::fence_proxy_async();
         ok_w = named_barrier_and(kBarQuery, 128, ok_w);
-        const int np = min(C, len - (k - 1) * C);
-        const int kw = 2 * (warp >> 2) + (warp & 1);  // 0..3 over the query-side warps
+        if (ok_w && tid == kStoreThread) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int row = 16 * kw + 2 * i + (lane >> 4), ch = lane & 15;
-          if (ok_w && row < np && ch * 8 < DI)
-            reinterpret_cast<uint4*>(gout + ((t0 + (int64_t)(k - 1) * C + row) * H + head) * DI)[ch] =
-                *reinterpret_cast<const uint4*>(sm + S_OSTG + row * OSTG_ROW + ch * 16);
+          for (int hx = 0; hx < DI / 64; ++hx)
+            tc::tma_store_3d(&out_map, 64 * hx, head, (int)(t0 + (int64_t)(k - 1) * C), sm + S_OSTG + hx * OBOX_BYTES);
+          tc::bulk_commit_group();
         }
       }
     } else {
@@ -1527,6 +1543,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p)
     store_pending_ck();
     store_state_block<DI>(slot_state, S, quad, lane, hh);
   }
+  if (tid == kStoreThread) tc::bulk_wait_all();  // output tensor stores complete before the CTA exits
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
@@ -1618,8 +1635,11 @@ static cudaError_t launch_prefill_tc_d(const PrefillParams& p, cudaStream_t stre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = intra ? 1 : 0;
-  if (p.state_dtype == KDA_F32) return cudaLaunchKernelEx(&cfg, tcp::kda_state_kernel<float, DI>, p);
-  return cudaLaunchKernelEx(&cfg, tcp::kda_state_kernel<bf16, DI>, p);
+  CUtensorMap out_map;
+  memset(&out_map, 0, sizeof(out_map));  // unused without tokens
+  if (p.T > 0 && !encode_rows(&out_map, p.out, p.T, p.H, DI)) return cudaErrorInvalidValue;
+  if (p.state_dtype == KDA_F32) return cudaLaunchKernelEx(&cfg, tcp::kda_state_kernel<float, DI>, p, out_map);
+  return cudaLaunchKernelEx(&cfg, tcp::kda_state_kernel<bf16, DI>, p, out_map);
 }
 
 cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {

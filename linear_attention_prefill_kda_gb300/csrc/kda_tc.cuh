@@ -149,6 +149,21 @@ __device__ __forceinline__ void tma_load_3d(void* dst_smem, const void* tmap, in
       : "memory");
 }
 
+// Tiled tensor copy shared -> global (TMA store) of one box of a 3-D tensor
+// map at (x, y, z), tracked by the issuing thread's bulk async-groups.  The
+// same coordinate rules as the load; elements outside the tensor are not
+// written.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, int x, int y, int z, const void* src_smem) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap),
+               "r"(x), "r"(y), "r"(z), "r"(smem_u32(src_smem))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every bulk store of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every bulk store of this thread is complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
