@@ -1453,7 +1453,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p,
         }
       }
     } else {
-      // U = U0 - W S (key-side rows 0-63) -> fp16 MN-major B operand
+      // U = U0 - W S (key-side rows 0-63) -> fp16 MN-major B operand; this
+      // row's U0 is read while the P product runs
+      uint4 u0h[8];
+#pragma unroll
+      for (int g8 = 0; g8 < 8; ++g8)
+        u0h[g8] = *reinterpret_cast<const uint4*>(st + ST_U0 + ((hh * 64 + 8 * g8) >> 3) * 1024 + lrow * 16);
       ok_w = __all_sync(0xffffffffu, tc::mbar_wait(&bar_p, ph));
       tc::fence_after_sync();
       if (ok_w) {
@@ -1464,7 +1469,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p,
           tc::tmem_ld32(tc::tmem_addr(tP, 32 * quad, cb), ws32);
 #pragma unroll
           for (int g8 = 0; g8 < 4; ++g8) {
-            unpack_half8(*reinterpret_cast<const uint4*>(st + ST_U0 + ((cb + 8 * g8) >> 3) * 1024 + lrow * 16), u0);
+            unpack_half8(u0h[4 * part + g8], u0);
 #pragma unroll
             for (int u = 0; u < 8; ++u) u0[u] -= ws32[8 * g8 + u];
             *reinterpret_cast<uint4*>(sm + S_UOP + mnmaj(cb + 8 * g8, lrow, 2048)) = pack_half8(u0);
