@@ -348,24 +348,29 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
     for (int base = 0; base < p.N; base += 32) {
       const int i = base + lane;
       bool mine = false;
+      // every lane's sequence bounds, slot index and flag are read at once
+      int64_t t0 = 0, t1 = 0;
+      int32_t si = -1;
+      bool init = true;
       if (i < p.N) {
-        const int64_t t0 = p.cu_seqlens[i];
-        const int64_t nx = i + 1 < p.N ? (int64_t)p.cu_seqlens[i + 1] / C + i + 1 : INT64_MAX;
+        t0 = p.cu_seqlens[i];
+        t1 = p.cu_seqlens[i + 1];
+        si = p.state_indices[i];
+        if (CONV && p.has_initial_state) init = p.has_initial_state[i] != 0;
+        const int64_t nx = i + 1 < p.N ? t1 / C + i + 1 : INT64_MAX;
         mine = t0 / C + i <= slot && slot < nx;
       }
       const unsigned who = __ballot_sync(0xffffffffu, mine);
       if (mine) {
-        const int64_t t0 = p.cu_seqlens[i], t1 = p.cu_seqlens[i + 1];
         const int64_t kk = slot - (t0 / C + i);
         const int64_t len = t1 - t0;
-        const int32_t si = p.state_indices[i];
         if (t0 >= 0 && len > 0 && t1 <= p.T && kk * C < len && si >= 0 && si < p.num_slots &&
             (!CONV || si < p.conv_num_slots)) {
           s_misc[0] = i;
           s_misc[1] = (int)kk;
           s_misc[2] = (int)(len - kk * C < C ? len - kk * C : C);
           s_misc[4] = si;
-          s_misc[5] = p.has_initial_state == nullptr || p.has_initial_state[i] != 0;
+          s_misc[5] = init;
         }
       }
       if (who) break;
@@ -741,14 +746,19 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) {
+      // hi x [B_hi | B_lo] as one N = 128 product (the lo rows of the right
+      // operand follow its hi rows in shared memory): hi*hi in TMEM columns
+      // 128-191, hi*lo in 192-255; then lo x B_hi onto columns 128-191.  The
+      // read-out adds the two column blocks.
+      constexpr uint32_t idA2 = tc::idesc_f16(128, 128, true, false, false);
       constexpr uint32_t idA = tc::idesc_f16(128, 64, true, false, false);
+      static_assert(S_BCOL_LO == S_BCOL_HI + 64 * 256, "the lo rows of the right operand follow its hi rows");
       const uint32_t ah = tc::smem_u32(sm + S_AROW_HI), al = tc::smem_u32(sm + S_AROW_LO);
-      const uint32_t bh = tc::smem_u32(sm + S_BCOL_HI), bl = tc::smem_u32(sm + S_BCOL_LO);
+      const uint32_t bh = tc::smem_u32(sm + S_BCOL_HI);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t o = kk * 256;
-        tc::mma_f16(tmem + 128, tc::sdesc(ah + o, 128, 2048), tc::sdesc(bh + o, 128, 2048), idA, kk > 0);
-        tc::mma_f16(tmem + 128, tc::sdesc(ah + o, 128, 2048), tc::sdesc(bl + o, 128, 2048), idA, true);
+        tc::mma_f16(tmem + 128, tc::sdesc(ah + o, 128, 2048), tc::sdesc(bh + o, 128, 2048), idA2, kk > 0);
         tc::mma_f16(tmem + 128, tc::sdesc(al + o, 128, 2048), tc::sdesc(bh + o, 128, 2048), idA, true);
       }
       tc::mma_commit(&bar);
@@ -810,6 +820,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
     load_v();
     if (ok) {
       tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, 128 + hh * 32), a32);
+      {
+        float b32[32];  // the hi*lo block
+        tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, 192 + hh * 32), b32);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) a32[u] += b32[u];
+      }
       // K e^G = (K e^(G - G_m)) e^(G_m), from the hi + lo operand still in place
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
