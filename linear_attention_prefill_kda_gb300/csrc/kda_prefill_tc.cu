@@ -204,8 +204,8 @@ constexpr uint32_t S_REGION = 98304;
 constexpr uint32_t S_AKK = 0;           // fp32 [64][65]   beta-scaled strictly-lower A
 constexpr uint32_t S_TF = 16640;        // fp32 [64][65]   (I + A)^-1
 constexpr uint32_t S_MB = 33280;        // fp32 [2][16][17] + [32][33] block products of the solve
-constexpr uint32_t S_KW = 49152;        // bf16 MN-major [K=j 64 x N=c 128]: K e^G
-constexpr uint32_t S_VB = 65536;        // bf16 MN-major [K=j 64 x N=v 128]: V
+constexpr uint32_t S_KW = 49152;        // bf16 MN-major [K=j 64 x N=256] (K stride 4096): K e^G in N = 0-127,
+constexpr uint32_t S_VB = S_KW + 2048;  //   V in N = 128-255 (one right operand for W and U0)
 constexpr uint32_t S_TP = 81920;        // bf16 K-major [128 x 64] (SBO 1024): T Diag(beta), rows 64-127 zero
 //  exact path (extreme decay) instead of phase 2:
 constexpr uint32_t S_FK = 0, S_FQ = 16384, S_FG = 32768, S_FAKK = 65536, S_FAQK = 81920;
@@ -807,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
       else
         src = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(p.v) + (vlive ? rowoff : row0off)) +
               (vlive ? i : 0);
-      tc::cp_async16(sm + S_VB + mnmaj(cb + 8 * i, r, 2048), src, vlive);
+      tc::cp_async16(sm + S_VB + mnmaj(cb + 8 * i, r, 4096), src, vlive);
     }
     tc::cp_async_commit();
   };
@@ -899,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
   }
   // K e^G -> W operand (bf16 MN-major [K=j 64 x N=c 128])
 #pragma unroll
-  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(sm + S_KW + mnmaj(cb + 8 * i, r, 2048)) = kw[i];
+  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(sm + S_KW + mnmaj(cb + 8 * i, r, 4096)) = kw[i];
   __syncthreads();
   // ---- T = (I + A)^-1 on all eight warps ----
   if (warp < 4 && lane < 16) {
@@ -1057,16 +1057,13 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  // ---- W = T' (K e^G) -> TMEM cols 0-127 ; U0 = T' V -> cols 128-255 ----
+  // ---- [W | U0] = T' [K e^G | V] -> TMEM cols 0-127 | 128-255, one N = 256 product ----
   if (tid == 0) {
-    constexpr uint32_t idW = tc::idesc_f16(128, 128, true, false, true);
-    const uint32_t ta = tc::smem_u32(sm + S_TP), kwb = tc::smem_u32(sm + S_KW), vb = tc::smem_u32(sm + S_VB);
+    constexpr uint32_t idW = tc::idesc_f16(128, 256, true, false, true);
+    const uint32_t ta = tc::smem_u32(sm + S_TP), kwb = tc::smem_u32(sm + S_KW);
 #pragma unroll
-    for (int kk = 0; kk < C / 16; ++kk) {
-      const uint64_t a = tc::sdesc(ta + kk * 256, 128, 1024);
-      tc::mma_f16(tmem, a, tc::sdesc(kwb + kk * 4096, 2048, 128), idW, kk > 0);
-      tc::mma_f16(tmem + 128, a, tc::sdesc(vb + kk * 4096, 2048, 128), idW, kk > 0);
-    }
+    for (int kk = 0; kk < C / 16; ++kk)
+      tc::mma_f16(tmem, tc::sdesc(ta + kk * 256, 128, 1024), tc::sdesc(kwb + kk * 8192, 4096, 128), idW, kk > 0);
     tc::mma_commit(&bar);
   }
   ok = cta_wait(&bar, phase);
