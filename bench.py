@@ -517,8 +517,8 @@ def run_gpu(args):
                 long_call(c)
                 lends[i * ncall + c].record(stream)
         barrier()
-        long_ms = (sum(a.elapsed_time(b) for a, b in zip(lstarts, lends)) / (args.steps * ncall)
-                   if with_long else float("nan"))
+        long_list = [a.elapsed_time(b) for a, b in zip(lstarts, lends)] if with_long else []
+        long_ms = sum(long_list) / (args.steps * ncall) if with_long else float("nan")
         # varlen (a latency-bound correctness workload): each call timed with
         # the L2 flushed before it
         vstarts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -544,12 +544,16 @@ def run_gpu(args):
             fused_call()
             fends[i].record(stream)
         barrier()
-        fused_ms = (sum(a.elapsed_time(b) for a, b in zip(fstarts, fends)) / args.steps
-                    if with_fused else float("nan"))
+        fused_list = [a.elapsed_time(b) for a, b in zip(fstarts, fends)] if with_fused else []
+        fused_ms = sum(fused_list) / args.steps if with_fused else float("nan")
     clocks = clk.summary()
     st = int(status.item())
     if st != 0:
         raise RuntimeError(f"device status {st}: {kda.DEV_STATUS.get(st)}")
+
+    def spread(ms):  # min / median / max of the per-call times of one rank (diagnostic)
+        v = sorted(x for x in ms if x == x)
+        return [round(v[0], 4), round(v[len(v) // 2], 4), round(v[-1], 4)] if v else None
 
     pre_ms_mean = sum(pre_ms) / len(pre_ms)
     dec_ms = dec_ms_total / args.steps
@@ -659,6 +663,7 @@ def run_gpu(args):
                          "streams 1.07 GB per step (> L2)",
                    "parallelism": f"replicas x{ws}"},
         "prefill_ms": round(pre_ms_mean, 4),
+        "prefill_ms_spread": spread(pre_ms),
         "roofline": {"bound": "hbm", "achieved": round(pre_gbs, 1), "peak": pk["hbm"],
                      "unit": "GB/s", "frac": round(pre_gbs / pk["hbm"], 4),
                      "traffic": recorded_traffic("prefill", "prefill_call_dram_bytes"),
@@ -689,7 +694,7 @@ def run_gpu(args):
                                       "algorithmic_bytes": conv_bytes}},
         "longprompt": {"workload": lw.name, "value": round(replica_rate(LSEG, ws, long_ms), 1),
                        "unit": "tokens/s", "calls": lw.T // LSEG, "tokens_per_call": LSEG,
-                       "ms_per_call": round(long_ms, 4), "state_dtype": "bf16",
+                       "ms_per_call": round(long_ms, 4), "ms_spread": spread(long_list), "state_dtype": "bf16",
                        "checkpoint_every": lw.checkpoint_every,
                        "roofline": {"bound": "hbm", "achieved": round(long_gbs, 1),
                                     "peak": pk["hbm"], "unit": "GB/s",
@@ -704,7 +709,7 @@ def run_gpu(args):
                    "path": kda.kda_prefill_path(vw.dk, vw.dv, vw.chunk, vw.in_dtype)},
         "conv_fused_prefill": {
             "workload": w.name + "_conv4_silu", "value": round(replica_rate(T, ws, fused_ms), 1),
-            "unit": "tokens/s", "ms_per_call": round(fused_ms, 4),
+            "unit": "tokens/s", "ms_per_call": round(fused_ms, 4), "ms_spread": spread(fused_list),
             "separate_ms": round(conv_ms + pre_ms_mean, 4),
             "separate": "the convolution kernel and the prefill timed above, one after the other "
                         "(the q/k normalisation between them, which the library has no separate "
