@@ -339,10 +339,25 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
   // completion (griddepcontrol.wait) before reading the workspace.
   asm volatile("griddepcontrol.launch_dependents;");
 
+  // TMEM, the barriers and the L-operand copy do not depend on the chunk:
+  // warp 0 and thread 0 set them up while warp 1 looks the chunk up
+  if (warp == 0) {
+    tc::tmem_alloc(&s_tmem, 256);
+    tc::fence_before_sync();
+  }
+  if (tid == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::mbar_init(&bar_l, 1);
+    tc::mbar_init(&bar_fin, 1);
+    tc::mbar_init(&bar_x, 1);
+    tc::mbar_fence_init();
+    tc::mbar_arrive_expect_tx(&bar_l, sizeof(LTable));
+    tc::bulk_g2s(sm + S_LOP, &g_ltable, sizeof(LTable), &bar_l);
+  }
   // ---- locate (sequence, chunk) of this slot: sequence i owns the slots
   //      [first(i), first(i+1)) with first(i) = cu[i]/C + i (strictly
-  //      increasing in i); warp 0 scans 32 sequences per step ----
-  if (warp == 0) {
+  //      increasing in i); warp 1 scans 32 sequences per step ----
+  if (warp == 1) {
     if (lane == 0) s_misc[0] = -1;
     __syncwarp();
     for (int base = 0; base < p.N; base += 32) {
@@ -371,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
           s_misc[2] = (int)(len - kk * C < C ? len - kk * C : C);
           s_misc[4] = si;
           s_misc[5] = init;
+          s_misc[6] = (int)t0;  // cu_seqlens values are int32
         }
       }
       if (who) break;
@@ -379,25 +395,23 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
   }
   __syncthreads();
   const int seq = s_misc[0];
-  if (seq < 0) return;
-  const int n = s_misc[2];
-  const int64_t tb = (int64_t)p.cu_seqlens[seq] + (int64_t)s_misc[1] * C;
-  uint8_t* ws = reinterpret_cast<uint8_t*>(p.workspace) + (slot * H + head) * (int64_t)WS_BYTES;
-
-  if (warp == 0) {
-    tc::tmem_alloc(&s_tmem, 256);
+  if (seq < 0) {
+    // no chunk in this slot: the L-operand copy lands (bounded wait) before
+    // the shared memory and TMEM are released
+    if (tid == 0) tc::mbar_wait(&bar_l, 0);
     tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(s_tmem, 256);
+    return;
   }
-  if (tid == 0) {
-    tc::mbar_init(&bar, 1);
-    tc::mbar_init(&bar_l, 1);
-    tc::mbar_init(&bar_fin, 1);
-    tc::mbar_init(&bar_x, 1);
-    tc::mbar_fence_init();
-    tc::mbar_arrive_expect_tx(&bar_l, sizeof(LTable));
-    tc::bulk_g2s(sm + S_LOP, &g_ltable, sizeof(LTable), &bar_l);
-  }
+  const int n = s_misc[2];
+  const int64_t tb = (int64_t)s_misc[6] + (int64_t)s_misc[1] * C;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(p.workspace) + (slot * H + head) * (int64_t)WS_BYTES;
   const bool valid = r < n;
+  // beta of row r, read now so that its latency overlaps the row copies
+  const float beta_r = (hh == 0 && side == 0 && valid)
+                           ? __bfloat162float(reinterpret_cast<const bf16*>(p.beta)[(tb + r) * H + head])
+                           : 0.f;
   const bool vlive = valid && cb < DI;  // this thread's v channels exist
   const int64_t rowoff = ((tb + r) * H + head) * (int64_t)DI + cb;
   const int64_t row0off = (tb * H + head) * (int64_t)DI;  // a row that exists (for zero-filled copies)
@@ -520,8 +534,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
       *reinterpret_cast<uint4*>(sm + S_GOP + mnmaj(cb + 8 * i, r, 2048)) = gr[i];
     }
   }
-  if (hh == 0 && side == 0)
-    s_beta[r] = valid ? __bfloat162float(reinterpret_cast<const bf16*>(p.beta)[(tb + r) * H + head]) : 0.f;
+  if (hh == 0 && side == 0) s_beta[r] = beta_r;
   tc::fence_proxy_async();
   tc::fence_before_sync();
   __syncthreads();
