@@ -671,9 +671,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
   tc::fence_after_sync();
   const int m = min(C / 2 - 1, n - 1);
   // tcgen05.ld is warp-collective (.sync.aligned): whole warps load, and only
-  // the lanes of rows m and n-1 store.
+  // the lanes of rows m and n-1 store; every thread keeps its G row slice
+  // for the operand build
+  float g32[32];
   if (ok) {
-    float g32[32];
     tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, cb), g32);
     if (r == m) {
 #pragma unroll
@@ -708,8 +709,6 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
   // is redone on the exact path below (these values are then discarded).
   {
     bool big = false;
-    float g32[32];
-    tc::tmem_ld32(tc::tmem_addr(tmem, lane_base, cb), g32);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int c0 = cb + 8 * i;
