@@ -118,6 +118,13 @@ def test_roofline_numerators_match_hand_counts():
     expect = 4 * T * H * dd * 2 + T * H * 2 + T * H * dd * 2 + 2 * H * bstate + 16 * H * bstate
     assert expect == 186_908_672
     assert b.prefill_algorithmic(lw, {"cu_seqlens": W.cu_from_lengths([4096])})[0] == expect
+    # the scheduler step with the width-4 convolution fused in: the prefill's
+    # bytes (the packed projection x replaces q, k, v, the same size), taps and
+    # bias of 3 x 32 x 128 channels, 8 convolution caches of 3 rows read and
+    # written
+    expect = 262_406_400 + C * 5 * 2 + 2 * 8 * 3 * C * 2
+    assert expect == 263_708_928
+    assert b.prefill_conv_algorithmic(w, d, 4)[0] == expect
 
 
 def test_prefill_flop_count_matches_hand_count():
