@@ -236,6 +236,7 @@ constexpr uint32_t SMEM_BYTES = S_MISC + 64;
 // of 64 tokens x 1 head x 64 channels with 128-byte swizzle.
 struct RowMaps {
   CUtensorMap k, q, g;
+  CUtensorMap v, gate;  // L2 prefetches of the rows read later (gate: zero without a gate)
 };
 
 // Element-wise exact A for chunks with extreme decay (rare): no factorisation.
@@ -436,11 +437,11 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
           tc::tma_load_3d(sm + S_RAWT + (2 * t + hx) * BOX_BYTES, t == 0 ? &maps.k : t == 1 ? &maps.q : &maps.g,
                           64 * hx, head, (int)tb, &bar_x);
     }
-    if (warp >= 1 && warp <= 4) {
-      const int s = tid - 32, t = s / C, j = s % C;  // t = 0: v, 1: gate
-      if (j < n && (t == 0 || p.gate)) {
-        const bf16* base = reinterpret_cast<const bf16*>(t == 0 ? p.v : p.gate);
-        tc::prefetch_l2(base + ((tb + j) * H + head) * (int64_t)DI, DI * 2);
+    if (tid == 0) {
+#pragma unroll
+      for (int hx = 0; hx < DI / 64; ++hx) {
+        tc::tma_prefetch_3d(&maps.v, 64 * hx, head, (int)tb);
+        if (p.gate) tc::tma_prefetch_3d(&maps.gate, 64 * hx, head, (int)tb);
       }
     }
     __syncthreads();  // the barriers are initialised
@@ -519,8 +520,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_intra_kernel(PrefillParams p,
       const uint4* gp = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(p.g) + (vlive ? rowoff : row0off));
 #pragma unroll
       for (int i = 0; i < 4; ++i) gr[i] = vlive ? __ldg(gp + i) : make_uint4(0u, 0u, 0u, 0u);
-      if (p.gate && warp >= 1 && warp <= 2 && tid - 32 < n)
-        tc::prefetch_l2(reinterpret_cast<const bf16*>(p.gate) + ((tb + tid - 32) * H + head) * (int64_t)DI, DI * 2);
+      if (p.gate && tid == 0) {
+#pragma unroll
+        for (int hx = 0; hx < DI / 64; ++hx) tc::tma_prefetch_3d(&maps.gate, 64 * hx, head, (int)tb);
+      }
     }
   }
   {
@@ -1643,10 +1646,11 @@ static cudaError_t launch_prefill_tc_d(const PrefillParams& p, cudaStream_t stre
   const bool intra = p.T > 0 && slots > 0;
   if (intra) {
     tcp::RowMaps maps;
-    memset(&maps, 0, sizeof(maps));  // unused with the convolution fused in
+    memset(&maps, 0, sizeof(maps));  // k, q, v unused with the convolution fused in, gate without a gate
     if (!p.conv && !(encode_rows(&maps.k, p.k, p.T, p.H, DI) && encode_rows(&maps.q, p.q, p.T, p.H, DI) &&
-                     encode_rows(&maps.g, p.g, p.T, p.H, DI)))
+                     encode_rows(&maps.g, p.g, p.T, p.H, DI) && encode_rows(&maps.v, p.v, p.T, p.H, DI)))
       return cudaErrorInvalidValue;
+    if (p.gate && !encode_rows(&maps.gate, p.gate, p.T, p.H, DI)) return cudaErrorInvalidValue;
     dim3 g1((unsigned)(slots * p.H));
     intra_kernel<<<g1, tcp::kThreads, tcp::intra::SMEM_BYTES, stream>>>(p, maps);
     e = cudaGetLastError();
