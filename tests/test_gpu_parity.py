@@ -643,6 +643,21 @@ def test_prefill_conv_fused(kda_gpu, d, cw, act, state_dtype):
     _check_prefill_conv(kda_gpu, w, inp, act)
 
 
+def test_prefill_conv_fused_many_sequences(kda_gpu):
+    """70 sequences of 0-130 tokens (the chunk lookup steps past 32 sequences;
+    many are shorter than the convolution's context), width 3, d = 64, bf16
+    state, a mix of initial-state flags and two padding sequences."""
+    gen = torch.Generator().manual_seed(951)
+    lens = [int(x) for x in torch.randint(0, 131, (70,), generator=gen)]
+    lens[3], lens[40] = 1, 2
+    w = W.VARLEN.replace(seqlens=tuple(lens), H=2, dk=64, dv=64, num_slots=80, state_dtype=torch.bfloat16,
+                         checkpoint_every=64, seed=952)
+    d = W.make_prefill_conv(w, 3)
+    d["state_indices"][[10, 55]] = -1
+    d["has_initial_state"] = (torch.arange(70) % 3 != 0).to(torch.int32)
+    _check_prefill_conv(kda_gpu, w, d, "silu")
+
+
 def test_prefill_conv_fused_sched_workload(kda_gpu):
     """The 4096-token scheduler mix at its full width (32 heads of 128) with a
     width-4 SiLU convolution in front, with the output norm-gate and without
