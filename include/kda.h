@@ -313,7 +313,9 @@ KDA_API kda_status kda_causal_conv1d_decode(const void* x, const void* weight, c
  *                 state_indices as the state pool and read as initial context
  *                 under the same has_initial_state flag; rewritten with each
  *                 sequence's last W-1 extended inputs (an empty sequence or a
- *                 padding index leaves its slot alone).
+ *                 padding index leaves its slot alone, and so does a sequence
+ *                 whose chain latched an error: its state slot and its cache
+ *                 slot are both left as they were).
  * Other arguments as for kda_prefill_chunked (same workspace size).  Supported
  * only where kda_prefill_path reports KDA_PATH_TENSOR_CORES (bf16 inputs,
  * dk = dv in {64, 128}, chunk 64); otherwise KDA_ERR_UNSUPPORTED, as for W

@@ -1204,7 +1204,8 @@ __device__ __forceinline__ void store_state_block(TS* blk, const float* s, int q
 // i.e. xe[len .. len + W-1).  Every read precedes the barrier and every write
 // follows it, so a sequence shorter than W-1 that keeps some of its old rows
 // moves them in place safely.  Called after the intra grid -- the only other
-// reader of the old rows -- has completed.
+// reader of the old rows -- has completed, and only once the sequence's chain
+// has succeeded and its state is stored.
 template <int DI>
 __device__ void conv_cache_update(const PrefillParams& p, const SeqInfo& si, int head) {
   constexpr int P = DI / 8;  // 16-byte pieces per head row
@@ -1328,7 +1329,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p,
     issue_load_main(0);
     issue_load_tail(0);
   }
-  if (p.conv) conv_cache_update<DI>(p, si, head);
   int last_issued = 0, last_landed = -1;  // bulk copies in flight: (last_landed, last_issued]
 
   auto write_sop = [&]() {
@@ -1575,6 +1575,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p,
   } else {
     store_pending_ck();
     store_state_block<DI>(slot_state, S, quad, lane, hh);
+    // the sequence's convolution cache advances only with its state: a chain
+    // that failed leaves both as they were
+    if (p.conv) conv_cache_update<DI>(p, si, head);
   }
   if (tid == kStoreThread) tc::bulk_wait_all();  // output tensor stores complete before the CTA exits
   tc::fence_before_sync();
