@@ -883,3 +883,62 @@ def test_graph_capture_replay(kda_gpu, dim):
     graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, out_e) and torch.equal(dout, dout_e) and torch.equal(t["pool"], pool_e)
+
+
+def test_graph_capture_replay_conv_fused(kda_gpu):
+    """The fused convolution prefill captured in a CUDA graph, gated and with
+    checkpoints: one replay equals an eager call, and a second replay carries
+    both pools updated in place (the recurrent state and the convolution cache)
+    exactly like a second eager call.  The first sequence is shorter than the
+    convolution's context, so its cache keeps old rows and moves on with every
+    call."""
+    w = W.VARLEN.replace(dk=128, dv=128, H=4, seqlens=(2, 100, 64, 129), num_slots=8,
+                         checkpoint_every=64, gate=True, seed=961)
+    d = W.make_prefill_conv(w, 4)
+    t = to_dev(d, DEV)
+    T = t["x"].shape[0]
+    out = torch.empty(T, w.H, w.dv, device=DEV, dtype=w.in_dtype)
+    ck = torch.zeros(T // 64, w.H, w.dk, w.dv, device=DEV, dtype=w.state_dtype)
+    offs = torch.zeros(w.N + 1, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    wsb = kda_gpu.kda_prefill_workspace_bytes(w.N, T, w.H, w.dk, w.dv, w.chunk)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=DEV)
+    pool0, cpool0 = t["pool"].clone(), t["conv_pool"].clone()
+
+    def step(stream=None):
+        kda_gpu.kda_prefill_chunked_conv(t["x"], t["conv_w"], t["conv_pool"], t["g"], t["beta"],
+                                         t["cu_seqlens"], t["state_indices"], t["pool"], out,
+                                         conv_b=t["conv_b"], conv_act="silu", chunk=w.chunk,
+                                         checkpoints=ck, checkpoint_every=64, ckpt_offsets=offs,
+                                         gate=t["gate"], norm_w=t["norm_w"], eps=d.get("eps", 1e-6),
+                                         scale=d["scale"], workspace=ws, dev_status=status,
+                                         stream=stream)
+
+    eager = []
+    for _ in range(2):
+        step()
+        torch.cuda.synchronize()
+        eager.append((out.clone(), t["pool"].clone(), t["conv_pool"].clone(), ck.clone()))
+    assert int(status.item()) == 0
+    slot = int(d["state_indices"][0])
+    assert not torch.equal(eager[0][2][slot], eager[1][2][slot])  # the second call moved that cache on
+    t["pool"].copy_(pool0)
+    t["conv_pool"].copy_(cpool0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            step(stream=s)
+    torch.cuda.synchronize()
+    t["pool"].copy_(pool0)
+    t["conv_pool"].copy_(cpool0)
+    for i in range(2):
+        out.zero_()
+        ck.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        o_e, p_e, c_e, k_e = eager[i]
+        assert torch.equal(out, o_e) and torch.equal(t["pool"], p_e), i
+        assert torch.equal(t["conv_pool"], c_e) and torch.equal(ck, k_e), i
+    assert int(status.item()) == 0
