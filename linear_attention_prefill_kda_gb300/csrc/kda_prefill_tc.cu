@@ -1446,7 +1446,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p,
       // (issued with the next chunk's product) finds it there
       if (k + 2 < nchunks) tc::prefetch_l2(ws_block(k + 2), p.gate ? WS_BYTES : WS_COPY0 + WS_COPY1);
     }
-    store_pending_ck();
     // The two halves now run apart until the state product completes: the
     // key side forms U and meets on its own barrier, after which warp 0
     // issues the state and output products at once; the query side finishes
@@ -1480,6 +1479,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p,
           tc::bulk_commit_group();
         }
       }
+      // a pending checkpoint leaves once this side's rows are out, while the
+      // key side forms U
+      store_pending_ck();
     } else {
       // U = U0 - W S (key-side rows 0-63) -> fp16 MN-major B operand; this
       // row's U0 is read while the P product runs
@@ -1532,6 +1534,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p,
           tc::mbar_arrive(&bar_s);
         }
       }
+      // a pending checkpoint leaves while the state product runs, off U's path
+      store_pending_ck();
     }
     // ---- state carry: S <- Diag(e^G_last) S + (K e^(G_last-G))^T U ----
     // (both halves meet here; a failure on either side ends the chain)
@@ -1550,7 +1554,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_kernel(PrefillParams p,
     }
     // checkpoint after every checkpoint_every tokens of this segment; the
     // registers keep this state until the next chunk's update, so the store is
-    // issued there, overlapping that chunk's first product
+    // issued there, where each side waits anyway (the key side for the state
+    // product, the query side for the key side)
     if (si.ckpt_ok && p.checkpoint_every > 0 && (c0 + n) % p.checkpoint_every == 0)
       pending_ck = si.ckpt_off + (c0 + n) / p.checkpoint_every - 1;
     write_sop();
