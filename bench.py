@@ -309,6 +309,8 @@ def run_gpu(args):
 
     # ---------------- decode
     dw = W.DECODE
+    if args.decode_sequences:  # a smaller case of the same shape, for single-launch captures
+        dw = W.DECODE.replace(N=args.decode_sequences, num_slots=4 * args.decode_sequences)
     with_decode = args.workload in ("both", "decode")
     with_prefill = args.workload in ("both", "prefill")
     with_spec = args.workload in ("both", "spec")
@@ -656,7 +658,7 @@ def run_gpu(args):
         "config": {"workload": w.name, "prefill_tokens": T, "sequences": list(w.seqlens),
                    "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
                    "checkpoint_every": w.checkpoint_every, "state_dtype": "f32",
-                   "fused_norm_gate": True, "decode_workload": dw.name,
+                   "fused_norm_gate": True, "decode_workload": dw.name, "decode_sequences": dw.N,
                    "l2": "flushed before each timed prefill call (256 MiB write, then a 256 MiB "
                          "read of another buffer, so no dirty lines are written back in the timed "
                          "call); decode "
@@ -854,6 +856,10 @@ def main(argv=None):
                                            "longprompt", "varlen", "convfused"],
                     default="both",
                     help="time every part (default) or one of them (for profiling runs)")
+    ap.add_argument("--decode-sequences", type=int, default=0,
+                    help="sequences of the decode and verification workloads (default: the workload's "
+                         "256), with a pool of four slots per sequence: a smaller case of the same "
+                         "kernels for single-launch profiler captures")
     raw = list(sys.argv[1:] if argv is None else argv)
     args = ap.parse_args(raw)
     if args.warmup < 3:
