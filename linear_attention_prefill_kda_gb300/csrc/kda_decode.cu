@@ -50,7 +50,9 @@ decode_kernel(DecodeParams p) {
   const int cg = tid % CG, rg = tid / CG;
 
   extern __shared__ __align__(16) uint8_t s_next[];  // the next row's state, prefetched
-  __shared__ float s_q[DK], s_k[DK], s_a[DK];
+  // q, k and the decay of a row, by row parity: a row's are written before
+  // the barrier that starts it, while the previous row's may still be read
+  __shared__ float s_qb[2][DK], s_kb[2][DK], s_ab[2][DK];
   __shared__ float s_pk[RG][DV], s_pq[RG][DV];
   __shared__ float s_qk;
   __shared__ __align__(8) uint64_t bar_pf;
@@ -69,10 +71,14 @@ decode_kernel(DecodeParams p) {
   bool pf = false;           // this row's state is being prefetched into s_next
   bool prefetching = true;   // turned off for good after a wait that gave up
   bool in_flight = false;    // a copy that gave up may still land (drained at the end)
-  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+  int par = 0;               // row parity of this CTA's walk
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, par ^= 1) {
     const int seq = (int)(row / p.H), head = (int)(row % p.H);
     const int32_t slot = p.state_indices[seq];
     const bool valid = slot_ok(slot);
+    float* s_q = s_qb[par];
+    float* s_k = s_kb[par];
+    float* s_a = s_ab[par];
     // Issue the state loads first: they are the whole cost of the step.
     float4 st[RPT];
     bool ok = true;
@@ -85,8 +91,16 @@ decode_kernel(DecodeParams p) {
       }
 #pragma unroll
       for (int m = 0; m < RPT; ++m) st[m] = load4(src + (rg + m * RG) * DV + cg * 4);
+      const TI* q = reinterpret_cast<const TI*>(p.q) + row * DK;
+      const TI* k = reinterpret_cast<const TI*>(p.k) + row * DK;
+      const TI* g = reinterpret_cast<const TI*>(p.g) + row * DK;
+      for (int i = tid; i < DK; i += blockDim.x) {
+        s_q[i] = to_f32(q[i]);
+        s_k[i] = to_f32(k[i]);
+        s_a[i] = expf(to_f32(g[i]));
+      }
     }
-    // every thread has read s_next (and the inputs of the previous row); a
+    // every thread has read s_next and written this row's q, k and decay; a
     // wait that gave up (its copy may still land) ends the prefetching
     const bool all_ok = __syncthreads_and(ok) != 0;
     if (!all_ok && pf) {
@@ -117,15 +131,6 @@ decode_kernel(DecodeParams p) {
     if (head == 0) check_duplicate_slot(p.state_indices, seq, slot, p.dev_status);
     TS* S = state_block(slot, row);
 
-    const TI* q = reinterpret_cast<const TI*>(p.q) + row * DK;
-    const TI* k = reinterpret_cast<const TI*>(p.k) + row * DK;
-    const TI* g = reinterpret_cast<const TI*>(p.g) + row * DK;
-    for (int i = tid; i < DK; i += blockDim.x) {
-      s_q[i] = to_f32(q[i]);
-      s_k[i] = to_f32(k[i]);
-      s_a[i] = expf(to_f32(g[i]));
-    }
-    __syncthreads();
     if (tid < 32) {
       float acc = 0.f;
       for (int i = tid; i < DK; i += 32) acc += s_q[i] * s_k[i];
